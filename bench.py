@@ -1,0 +1,488 @@
+#!/usr/bin/env python3
+"""Benchmark of one continuous-batching step of paged GQA attention on GB300.
+
+A step is the whole hot path for every layer of the model: kv_append of all
+new tokens (one per decode sequence plus the prefill chunk), paged decode
+attention over every decode sequence's cache (split-K main + reduce), and a
+chunked-prefill attention of the chunk over itself and its prior cache.
+
+Default workload: the ragged continuous batch -- 32 layers, 32 query / 8 KV
+heads, head_dim 128, bf16 cache in 16-token blocks, 128 decode sequences at
+seeded log-uniform context in [128, 32768], plus one 2,048-token prefill chunk
+over 4,096 cached tokens.  Every layer has its own pools (about 3.1 GB per
+layer, far larger than L2), so no L2 flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  `value` is achieved algorithmic HBM GB/s of
+the whole step; decode tokens/s and prefill TFLOP/s ride along.  The
+`reference` arm times the fp64 CPU oracle on a bounded sample of the same
+workload (the pages ship no runnable implementation of this path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from paged_kv_cache_104_gb300 import workloads as W  # noqa: E402
+
+METRIC = "paged GQA decode attn: achieved HBM GB/s (% of GB300 peak); decode tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# --------------------------------------------------------------------------- accounting
+def step_accounting(w: W.Workload, lay: W.Layout):
+    """Algorithmic bytes and flops of one step (all layers).
+
+    decode: every stored K and V row of every decode sequence read once (the
+            GQA group is resident), plus q read and out written;
+    append: new K/V rows read and written once;
+    prefill: the chunk's q read and out written, and the K/V of the sequence
+            (prior + chunk tokens) read once; flops count causal pairs only:
+            4 * D * Hq per visible (query, key) pair."""
+    e, hq, hkv, d, L = w.elem_bytes, w.num_q_heads, w.num_kv_heads, w.head_dim, w.layers
+    tokens = int(lay.seq_lens.to(torch.int64).sum())
+    b = lay.num_decode_tokens
+    dec = tokens * hkv * d * 2 * e + 2 * b * hq * d * e
+    t = lay.slot_mapping.shape[0]
+    app = 2 * t * hkv * d * 2 * e
+    c, p = w.prefill_chunk, w.prefill_prior
+    pre = 2 * c * hq * d * e + (p + c) * hkv * d * 2 * e if c else 0
+    pairs = c * p + c * (c + 1) // 2
+    flops = 4 * d * hq * pairs
+    return {"decode_bytes_layer": dec, "append_bytes_layer": app, "prefill_bytes_layer": pre,
+            "prefill_flops_layer": flops, "bytes_step": L * (dec + app + pre),
+            "decode_tokens_step": b}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 0) or 0), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, 1900.0, "fallback"
+
+
+def profiled_traffic(kernel: str, source: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the kernel source as it is now (else None)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        rec = json.load(open(path)).get(kernel)
+        src = open(os.path.join(ROOT, "paged_kv_cache_104_gb300", "csrc", source), "rb").read()
+        if rec and rec.get("source_sha256") == hashlib.sha256(src).hexdigest():
+            return rec.get("dram_bytes_per_launch_full_size")
+    except Exception:
+        return None
+    return None
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling every 200 ms while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.samples = []
+        if self.proc is None:
+            return False
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 9:
+                self.samples.append(f)
+        return False
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        mx = [float(s[2]) for s in self.samples if s[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4)
+                          if s[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.samples)}
+
+
+# --------------------------------------------------------------------------- oracle timing
+def oracle_prepare(w, lay, n_dec_seqs: int, device="cpu"):
+    """Inputs for the oracle sample: a layout holding the first n_dec_seqs
+    decode sequences (same lengths as the full batch) and the prefill chunk,
+    drawn from the seeded generator (on `device`, then copied to the host) and
+    appended by the oracle's own scatter."""
+    import oracle
+    oracle.build()
+    sub = W.make_layout(w, seq_lens_after=lay.seq_lens[:n_dec_seqs],
+                        prefill=(w.prefill_prior, w.prefill_chunk))
+    x = W.draw_layer(w, sub, 0, device=device)
+    x = W.LayerInputs(*(t.to("cpu") for t in (x.q_decode, x.q_prefill, x.k_new, x.v_new,
+                                               x.k_cache, x.v_cache)))
+    oracle.kv_append(x.k_new, x.v_new, x.k_cache, x.v_cache, sub.slot_mapping)
+    return sub, x
+
+
+def oracle_sample_rates(w, sub, x, n_pre_rows: int):
+    """Time the fp64 CPU oracle: decode of every sequence of `sub` (every head)
+    and prefill of n_pre_rows evenly spaced chunk rows (every head).
+    Returns (decode algorithmic bytes/s, prefill rows/s, description, seconds)."""
+    import oracle
+    e, hq, hkv, d = w.elem_bytes, w.num_q_heads, w.num_kv_heads, w.head_dim
+    n_dec = sub.num_decode_tokens
+    t0 = time.perf_counter()
+    oracle.paged_decode(x.q_decode, x.k_cache, x.v_cache, sub.decode_block_table, sub.seq_lens,
+                        w.scale)
+    t_dec = time.perf_counter() - t0
+    sample_tokens = int(sub.seq_lens.to(torch.int64).sum())
+    dec_bytes = sample_tokens * hkv * d * 2 * e + 2 * n_dec * hq * d * e
+    pre_rate, t_pre = None, 0.0
+    if w.prefill_chunk and n_pre_rows:
+        stride = max(1, w.prefill_chunk // n_pre_rows)
+        rows = [(i, h) for i in list(range(0, w.prefill_chunk, stride))[:n_pre_rows]
+                for h in range(hq)]
+        bt = sub.block_table[sub.prefill_row]
+        t0 = time.perf_counter()
+        oracle.chunked_prefill(x.q_prefill, x.k_cache, x.v_cache, bt, w.prefill_prior, w.scale,
+                               rows=rows)
+        t_pre = time.perf_counter() - t0
+        pre_rate = (len(rows) / hq) / t_pre
+    desc = (f"one layer: decode of {n_dec} of the batch's sequences ({sample_tokens} cached "
+            f"tokens, all {hq} heads) in {t_dec:.2f} s"
+            + (f"; prefill of {n_pre_rows} evenly spaced chunk rows (all heads) in {t_pre:.2f} s"
+               if pre_rate else "")
+            + "; the full step (all layers, sequences and chunk rows) is extrapolated from "
+              "these rates")
+    return dec_bytes / t_dec, pre_rate, desc, t_dec + t_pre
+
+
+def oracle_step_estimate(w, lay, acct, dec_rate, pre_rate):
+    """Seconds the oracle would take for one full step, from sample rates."""
+    t = w.layers * acct["decode_bytes_layer"] / dec_rate
+    if w.prefill_chunk and pre_rate:
+        t += w.layers * w.prefill_chunk / pre_rate
+    return t
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# --------------------------------------------------------------------------- distributed
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo")
+        return dist
+    return None
+
+
+def max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------- reference arm
+def run_reference(args, w, lay, acct):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    os.environ.setdefault("OMP_NUM_THREADS", str(cpu_cores()))
+    import oracle
+    oracle.build()
+    threads = oracle.num_threads()
+    times = []
+    desc = ""
+    sub, x = oracle_prepare(w, lay, args.ref_decode_seqs, device="cpu")
+    for i in range(args.warmup + args.steps):
+        dec_rate, pre_rate, desc, _ = oracle_sample_rates(w, sub, x, args.ref_prefill_rows)
+        if i >= args.warmup:
+            times.append(oracle_step_estimate(w, lay, acct, dec_rate, pre_rate))
+    t = statistics.median(times)
+    value = acct["bytes_step"] / t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "description": w.description, "layers": w.layers},
+        "decode_tokens_per_s": acct["decode_tokens_step"] / t,
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": desc + " (per step; median over the timed steps)"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------- our arm
+def run_ours(args, w, lay, acct):
+    from paged_kv_cache_104_gb300 import binding as B
+
+    ws, rank, local = dist_env()
+    dist = init_dist(ws)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the CUDA path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B.load()
+    stream = torch.cuda.current_stream(dev)
+
+    L = w.layers
+    hq, hkv, d = w.num_q_heads, w.num_kv_heads, w.head_dim
+    # distinct pools per layer if they fit, else cycle as many as fit (>= 2)
+    pool_bytes = 2 * lay.num_blocks * hkv * w.block_size * d * w.elem_bytes
+    free, _ = torch.cuda.mem_get_info(dev)
+    n_pools = L if args.layer_pools <= 0 else min(L, args.layer_pools)
+    fit = int((free - 8 * 2 ** 30) // max(pool_bytes, 1))
+    if fit < n_pools:
+        n_pools = max(2, fit)
+    pools, inputs = [], []
+    for li in range(L):
+        x = W.draw_layer(w, lay, li + 1000 * rank, device=dev, with_pool=li < n_pools)
+        if li < n_pools:
+            pools.append((x.k_cache, x.v_cache))
+            x.k_cache = x.v_cache = None
+        inputs.append(x)
+    slot = lay.slot_mapping.to(dev)
+    bt_dec = lay.decode_block_table.to(dev).contiguous()
+    seq_lens = lay.seq_lens.to(dev)
+    bt_pre = lay.block_table[lay.prefill_row].to(dev).contiguous() if w.prefill_chunk else None
+    max_seq = int(lay.seq_lens.max())
+    wsp = B.decode_workspace(lay.num_decode_tokens, hq, d, max_seq, device=dev)
+    out_dec = [torch.empty_like(inputs[li].q_decode) for li in range(L)]
+    out_pre = [torch.empty_like(inputs[li].q_prefill) for li in range(L)]
+    split_launch = 2 if max_seq > 512 else 1  # decode main (+ reduce when any sequence splits)
+
+    def step(ev=None):
+        for li in range(L):
+            x = inputs[li]
+            kc, vc = pools[li % n_pools]
+            B.kv_append(x.k_new, x.v_new, kc, vc, slot, stream=stream)
+            if ev is not None:
+                ev[li][0].record(stream)
+            B.paged_decode_attention(out_dec[li], x.q_decode, kc, vc, bt_dec, seq_lens, max_seq,
+                                     w.scale, wsp, stream=stream)
+            if ev is not None:
+                ev[li][1].record(stream)
+            if w.prefill_chunk:
+                B.chunked_prefill_attention(out_pre[li], x.q_prefill, kc, vc, bt_pre,
+                                            w.prefill_prior, w.scale, stream=stream)
+                if ev is not None:
+                    ev[li][2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    assert B.get_device_error() == 0, "device error word set during warm-up"
+
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(L)]
+           for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t_start.record(stream)
+        for k in range(args.steps):
+            step(evs[k])
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(dist)
+    total_ms = t_start.elapsed_time(t_end)
+    total_ms = max_over_ranks(dist, total_ms)
+    assert B.get_device_error() == 0, "device error word set during the timed steps"
+    dec_ms = [evs[k][li][0].elapsed_time(evs[k][li][1]) for k in range(args.steps) for li in range(L)]
+    pre_ms = ([evs[k][li][1].elapsed_time(evs[k][li][2]) for k in range(args.steps)
+               for li in range(L)] if w.prefill_chunk else [])
+    ms_step = total_ms / args.steps
+    n = ws
+    value = n * acct["bytes_step"] / (ms_step / 1e3) / 1e9
+    hbm_peak, bf16_peak, peak_src = measured_peaks()
+    dec_avg = sum(dec_ms) / len(dec_ms)
+    dec_gbs = acct["decode_bytes_layer"] / (dec_avg / 1e3) / 1e9
+    traffic = profiled_traffic("decode_split_kernel", "decode.cu")
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": n, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": w.name, "description": w.description, "layers": L,
+            "decode_seqs": lay.num_decode_tokens, "cached_tokens": int(lay.seq_lens.sum()),
+            "prefill_chunk": w.prefill_chunk, "prefill_prior": w.prefill_prior,
+            "distinct_layer_pools": n_pools, "pool_gb_per_layer": pool_bytes / 1e9,
+            "l2": "inputs larger than L2: every layer has its own pools, each far larger than L2",
+            "parallelism": f"replicas x{n} (independent batches, no collective)",
+            "bytes_per_step": acct["bytes_step"],
+        },
+        "decode_tokens_per_s": n * acct["decode_tokens_step"] / (ms_step / 1e3),
+        "decode_gbs": dec_gbs,
+        "decode_hbm_frac": dec_gbs / hbm_peak,
+        "prefill_tflops": (acct["prefill_flops_layer"] / (sum(pre_ms) / len(pre_ms) / 1e3) / 1e12
+                           if pre_ms else None),
+        "prefill_ms_per_layer": sum(pre_ms) / len(pre_ms) if pre_ms else None,
+        "decode_ms_per_layer": dec_avg,
+        "roofline": {
+            "kernel": "paged_decode_attention (split-K main + reduce)",
+            "bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s",
+            "frac": dec_gbs / hbm_peak, "traffic": traffic,
+            "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+            else "fallback 6.8 TB/s",
+        },
+        "clocks": clk.summary(),
+        "gpu_launches": args.steps * L * (1 + split_launch + (1 if w.prefill_chunk else 0)),
+    }
+
+    # ---- end to end through the C ABI with host buffers (pinned), same step
+    if args.e2e_steps > 0:
+        h_in = []
+        h2d = 0
+        for li in range(L):
+            x = inputs[li]
+            hb = [t.to("cpu").pin_memory() for t in (x.q_decode, x.q_prefill, x.k_new, x.v_new)]
+            h2d += sum(t.numel() * t.element_size() for t in hb)
+            h_in.append(hb)
+        h_meta = [lay.slot_mapping.pin_memory(), lay.decode_block_table.contiguous().pin_memory(),
+                  lay.seq_lens.pin_memory()]
+        if w.prefill_chunk:
+            h_meta.append(lay.block_table[lay.prefill_row].contiguous().pin_memory())
+        h2d += sum(t.numel() * t.element_size() for t in h_meta)
+        d_meta = [slot, bt_dec, seq_lens] + ([bt_pre] if w.prefill_chunk else [])
+        h_out = [(torch.empty_like(out_dec[li], device="cpu").pin_memory(),
+                  torch.empty_like(out_pre[li], device="cpu").pin_memory()) for li in range(L)]
+        d2h = sum(a.numel() * a.element_size() + b.numel() * b.element_size() for a, b in h_out)
+
+        def e2e_step():
+            for hsrc, dst in zip(h_meta, d_meta):
+                dst.copy_(hsrc, non_blocking=True)
+            for li in range(L):
+                x = inputs[li]
+                for hsrc, dst in zip(h_in[li], (x.q_decode, x.q_prefill, x.k_new, x.v_new)):
+                    dst.copy_(hsrc, non_blocking=True)
+            step()
+            for li in range(L):
+                h_out[li][0].copy_(out_dec[li], non_blocking=True)
+                h_out[li][1].copy_(out_pre[li], non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(dist)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = max_over_ranks(dist, e0.elapsed_time(e1)) / args.e2e_steps
+        line["e2e"] = {"value": n * acct["bytes_step"] / (e_ms / 1e3) / 1e9, "unit": "GB/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": e_ms, "steps": args.e2e_steps}
+
+    # ---- the oracle on this host's cores, bounded sample, rank 0 at N=1 only
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        del pools, inputs, out_dec, out_pre
+        torch.cuda.empty_cache()
+        os.environ.setdefault("OMP_NUM_THREADS", str(cpu_cores()))
+        import oracle
+        sub, xs = oracle_prepare(w, lay, args.cpu_decode_seqs, device=dev)
+        dec_rate, pre_rate, desc, spent = oracle_sample_rates(w, sub, xs, args.cpu_prefill_rows)
+        t_cpu = oracle_step_estimate(w, lay, acct, dec_rate, pre_rate)
+        line["cpu_baseline"] = {"value": acct["bytes_step"] / t_cpu / 1e9, "unit": "GB/s",
+                                "cores": oracle.num_threads(), "kind": "oracle",
+                                "sample": desc, "seconds": spent}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="ragged_prefill", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--layer-pools", type=int, default=0,
+                    help="distinct layer pools to allocate (0 = one per layer); the step always "
+                         "runs every layer, cycling the pools")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-decode-seqs", type=int, default=128,
+                    help="decode sequences in the oracle sample of cpu_baseline")
+    ap.add_argument("--cpu-prefill-rows", type=int, default=256,
+                    help="chunk rows in the oracle sample of cpu_baseline")
+    ap.add_argument("--ref-decode-seqs", type=int, default=16,
+                    help="decode sequences per step of the reference (oracle) arm")
+    ap.add_argument("--ref-prefill-rows", type=int, default=32,
+                    help="chunk rows per step of the reference (oracle) arm")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    w = W.WORKLOADS[args.workload]
+    lay = W.make_layout(w)
+    acct = step_accounting(w, lay)
+    if args.impl == "reference":
+        return run_reference(args, w, lay, acct)
+    return run_ours(args, w, lay, acct)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

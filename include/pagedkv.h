@@ -1,0 +1,161 @@
+/*
+ * pagedkv.h -- C ABI of the GB300 (sm_103a) paged KV-cache attention library
+ * (libpagedkv.so).
+ *
+ * The library implements the per-step attention of continuous batching over
+ * a block-paged KV cache:
+ *   - kv_append: write each running sequence's new key and value into the
+ *     cache ("KV cache and continuous batching: 1,000 people ask AI", section
+ *     "What does a KV cache keep?"; "The KV cache and prefix caching",
+ *     section "What prefill stores and decode reads": a decode step appends
+ *     the new key and value to the cache);
+ *   - paged_decode_attention: attend each sequence's new query over every
+ *     key and value it has stored, under grouped-query attention, across a
+ *     ragged batch (same sections; the cache is held in fixed-size blocks
+ *     reached through a per-sequence block table, the PagedAttention layout);
+ *   - chunked_prefill_attention: a capped chunk of prompt tokens attends
+ *     causally over itself and the sequence's earlier cache ("The KV cache is
+ *     not your bottleneck", section "The fix that mattered").
+ *
+ * Conventions shared by every call
+ *   Layouts (row-major, element type given by `dtype`):
+ *     k_cache, v_cache   [num_blocks][num_kv_heads][block_size][head_dim]
+ *     block_table        int32 [num_seqs][max_blocks_per_seq]; entry j of a
+ *                        row is the physical block holding the sequence's
+ *                        tokens j*block_size .. j*block_size+block_size-1
+ *     slot_mapping       int64, slot = physical_block*block_size + row
+ *     q, out (decode)    [num_seqs][num_q_heads][head_dim]
+ *     q, out (prefill)   [chunk_len][num_q_heads][head_dim]
+ *   Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *   seq_lens counts the tokens stored after this step's append, so each new
+ *   query attends over its own key as well.
+ *   Memory: every pointer except those named "host" is a device pointer the
+ *   caller owns; the library allocates no memory and keeps no state between
+ *   calls other than a per-device error word.  Pointers must be 16-byte
+ *   aligned.
+ *   Streams: work is enqueued on `stream` (NULL = the legacy default stream)
+ *   and the call returns without synchronising.
+ *   Errors: argument errors are found on the host and returned before any
+ *   launch.  Values that live in device memory (slots, block ids, sequence
+ *   lengths) are checked by the kernels: an offending entry is skipped (no
+ *   out-of-bounds access happens), its outputs are unspecified, and a code
+ *   is recorded in the device error word (pkv_get_device_error).  Kernels
+ *   never trap; every internal wait is bounded.
+ *   Supported shapes: block_size 16; bf16 with head_dim 128, or fp32 with
+ *   head_dim 16 or 128; num_q_heads / num_kv_heads in {1, 2, 4, 8}.
+ *   The library runs on sm_103 GPUs (GB300).
+ */
+#ifndef PAGEDKV_H_
+#define PAGEDKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t. */
+typedef struct CUstream_st *pkv_stream_t;
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_EINVAL = 1,       /* null pointer, negative size, misaligned pointer, inconsistent shape */
+  PKV_EDTYPE = 2,       /* dtype not one of pkv_dtype */
+  PKV_ERANGE = 3,       /* a size beyond a limit (workspace too small, too many sequences) */
+  PKV_ECUDA = 4,        /* the CUDA runtime reported an error at launch */
+  PKV_EUNSUPPORTED = 5  /* a shape this build has no kernel for */
+} pkv_status;
+
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* Device error word values (pkv_get_device_error). */
+#define PKV_DEVERR_NONE 0
+#define PKV_DEVERR_SLOT_RANGE 1   /* kv_append: slot >= num_blocks*block_size (entry skipped) */
+#define PKV_DEVERR_BLOCK_RANGE 2  /* block-table entry outside [0, num_blocks) (block 0 read instead) */
+#define PKV_DEVERR_SEQLEN_RANGE 3 /* sequence length < 1 or beyond its bound (sequence skipped) */
+#define PKV_DEVERR_TIMEOUT 4      /* an internal wait ran out of time (results unspecified) */
+
+/* Largest num_seqs accepted by paged_decode_attention. */
+#define PKV_MAX_SEQS 8192
+
+/*
+ * kv_append -- write new keys and values into the paged pools (bit-exact copy).
+ *   k_new, v_new   [num_tokens][num_kv_heads][head_dim], device, read
+ *   k_cache, v_cache  pools, device, written in place at the given slots only
+ *   slot_mapping   int64 [num_tokens], device; slot < 0 means padding (skipped)
+ *   num_tokens >= 0 (0: no-op), num_blocks >= 1
+ * Slots must be distinct; two tokens writing one slot leave either row there.
+ */
+pkv_status pkv_kv_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                         const int64_t *slot_mapping, int64_t num_tokens, int64_t num_blocks,
+                         int num_kv_heads, int head_dim, int block_size, pkv_dtype dtype,
+                         pkv_stream_t stream);
+
+/*
+ * Bytes of device workspace paged_decode_attention needs for these sizes
+ * (0 when no sequence can need more than one split).  Host-only, no GPU use.
+ */
+size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_seq_len);
+
+/*
+ * paged_decode_attention -- one new query per sequence over its whole cache.
+ *   out    [num_seqs][num_q_heads][head_dim], device, written
+ *   q      [num_seqs][num_q_heads][head_dim], device, read
+ *   block_table  int32 [num_seqs][max_blocks_per_seq], device
+ *   seq_lens     int32 [num_seqs], device; 1 <= seq_lens[b] <= max_seq_len
+ *   max_seq_len  host bound on every seq_lens entry (sizes the split grid)
+ *   scale        softmax scale (usually 1/sqrt(head_dim))
+ *   workspace    device scratch of at least pkv_decode_workspace_bytes(...)
+ *                bytes (may be NULL when that is 0); overwritten
+ *   1 <= num_seqs <= PKV_MAX_SEQS; max_seq_len <= max_blocks_per_seq*block_size
+ * Output: out[b][h] = sum_j softmax_j(scale * q[b][h].k_j) v_j over the
+ * seq_lens[b] stored tokens j of sequence b and KV head h/(Hq/Hkv), rounded
+ * to the storage type.
+ */
+pkv_status pkv_paged_decode_attention(void *out, const void *q, const void *k_cache,
+                                      const void *v_cache, const int32_t *block_table,
+                                      const int32_t *seq_lens, int num_seqs,
+                                      int max_blocks_per_seq, int max_seq_len,
+                                      int64_t num_blocks, int num_q_heads, int num_kv_heads,
+                                      int head_dim, int block_size, float scale,
+                                      void *workspace, size_t workspace_bytes, pkv_dtype dtype,
+                                      pkv_stream_t stream);
+
+/*
+ * chunked_prefill_attention -- a chunk of one sequence's prompt attends
+ * causally over itself and the cache before it.
+ *   out, q   [chunk_len][num_q_heads][head_dim], device
+ *   block_table_row  int32 [max_blocks], device: the sequence's block table
+ *   prior_len   tokens the sequence had before this chunk (host value)
+ *   chunk_len   tokens in the chunk (host value, >= 0; 0 is a no-op)
+ * The chunk's own keys and values must already be in the pools (kv_append
+ * first).  Row i sits at position prior_len + i and sees keys
+ * 0 .. prior_len + i.  Requires prior_len + chunk_len <= max_blocks*block_size.
+ * bf16 with head_dim 128 runs on the tcgen05 tensor cores; other supported
+ * shapes run a CUDA-core kernel.
+ */
+pkv_status pkv_chunked_prefill_attention(void *out, const void *q, const void *k_cache,
+                                         const void *v_cache, const int32_t *block_table_row,
+                                         int max_blocks, int prior_len, int chunk_len,
+                                         int64_t num_blocks, int num_q_heads, int num_kv_heads,
+                                         int head_dim, int block_size, float scale,
+                                         pkv_dtype dtype, pkv_stream_t stream);
+
+/*
+ * Read the device error word of the current device into *code (host) and,
+ * if clear != 0, reset it to PKV_DEVERR_NONE.  Synchronises the device.
+ */
+pkv_status pkv_get_device_error(int *code, int clear);
+
+/* Static description of a status code.  Host-only. */
+const char *pkv_status_str(pkv_status status);
+
+/* ABI version of this header (bumped on any incompatible change).  Host-only. */
+int pkv_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H_ */

@@ -1,0 +1,144 @@
+"""Thin Python binding of libpagedkv.so (argument marshalling only).
+
+Every function takes torch CUDA tensors, passes their device pointers, sizes
+and the current CUDA stream to the C ABI of the same name (``include/pagedkv.h``)
+and raises ``PagedKVError`` on a non-zero status.  No step of the computation
+runs here: if the library is missing the import of a function fails loudly
+instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpagedkv.so")
+_lib = None
+_lock = threading.Lock()
+
+PKV_F32, PKV_BF16 = 0, 1
+DEVERR = {0: "none", 1: "slot out of range", 2: "block id out of range",
+          3: "sequence length out of range", 4: "internal wait timed out"}
+EXPORTS = ("pkv_kv_append", "pkv_decode_workspace_bytes", "pkv_paged_decode_attention",
+           "pkv_chunked_prefill_attention", "pkv_get_device_error", "pkv_status_str",
+           "pkv_abi_version")
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} failed: status {status} ({msg})")
+        self.status = status
+
+
+def load():
+    """Load the shared library (built by ``paged_kv_cache_104_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: run `python -m paged_kv_cache_104_gb300.build`")
+        lib = ctypes.CDLL(LIB_PATH)
+        p, i, i64, f, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                            ctypes.c_size_t)
+        lib.pkv_kv_append.argtypes = [p, p, p, p, p, i64, i64, i, i, i, i, p]
+        lib.pkv_decode_workspace_bytes.argtypes = [i, i, i, i]
+        lib.pkv_decode_workspace_bytes.restype = sz
+        lib.pkv_paged_decode_attention.argtypes = [p, p, p, p, p, p, i, i, i, i64, i, i, i, i, f,
+                                                   p, sz, i, p]
+        lib.pkv_chunked_prefill_attention.argtypes = [p, p, p, p, p, i, i, i, i64, i, i, i, i, f,
+                                                      i, p]
+        lib.pkv_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int), i]
+        lib.pkv_status_str.argtypes = [i]
+        lib.pkv_status_str.restype = ctypes.c_char_p
+        for name in ("pkv_kv_append", "pkv_paged_decode_attention",
+                     "pkv_chunked_prefill_attention", "pkv_get_device_error", "pkv_abi_version"):
+            getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return PKV_BF16
+    if t.dtype == torch.float32:
+        return PKV_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise PagedKVError(fn, status, load().pkv_status_str(status).decode())
+
+
+def status_str(status: int) -> str:
+    return load().pkv_status_str(status).decode()
+
+
+def abi_version() -> int:
+    return int(load().pkv_abi_version())
+
+
+def kv_append(k_new, v_new, k_cache, v_cache, slot_mapping, stream=None) -> None:
+    """k_new, v_new [T, Hkv, D]; pools [NB, Hkv, bs, D]; slot_mapping [T] int64."""
+    nb, hkv, bs, d = k_cache.shape
+    st = load().pkv_kv_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                              _ptr(slot_mapping), int(slot_mapping.shape[0]), nb, hkv, d, bs,
+                              _dtype_code(k_cache), _stream(stream))
+    _check("pkv_kv_append", st)
+
+
+def decode_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: int, max_seq_len: int) -> int:
+    return int(load().pkv_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len))
+
+
+def decode_workspace(num_seqs, num_q_heads, head_dim, max_seq_len, device="cuda"):
+    """Allocate (through torch) the workspace paged_decode_attention needs."""
+    n = decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def paged_decode_attention(out, q, k_cache, v_cache, block_table, seq_lens, max_seq_len: int,
+                           scale: float, workspace=None, stream=None) -> None:
+    """out, q [B, Hq, D]; pools [NB, Hkv, bs, D]; block_table [B, max_blocks]
+    int32; seq_lens [B] int32 (after the append); max_seq_len >= max(seq_lens)."""
+    b, hq, d = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().pkv_paged_decode_attention(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
+        b, int(block_table.shape[1]), int(max_seq_len), nb, hq, hkv, d, bs, float(scale),
+        _ptr(workspace), ws_bytes, _dtype_code(q), _stream(stream))
+    _check("pkv_paged_decode_attention", st)
+
+
+def chunked_prefill_attention(out, q, k_cache, v_cache, block_table_row, prior_len: int,
+                              scale: float, stream=None) -> None:
+    """out, q [C, Hq, D]; block_table_row [max_blocks] int32; the chunk sits at
+    positions prior_len .. prior_len+C-1 and its K/V are already appended."""
+    c, hq, d = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    st = load().pkv_chunked_prefill_attention(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table_row),
+        int(block_table_row.shape[0]), int(prior_len), c, nb, hq, hkv, d, bs, float(scale),
+        _dtype_code(q), _stream(stream))
+    _check("pkv_chunked_prefill_attention", st)
+
+
+def get_device_error(clear: bool = True) -> int:
+    """Device error word of the current device (0 = none); synchronises."""
+    code = ctypes.c_int(0)
+    _check("pkv_get_device_error", load().pkv_get_device_error(ctypes.byref(code), int(clear)))
+    return code.value

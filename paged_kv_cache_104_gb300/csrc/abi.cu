@@ -1,0 +1,243 @@
+// C ABI of libpagedkv.so: argument validation, workspace layout, dispatch to
+// the kernel launchers, and the per-device error word.  The declarations and
+// their contracts are in include/pagedkv.h.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "launch.h"
+#include "pagedkv.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// One error word per device: kernels record the first device-side error here.
+__device__ int g_pkv_error_word;
+
+int* g_err_ptr[kMaxDevices];
+int g_num_sms[kMaxDevices];
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_bytes(pkv_dtype d) { return d == PKV_BF16 ? 2 : 4; }
+
+bool dtype_ok(pkv_dtype d) { return d == PKV_F32 || d == PKV_BF16; }
+
+// Device-side address of this device's error word and its SM count; resolved
+// once per device with that device current.
+pkv_status device_state(int** err, int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_ECUDA;
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_pkv_error_word) != cudaSuccess) return PKV_ECUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return PKV_ECUDA;
+    g_num_sms[dev] = sms;
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  *err = g_err_ptr[dev];
+  *num_sms = g_num_sms[dev];
+  return PKV_OK;
+}
+
+int max_splits_for(int max_seq_len) {
+  return (max_seq_len + pkv::kSplitTokens - 1) / pkv::kSplitTokens;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Shape checks shared by decode and prefill.
+pkv_status check_heads(int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                       pkv_dtype dtype) {
+  if (!dtype_ok(dtype)) return PKV_EDTYPE;
+  if (num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 || block_size < 1) return PKV_EINVAL;
+  if (num_q_heads % num_kv_heads != 0) return PKV_EINVAL;
+  if (block_size != pkv::kBlockSize) return PKV_EUNSUPPORTED;
+  if (!pkv::decode_supported(dtype == PKV_BF16, head_dim, num_q_heads / num_kv_heads))
+    return PKV_EUNSUPPORTED;
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_abi_version(void) { return 1; }
+
+const char* pkv_status_str(pkv_status s) {
+  switch (s) {
+    case PKV_OK: return "ok";
+    case PKV_EINVAL: return "invalid argument";
+    case PKV_EDTYPE: return "unknown dtype";
+    case PKV_ERANGE: return "size out of range";
+    case PKV_ECUDA: return "CUDA runtime error";
+    case PKV_EUNSUPPORTED: return "unsupported shape";
+  }
+  return "unknown status";
+}
+
+pkv_status pkv_get_device_error(int* code, int clear) {
+  if (!code) return PKV_EINVAL;
+  int* err = nullptr;
+  int sms = 0;
+  pkv_status st = device_state(&err, &sms);
+  if (st != PKV_OK) return st;
+  if (cudaDeviceSynchronize() != cudaSuccess) return PKV_ECUDA;
+  if (cudaMemcpy(code, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return PKV_ECUDA;
+  if (clear && cudaMemset(err, 0, sizeof(int)) != cudaSuccess) return PKV_ECUDA;
+  return PKV_OK;
+}
+
+pkv_status pkv_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                         const int64_t* slot_mapping, int64_t num_tokens, int64_t num_blocks,
+                         int num_kv_heads, int head_dim, int block_size, pkv_dtype dtype,
+                         pkv_stream_t stream) {
+  if (!dtype_ok(dtype)) return PKV_EDTYPE;
+  if (num_tokens < 0 || num_blocks < 1 || num_kv_heads < 1 || head_dim < 1 || block_size < 1)
+    return PKV_EINVAL;
+  if (block_size != pkv::kBlockSize) return PKV_EUNSUPPORTED;
+  const int row_bytes = head_dim * elem_bytes(dtype);
+  if (row_bytes % 16 != 0) return PKV_EUNSUPPORTED;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_new || !v_new || !k_cache || !v_cache || !slot_mapping) return PKV_EINVAL;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return PKV_EINVAL;
+  int* err = nullptr;
+  int sms = 0;
+  pkv_status st = device_state(&err, &sms);
+  if (st != PKV_OK) return st;
+  pkv::AppendArgs a{k_new, v_new, k_cache, v_cache, slot_mapping, num_tokens, num_blocks,
+                    num_kv_heads, row_bytes, err};
+  return pkv::launch_kv_append(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PKV_OK
+             : PKV_ECUDA;
+}
+
+size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_seq_len) {
+  if (num_seqs < 1 || num_q_heads < 1 || head_dim < 1 || max_seq_len < 1) return 0;
+  const int s = max_splits_for(max_seq_len);
+  if (s <= 1) return 0;
+  const size_t rows = (size_t)num_seqs * num_q_heads * s;
+  return align256(rows * head_dim * sizeof(float)) + align256(rows * 2 * sizeof(float));
+}
+
+pkv_status pkv_paged_decode_attention(void* out, const void* q, const void* k_cache,
+                                      const void* v_cache, const int32_t* block_table,
+                                      const int32_t* seq_lens, int num_seqs,
+                                      int max_blocks_per_seq, int max_seq_len,
+                                      int64_t num_blocks, int num_q_heads, int num_kv_heads,
+                                      int head_dim, int block_size, float scale,
+                                      void* workspace, size_t workspace_bytes, pkv_dtype dtype,
+                                      pkv_stream_t stream) {
+  pkv_status st = check_heads(num_q_heads, num_kv_heads, head_dim, block_size, dtype);
+  if (st != PKV_OK) return st;
+  if (num_seqs < 0 || max_blocks_per_seq < 1 || max_seq_len < 1 || num_blocks < 1)
+    return PKV_EINVAL;
+  if (num_seqs == 0) return PKV_OK;
+  if (num_seqs > PKV_MAX_SEQS) return PKV_ERANGE;
+  if ((int64_t)max_seq_len > (int64_t)max_blocks_per_seq * block_size) return PKV_EINVAL;
+  if (!isfinite(scale)) return PKV_EINVAL;
+  if (!out || !q || !k_cache || !v_cache || !block_table || !seq_lens) return PKV_EINVAL;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return PKV_EINVAL;
+  const size_t need = pkv_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len);
+  if (workspace_bytes < need) return PKV_ERANGE;
+  if (need > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))) return PKV_EINVAL;
+  int* err = nullptr;
+  int sms = 0;
+  st = device_state(&err, &sms);
+  if (st != PKV_OK) return st;
+  const int s = max_splits_for(max_seq_len);
+  const size_t rows = (size_t)num_seqs * num_q_heads * s;
+  float* ws_acc = static_cast<float*>(workspace);
+  float* ws_ml = need ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                 align256(rows * head_dim * sizeof(float)))
+                      : nullptr;
+  pkv::DecodeArgs a{};
+  a.out = out;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.ws_acc = ws_acc;
+  a.ws_ml = ws_ml;
+  a.err = err;
+  a.num_seqs = num_seqs;
+  a.bt_stride = max_blocks_per_seq;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.max_seq_len = max_seq_len;
+  a.max_splits = s;
+  a.split_tokens = pkv::kSplitTokens;
+  a.num_blocks = num_blocks;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.scale = scale;
+  a.chunk_prior = -1;
+  a.is_bf16 = dtype == PKV_BF16;
+  return pkv::launch_paged_decode(a, sms, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PKV_OK
+             : PKV_ECUDA;
+}
+
+pkv_status pkv_chunked_prefill_attention(void* out, const void* q, const void* k_cache,
+                                         const void* v_cache, const int32_t* block_table_row,
+                                         int max_blocks, int prior_len, int chunk_len,
+                                         int64_t num_blocks, int num_q_heads, int num_kv_heads,
+                                         int head_dim, int block_size, float scale,
+                                         pkv_dtype dtype, pkv_stream_t stream) {
+  pkv_status st = check_heads(num_q_heads, num_kv_heads, head_dim, block_size, dtype);
+  if (st != PKV_OK) return st;
+  if (max_blocks < 1 || prior_len < 0 || chunk_len < 0 || num_blocks < 1) return PKV_EINVAL;
+  if (chunk_len == 0) return PKV_OK;
+  if ((int64_t)prior_len + chunk_len > (int64_t)max_blocks * block_size) return PKV_EINVAL;
+  if (!isfinite(scale)) return PKV_EINVAL;
+  if (!out || !q || !k_cache || !v_cache || !block_table_row) return PKV_EINVAL;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(block_table_row) & 3u))
+    return PKV_EINVAL;
+  int* err = nullptr;
+  int sms = 0;
+  st = device_state(&err, &sms);
+  if (st != PKV_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == PKV_BF16 && head_dim == 128) {
+    pkv::PrefillArgs a{out, q, k_cache, v_cache, block_table_row, max_blocks, prior_len, chunk_len,
+                       num_blocks, num_q_heads, num_kv_heads, scale, err};
+    return pkv::launch_prefill_tc(a, sms, s) == cudaSuccess ? PKV_OK : PKV_ECUDA;
+  }
+  // CUDA-core path: every chunk row is one query over its causal prefix, run
+  // as a single split so no workspace is needed.
+  if (chunk_len > PKV_MAX_SEQS) return PKV_ERANGE;
+  const int total = prior_len + chunk_len;
+  pkv::DecodeArgs a{};
+  a.out = out;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_table = block_table_row;
+  a.seq_lens = nullptr;
+  a.err = err;
+  a.num_seqs = chunk_len;
+  a.bt_stride = 0;
+  a.max_blocks_per_seq = max_blocks;
+  a.max_seq_len = total;
+  a.max_splits = 1;
+  a.split_tokens = ((total + pkv::kSplitTokens - 1) / pkv::kSplitTokens) * pkv::kSplitTokens;
+  a.num_blocks = num_blocks;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.scale = scale;
+  a.chunk_prior = prior_len;
+  a.is_bf16 = dtype == PKV_BF16;
+  return pkv::launch_paged_decode(a, sms, s) == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+}  // extern "C"

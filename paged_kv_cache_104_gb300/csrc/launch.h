@@ -1,0 +1,75 @@
+// Internal launchers: one per kernel family, called by the C ABI layer
+// (abi.cu) after it has validated every host-side argument.  Each returns a
+// cudaError_t from the launch.  Not part of the public interface.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkv {
+
+constexpr int kBlockSize = 16;     // tokens per cache block (compiled)
+constexpr int kSplitTokens = 512;  // decode tokens per split-K unit
+
+struct AppendArgs {
+  const void* k_new;
+  const void* v_new;
+  void* k_cache;
+  void* v_cache;
+  const int64_t* slot_mapping;
+  int64_t num_tokens;
+  int64_t num_blocks;
+  int num_kv_heads;
+  int row_bytes;  // head_dim * element size
+  int* err;
+};
+cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream);
+
+struct DecodeArgs {
+  void* out;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_table;
+  const int32_t* seq_lens;  // may be null in chunk mode
+  float* ws_acc;            // [B][Hq][max_splits][D] fp32 (unused if max_splits == 1)
+  float* ws_ml;             // [B][Hq][max_splits][2] fp32
+  int* err;
+  int num_seqs;
+  int bt_stride;            // elements between block-table rows (0: all rows share one)
+  int max_blocks_per_seq;
+  int max_seq_len;          // host bound on every sequence length
+  int max_splits;           // ceil(max_seq_len / split_tokens)
+  int split_tokens;
+  int64_t num_blocks;
+  int num_q_heads;
+  int num_kv_heads;
+  int head_dim;
+  float scale;
+  int chunk_prior;          // -1: decode; >= 0: row b has length chunk_prior + b + 1
+  int is_bf16;
+};
+// True if (dtype, head_dim, group) has a compiled decode kernel.
+bool decode_supported(int is_bf16, int head_dim, int group);
+cudaError_t launch_paged_decode(const DecodeArgs& a, int num_sms, cudaStream_t stream);
+
+struct PrefillArgs {
+  void* out;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_table_row;
+  int max_blocks;
+  int prior_len;
+  int chunk_len;
+  int64_t num_blocks;
+  int num_q_heads;
+  int num_kv_heads;
+  float scale;
+  int* err;
+};
+// tcgen05 path: bf16, head_dim 128, block_size 16.
+cudaError_t launch_prefill_tc(const PrefillArgs& a, int num_sms, cudaStream_t stream);
+
+}  // namespace pkv

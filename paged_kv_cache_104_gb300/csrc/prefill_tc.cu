@@ -1,0 +1,518 @@
+// Chunked-prefill attention on the fifth-generation tensor cores (tcgen05).
+//
+// What it computes ("The KV cache is not your bottleneck", section "The fix
+// that mattered": prompts are admitted in capped chunks; "KV cache and
+// continuous batching: 1,000 people ask AI", section "What does a KV cache
+// keep?": prefill is matrix-matrix work): a chunk of C prompt tokens of one
+// sequence, at absolute positions prior .. prior+C-1, whose keys and values
+// were already appended to the paged pools, attends causally over the
+// sequence: row i sees keys 0 .. prior+i.  out[i][h] = softmax(scale *
+// q[i][h] . K[:, h/G]) V[:, h/G] over those keys.
+//
+// CTA = 128 query rows of one query head; keys stream in tiles of 128
+// (eight 16-token blocks gathered through the block table by 2-D TMA with
+// 128-byte swizzle, which is the canonical K-major operand layout).
+//   warp 4      TMA producer: Q once, then K/V tiles into a 2-stage ring;
+//               blocks past the end of the sequence are fetched at an
+//               out-of-range coordinate, which the TMA unit fills with zeros
+//   warp 5      TMEM allocator and single-thread MMA issuer:
+//               S[j%2] = Q K_j^T  (M=128, N=128, K=128, bf16 -> fp32 in TMEM)
+//               O     += P_j V_j  (P from shared memory, V as an MN-major operand)
+//   warps 0-3   softmax: thread r owns query row r = TMEM lane r; reads its S
+//               row with tcgen05.ld, applies the causal mask, keeps a running
+//               max (raised lazily, only when it grows by more than 2^8) and
+//               sum, writes P (bf16) into the swizzled A-operand tile, and
+//               rescales its O row in TMEM when the max moved.  Epilogue: O/l.
+// S is double-buffered in TMEM so Q K_{j+1}^T runs while the softmax of tile
+// j does; fully masked key tiles are never visited.
+// Every mbarrier wait is bounded; on time-out the kernel records an error,
+// stops issuing work, lets its copies land, frees its TMEM and returns.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace pkv {
+namespace {
+
+constexpr int BM = 128, BN = 128, HD = 128;
+constexpr int HALF = BM * 128;            // one 64-column half of a 128-row tile: 16 KiB
+constexpr int TILE = 2 * HALF;            // 32 KiB
+constexpr int NSTAGE = 2;
+constexpr int OFF_Q = 0;
+constexpr int OFF_K = OFF_Q + TILE;
+constexpr int OFF_V = OFF_K + NSTAGE * TILE;
+constexpr int OFF_P = OFF_V + NSTAGE * TILE;
+constexpr int OFF_BAR = OFF_P + TILE;
+constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + slack to align the base to 1 KiB
+constexpr int kThreadsTC = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t COL_S0 = 0, COL_O = 256;
+constexpr float kLazy = 8.0f;
+
+// barrier slots (8 bytes each) inside OFF_BAR
+enum { B_Q = 0, B_KV_FULL = 1, B_KV_EMPTY = 3, B_S_FULL = 5, B_S_FREE = 7, B_P_FULL = 9,
+       B_O_DONE = 10, B_COUNT = 11 };
+
+struct TcParams {
+  PrefillArgs a;
+  int total_len;     // prior + chunk
+  int kv_rows;       // num_blocks * Hkv * 16 (rows of the 2-D pool view)
+  int q_tiles;
+};
+
+// --- tcgen05 / TMA wrappers --------------------------------------------------
+__device__ __forceinline__ uint64_t make_sw128_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFF);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= 1ull << 46;  // descriptor version for sm_100-family tcgen05
+  d |= 2ull << 61;  // 128-byte swizzle
+  return d;
+}
+
+// kind::f16 instruction descriptor: fp32 accumulate, bf16 A and B, M=128, N=128
+__host__ __device__ constexpr uint32_t make_idesc(bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31])));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Registers written by tcgen05.ld are valid only after tcgen05.wait::ld.
+// Passing them through an empty volatile asm placed after the wait gives the
+// compiler a dependency it cannot hoist their uses above.
+template <int N>
+__device__ __forceinline__ void reg_fence(float (&v)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+f"(v[i]));
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// bounded wait that also honours a CTA-wide abort flag
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                              int* err) {
+  if (*abort_flag) return false;
+  if (!mbar_wait(bar, parity, err)) {
+    *abort_flag = 1;
+    return false;
+  }
+  return true;
+}
+
+__global__ void __launch_bounds__(kThreadsTC, 1)
+prefill_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tm_q,
+                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + B_COUNT);
+  int* abort_i = reinterpret_cast<int*>(tmem_slot + 1);
+  volatile int* abort_flag = abort_i;
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+
+  const PrefillArgs& a = p.a;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.x;                              // query head
+  const int qt = p.q_tiles - 1 - (int)blockIdx.y;        // heaviest tiles first
+  const int q0 = qt * BM;
+  const int g = h / (a.num_q_heads / a.num_kv_heads);    // KV head of the group
+  const int last_row_pos = a.prior_len + min(a.chunk_len, q0 + BM) - 1;
+  const int n_tiles = last_row_pos / BN + 1;             // key tiles with any visible key
+
+  if (tid == 0) {
+    mbar_init(bar(B_Q), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_KV_FULL + s), 1);
+      mbar_init(bar(B_KV_EMPTY + s), 1);
+      mbar_init(bar(B_S_FULL + s), 1);
+      mbar_init(bar(B_S_FREE + s), 128);
+    }
+    mbar_init(bar(B_P_FULL), 128);
+    mbar_init(bar(B_O_DONE), 1);
+    *abort_i = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
+      mbar_arrive_expect_tx(bar(B_Q), TILE);
+      tma_load_3d(sbase + OFF_Q, &tm_q, bar(B_Q), 0, h, q0);
+      tma_load_3d(sbase + OFF_Q + HALF, &tm_q, bar(B_Q), 64, h, q0);
+      int issued = 0;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int st = j & 1;
+        if (j >= 2 && !wait_or_abort(bar(B_KV_EMPTY + st), ((j >> 1) - 1) & 1, abort_flag, a.err))
+          break;
+        if (*abort_flag) break;
+        mbar_arrive_expect_tx(bar(B_KV_FULL + st), 2 * TILE);
+        const uint32_t kd = sbase + OFF_K + st * TILE, vd = sbase + OFF_V + st * TILE;
+        for (int i = 0; i < BN / kBlockSize; ++i) {
+          const int tok = j * BN + i * kBlockSize;
+          int y = p.kv_rows;  // past the end: zero fill
+          if (tok < p.total_len) {
+            int blk = __ldg(a.block_table_row + tok / kBlockSize);
+            if (blk < 0 || (int64_t)blk >= a.num_blocks) {
+              record_error(a.err, DEVERR_BLOCK_RANGE);
+              blk = 0;
+            }
+            y = (blk * a.num_kv_heads + g) * kBlockSize;
+          }
+          const uint32_t off = i * kBlockSize * 128;  // 16 rows x 128 B
+          tma_load_2d(kd + off, &tm_k, bar(B_KV_FULL + st), 0, y);
+          tma_load_2d(kd + HALF + off, &tm_k, bar(B_KV_FULL + st), 64, y);
+          tma_load_2d(vd + off, &tm_v, bar(B_KV_FULL + st), 0, y);
+          tma_load_2d(vd + HALF + off, &tm_v, bar(B_KV_FULL + st), 64, y);
+        }
+        issued = j + 1;
+      }
+      if (*abort_flag) {  // let the loads already issued land
+        mbar_wait(bar(B_Q), 0, nullptr);
+        for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
+          mbar_wait(bar(B_KV_FULL + (j & 1)), (j >> 1) & 1, nullptr);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = make_idesc(false);
+      constexpr uint32_t idesc_pv = make_idesc(true);
+      bool ok = wait_or_abort(bar(B_Q), 0, abort_flag, a.err);
+      tc_fence_after();
+      auto issue_pv = [&](int jj) {
+        const int st = jj & 1;
+        if (!wait_or_abort(bar(B_P_FULL), jj & 1, abort_flag, a.err)) return false;
+        tc_fence_after();
+        const uint32_t pa = sbase + OFF_P, vb = sbase + OFF_V + st * TILE;
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint64_t ad = make_sw128_desc(pa + (k >> 2) * HALF + (k & 3) * 32, 16, 1024);
+          const uint64_t bd = make_sw128_desc(vb + k * 16 * 128, HALF, 1024);
+          mma_bf16(tmem + COL_O, ad, bd, idesc_pv, (jj > 0 || k > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(B_O_DONE));
+        mma_commit(bar(B_KV_EMPTY + st));
+        return true;
+      };
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int st = j & 1, sb = j & 1;
+        ok = wait_or_abort(bar(B_KV_FULL + st), (j >> 1) & 1, abort_flag, a.err);
+        if (ok && j >= 2) ok = wait_or_abort(bar(B_S_FREE + sb), ((j >> 1) - 1) & 1, abort_flag, a.err);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t qa = sbase + OFF_Q, kb = sbase + OFF_K + st * TILE;
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint64_t ad = make_sw128_desc(qa + (k >> 2) * HALF + (k & 3) * 32, 16, 1024);
+          const uint64_t bd = make_sw128_desc(kb + (k >> 2) * HALF + (k & 3) * 32, 16, 1024);
+          mma_bf16(tmem + COL_S0 + sb * BN, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(B_S_FULL + sb));
+        if (j >= 1) ok = issue_pv(j - 1);
+      }
+      if (ok) issue_pv(n_tiles - 1);
+    }
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int r = tid;                      // query row in the tile, TMEM lane
+    const int row_pos = a.prior_len + q0 + r;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const float sl2 = a.scale * 1.4426950408889634f;
+    float m_run = -INFINITY, l_run = 0.f;
+    unsigned char* prow = smem + OFF_P + r * 128;
+    const int sw = r & 7;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int sb = j & 1;
+      wait_or_abort(bar(B_S_FULL + sb), (j >> 1) & 1, abort_flag, a.err);
+      __syncwarp();
+      tc_fence_after();
+      float s[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        float t[32];
+        tmem_ld32(lane_base + COL_S0 + sb * BN + c * 32, t);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = t[i];
+      }
+      tmem_wait_ld();
+      reg_fence(s);
+      tc_fence_before();
+      mbar_arrive(bar(B_S_FREE + sb));
+      // causal mask: key k visible iff k <= row_pos
+      const int k0 = j * BN;
+      float mx = -INFINITY;
+      if (k0 + BN - 1 > a.prior_len + q0) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c) {
+          s[c] = (k0 + c <= row_pos) ? s[c] * sl2 : -INFINITY;
+          mx = fmaxf(mx, s[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < BN; ++c) {
+          s[c] *= sl2;
+          mx = fmaxf(mx, s[c]);
+        }
+      }
+      float m_new = m_run;
+      if (mx > m_run + kLazy || m_run == -INFINITY) m_new = mx;
+      const float alpha = (m_new == m_run) ? 1.f : fast_exp2(m_run - m_new);
+      float rowsum = 0.f;
+      uint32_t packed[BN / 2];
+#pragma unroll
+      for (int c = 0; c < BN; c += 2) {
+        const float p0 = fast_exp2(s[c] - m_new);
+        const float p1 = fast_exp2(s[c + 1] - m_new);
+        packed[c / 2] = pack_bf16(p0, p1);
+        rowsum += bf16lo(packed[c / 2]) + bf16hi(packed[c / 2]);
+      }
+      // P_{j-1} . V must be finished before P is overwritten or O rescaled
+      if (j >= 1) {
+        wait_or_abort(bar(B_O_DONE), (j - 1) & 1, abort_flag, a.err);
+        __syncwarp();
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+          for (int c = 0; c < HD / 32; ++c) {
+            float o[32];
+            tmem_ld32(lane_base + COL_O + c * 32, o);
+            tmem_wait_ld();
+            reg_fence(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(lane_base + COL_O + c * 32, o);
+          }
+          tmem_wait_st();
+        }
+      }
+      l_run = l_run * alpha + rowsum;
+      m_run = m_new;
+      // the last tile may hold stale rows past the sequence end: zero their V
+      if (j == n_tiles - 1 && k0 + BN > p.total_len) {
+        wait_or_abort(bar(B_KV_FULL + (j & 1)), (j >> 1) & 1, abort_flag, a.err);
+        if (k0 + r >= p.total_len) {
+          unsigned char* vrow = smem + OFF_V + (j & 1) * TILE + r * 128;
+          const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            *reinterpret_cast<uint4*>(vrow + c * 16) = z;
+            *reinterpret_cast<uint4*>(vrow + HALF + c * 16) = z;
+          }
+        }
+      }
+      // write P row r into the 128B-swizzled K-major tile (two 64-column halves)
+#pragma unroll
+      for (int cc = 0; cc < 16; ++cc) {
+        const int half = cc >> 3, chunk = cc & 7;
+        uint4 v = make_uint4(packed[cc * 4 + 0], packed[cc * 4 + 1], packed[cc * 4 + 2],
+                             packed[cc * 4 + 3]);
+        *reinterpret_cast<uint4*>(prow + half * HALF + ((chunk ^ sw) << 4)) = v;
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(B_P_FULL));
+    }
+    // epilogue: O / l
+    wait_or_abort(bar(B_O_DONE), (n_tiles - 1) & 1, abort_flag, a.err);
+    __syncwarp();
+    tc_fence_after();
+    const float inv = 1.f / l_run;
+    const bool row_ok = (q0 + r) < a.chunk_len;
+    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
+                          ((int64_t)(q0 + r) * a.num_q_heads + h) * HD;
+#pragma unroll 1
+    for (int c = 0; c < HD / 32; ++c) {
+      float o[32];
+      tmem_ld32(lane_base + COL_O + c * 32, o);
+      tmem_wait_ld();
+      reg_fence(o);
+      if (row_ok) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) {
+          uint4 v = make_uint4(pack_bf16(o[i] * inv, o[i + 1] * inv),
+                               pack_bf16(o[i + 2] * inv, o[i + 3] * inv),
+                               pack_bf16(o[i + 4] * inv, o[i + 5] * inv),
+                               pack_bf16(o[i + 6] * inv, o[i + 7] * inv));
+          *reinterpret_cast<uint4*>(orow + c * 32 + i) = v;
+        }
+      }
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+  }
+}
+
+// --- host side: tensor maps through the driver entry point ------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const PrefillArgs& a, int num_sms, cudaStream_t stream) {
+  (void)num_sms;
+  EncodeTiledFn encode = get_encode_fn();
+  if (!encode) return cudaErrorNotSupported;
+  TcParams p;
+  p.a = a;
+  p.total_len = a.prior_len + a.chunk_len;
+  const int64_t kv_rows = a.num_blocks * a.num_kv_heads * kBlockSize;
+  if (kv_rows >= (1ll << 31) - 1) return cudaErrorInvalidValue;
+  p.kv_rows = (int)kv_rows;
+  p.q_tiles = (a.chunk_len + BM - 1) / BM;
+  if (p.q_tiles == 0) return cudaSuccess;
+
+  CUtensorMap tm_q, tm_k, tm_v;
+  {
+    cuuint64_t dims[3] = {HD, (cuuint64_t)a.num_q_heads, (cuuint64_t)a.chunk_len};
+    cuuint64_t strides[2] = {HD * 2, (cuuint64_t)a.num_q_heads * HD * 2};
+    cuuint32_t box[3] = {64, 1, BM};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (encode(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  for (int which = 0; which < 2; ++which) {
+    cuuint64_t dims[2] = {HD, (cuuint64_t)kv_rows};
+    cuuint64_t strides[1] = {HD * 2};
+    cuuint32_t box[2] = {64, kBlockSize};
+    cuuint32_t estr[2] = {1, 1};
+    void* base = const_cast<void*>(which == 0 ? a.k_cache : a.v_cache);
+    if (encode(which == 0 ? &tm_k : &tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.num_q_heads, p.q_tiles);
+  prefill_tc_kernel<<<grid, kThreadsTC, SMEM_BYTES, stream>>>(p, tm_q, tm_k, tm_v);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv
