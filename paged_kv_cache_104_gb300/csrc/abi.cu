@@ -56,7 +56,9 @@ pkv_status check_heads(int num_q_heads, int num_kv_heads, int head_dim, int bloc
   if (num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 || block_size < 1) return PKV_EINVAL;
   if (num_q_heads % num_kv_heads != 0) return PKV_EINVAL;
   if (block_size != pkv::kBlockSize) return PKV_EUNSUPPORTED;
-  if (!pkv::decode_supported(dtype == PKV_BF16, head_dim, num_q_heads / num_kv_heads))
+  const int group = num_q_heads / num_kv_heads;
+  if (!pkv::decode_supported(dtype == PKV_BF16, head_dim, group) &&
+      !pkv::decode_mma_supported(dtype == PKV_BF16, head_dim, group))
     return PKV_EUNSUPPORTED;
   return PKV_OK;
 }
@@ -181,9 +183,11 @@ pkv_status pkv_paged_decode_attention(void* out, const void* q, const void* k_ca
   a.scale = scale;
   a.chunk_prior = -1;
   a.is_bf16 = dtype == PKV_BF16;
-  return pkv::launch_paged_decode(a, sms, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? PKV_OK
-             : PKV_ECUDA;
+  cudaStream_t s_ = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t e = pkv::decode_mma_supported(a.is_bf16, head_dim, num_q_heads / num_kv_heads)
+                            ? pkv::launch_paged_decode_mma(a, sms, s_)
+                            : pkv::launch_paged_decode(a, sms, s_);
+  return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
 pkv_status pkv_chunked_prefill_attention(void* out, const void* q, const void* k_cache,

@@ -1,5 +1,6 @@
-// Paged grouped-query decode attention for sm_103a: split-K main kernel and
-// the reduce kernel that merges split partials.
+// Paged grouped-query decode attention on CUDA cores for fp32 storage (the
+// bf16 path runs on tensor-core tiles in decode_mma.cu), plus the reduce
+// kernel that merges split-K partials for both.
 //
 // What it computes ("KV cache and continuous batching: 1,000 people ask AI",
 // section "What does a KV cache keep?"; "The KV cache and prefix caching",
@@ -37,6 +38,7 @@
 //    chunk: row b is a query at position chunk_prior + b whose keys are the
 //    first chunk_prior + b + 1 tokens of one block-table row.
 #include "common.cuh"
+#include "decode_common.cuh"
 #include "launch.h"
 
 namespace pkv {
@@ -74,64 +76,6 @@ struct Cfg {
   static_assert(kSplitTokens % STAGE_TOK == 0, "split holds whole stages");
   static_assert(32 % BPS == 0, "a stage never straddles two block-id windows");
 };
-
-struct Unit {
-  int b, g, s, ns, tok_begin, tok_end;
-};
-
-// Length of row b (0 if the row is invalid; then err is set by the planner).
-__device__ __forceinline__ int row_len(const DecodeArgs& a, int b) {
-  return a.chunk_prior >= 0 ? a.chunk_prior + b + 1 : a.seq_lens[b];
-}
-
-// Build cu[0..B] (units per sequence, prefix-summed) with warp 0.
-__device__ void plan_units(const DecodeArgs& a, int* cu) {
-  const int lane = threadIdx.x & 31;
-  if (threadIdx.x < 32) {
-    int carry = 0;
-    if (lane == 0) cu[0] = 0;
-    const int limit = min(a.max_seq_len, a.max_blocks_per_seq * kBlockSize);
-    for (int base = 0; base < a.num_seqs; base += 32) {
-      const int b = base + lane;
-      int units = 0;
-      if (b < a.num_seqs) {
-        const int n = row_len(a, b);
-        if (n < 1 || n > limit) {
-          record_error(a.err, DEVERR_SEQLEN_RANGE);
-        } else {
-          units = a.num_kv_heads * ((n + a.split_tokens - 1) / a.split_tokens);
-        }
-      }
-      int x = units;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(kFull, x, o);
-        if (lane >= o) x += y;
-      }
-      if (b < a.num_seqs) cu[b + 1] = carry + x;
-      carry += __shfl_sync(kFull, x, 31);
-    }
-  }
-}
-
-__device__ __forceinline__ Unit find_unit(const DecodeArgs& a, const int* cu, int w) {
-  // largest b with cu[b] <= w  (cu is non-decreasing, cu[0] = 0 <= w < cu[B])
-  int lo = 0, hi = a.num_seqs - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (cu[mid] <= w) lo = mid; else hi = mid - 1;
-  }
-  Unit u;
-  u.b = lo;
-  const int rem = w - cu[lo];
-  u.ns = (cu[lo + 1] - cu[lo]) / a.num_kv_heads;
-  u.g = rem / u.ns;
-  u.s = rem - u.g * u.ns;
-  const int n = row_len(a, lo);
-  u.tok_begin = u.s * a.split_tokens;
-  u.tok_end = min(n, u.tok_begin + a.split_tokens);
-  return u;
-}
 
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kThreads, 2)
@@ -443,6 +387,13 @@ decode_reduce_kernel(const DecodeArgs a) {
   }
 }
 
+template <typename T, int D>
+cudaError_t launch_reduce_typed(const DecodeArgs& a, cudaStream_t stream) {
+  const int warps = a.num_seqs * a.num_q_heads;
+  decode_reduce_kernel<T, D><<<(warps + 7) / 8, 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
 template <typename T, int D, int G>
 cudaError_t launch_typed(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
   using C = Cfg<T, D, G>;
@@ -458,9 +409,7 @@ cudaError_t launch_typed(const DecodeArgs& a, int num_sms, cudaStream_t stream) 
   decode_split_kernel<T, D, G><<<grid, kThreads, smem, stream>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.max_splits <= 1) return e;
-  const int warps = a.num_seqs * a.num_q_heads;
-  decode_reduce_kernel<T, D><<<(warps + 7) / 8, 256, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_reduce_typed<T, D>(a, stream);
 }
 
 template <typename T, int D>
@@ -476,20 +425,19 @@ cudaError_t launch_group(const DecodeArgs& a, int num_sms, cudaStream_t stream) 
 
 }  // namespace
 
+cudaError_t launch_decode_reduce_bf16_128(const DecodeArgs& a, cudaStream_t stream) {
+  return launch_reduce_typed<__nv_bfloat16, 128>(a, stream);
+}
+
 bool decode_supported(int is_bf16, int head_dim, int group) {
   const bool g_ok = group == 1 || group == 2 || group == 4 || group == 8;
-  if (!g_ok) return false;
-  if (is_bf16) return head_dim == 128;
-  return head_dim == 16 || head_dim == 128;
+  return g_ok && !is_bf16 && (head_dim == 16 || head_dim == 128);
 }
 
 cudaError_t launch_paged_decode(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
-  if (a.is_bf16) {
-    if (a.head_dim == 128) return launch_group<__nv_bfloat16, 128>(a, num_sms, stream);
-  } else {
-    if (a.head_dim == 16) return launch_group<float, 16>(a, num_sms, stream);
-    if (a.head_dim == 128) return launch_group<float, 128>(a, num_sms, stream);
-  }
+  if (a.is_bf16) return cudaErrorInvalidValue;  // bf16 runs on the tensor-core kernels
+  if (a.head_dim == 16) return launch_group<float, 16>(a, num_sms, stream);
+  if (a.head_dim == 128) return launch_group<float, 128>(a, num_sms, stream);
   return cudaErrorInvalidValue;
 }
 

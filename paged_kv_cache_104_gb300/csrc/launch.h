@@ -53,6 +53,12 @@ struct DecodeArgs {
 // True if (dtype, head_dim, group) has a compiled decode kernel.
 bool decode_supported(int is_bf16, int head_dim, int group);
 cudaError_t launch_paged_decode(const DecodeArgs& a, int num_sms, cudaStream_t stream);
+// Tensor-core (mma.sync) decode for bf16, head_dim 128, group in {1,2,4,8,16};
+// decode mode only (chunk_prior < 0).  Launches the split reduce when needed.
+bool decode_mma_supported(int is_bf16, int head_dim, int group);
+cudaError_t launch_paged_decode_mma(const DecodeArgs& a, int num_sms, cudaStream_t stream);
+// Merge of split partials for bf16 / head_dim 128 (used by the mma decode).
+cudaError_t launch_decode_reduce_bf16_128(const DecodeArgs& a, cudaStream_t stream);
 
 struct PrefillArgs {
   void* out;

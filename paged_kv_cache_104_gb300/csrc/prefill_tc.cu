@@ -31,6 +31,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "tmap.h"
 
 namespace pkv {
 namespace {
@@ -451,31 +452,10 @@ prefill_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CU
   }
 }
 
-// --- host side: tensor maps through the driver entry point ------------------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
-  return fn;
-}
-
 }  // namespace
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, int num_sms, cudaStream_t stream) {
   (void)num_sms;
-  EncodeTiledFn encode = get_encode_fn();
-  if (!encode) return cudaErrorNotSupported;
   TcParams p;
   p.a = a;
   p.total_len = a.prior_len + a.chunk_len;
@@ -484,29 +464,11 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, int num_sms, cudaStream_t st
   p.kv_rows = (int)kv_rows;
   p.q_tiles = (a.chunk_len + BM - 1) / BM;
   if (p.q_tiles == 0) return cudaSuccess;
-
   CUtensorMap tm_q, tm_k, tm_v;
-  {
-    cuuint64_t dims[3] = {HD, (cuuint64_t)a.num_q_heads, (cuuint64_t)a.chunk_len};
-    cuuint64_t strides[2] = {HD * 2, (cuuint64_t)a.num_q_heads * HD * 2};
-    cuuint32_t box[3] = {64, 1, BM};
-    cuuint32_t estr[3] = {1, 1, 1};
-    if (encode(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  for (int which = 0; which < 2; ++which) {
-    cuuint64_t dims[2] = {HD, (cuuint64_t)kv_rows};
-    cuuint64_t strides[1] = {HD * 2};
-    cuuint32_t box[2] = {64, kBlockSize};
-    cuuint32_t estr[2] = {1, 1};
-    void* base = const_cast<void*>(which == 0 ? a.k_cache : a.v_cache);
-    if (encode(which == 0 ? &tm_k : &tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
+  if (!encode_rows_map_bf16(&tm_q, a.q, a.chunk_len, a.num_q_heads) ||
+      !encode_pool_map_bf16(&tm_k, a.k_cache, kv_rows) ||
+      !encode_pool_map_bf16(&tm_v, a.v_cache, kv_rows))
+    return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        SMEM_BYTES);
   if (e != cudaSuccess) return e;

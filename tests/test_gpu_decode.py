@@ -60,7 +60,8 @@ def test_decode_ragged_full_size_sampled():
 
 @pytest.mark.parametrize("dtype,hq,hkv,d", [
     (torch.bfloat16, 32, 8, 128), (torch.bfloat16, 8, 8, 128), (torch.bfloat16, 16, 8, 128),
-    (torch.bfloat16, 16, 2, 128), (torch.float32, 8, 2, 128), (torch.float32, 4, 2, 16),
+    (torch.bfloat16, 16, 2, 128), (torch.bfloat16, 16, 1, 128), (torch.float32, 8, 2, 128),
+    (torch.float32, 4, 2, 16),
     (torch.float32, 8, 1, 16), (torch.float32, 4, 4, 16)])
 def test_decode_edge_lengths_and_groups(dtype, hq, hkv, d):
     """Lengths at block (16) and split (512) boundaries, one token, every
