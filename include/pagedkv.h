@@ -31,8 +31,8 @@
  *   query attends over its own key as well.
  *   Memory: every pointer except those named "host" is a device pointer the
  *   caller owns; the library allocates no memory and keeps no state between
- *   calls other than a per-device error word.  Pointers must be 16-byte
- *   aligned.
+ *   calls other than a per-device error word (and the scratch array of
+ *   pkv_paged_decode_attention_noalloc).  Pointers must be 16-byte aligned.
  *   Streams: work is enqueued on `stream` (NULL = the legacy default stream)
  *   and the call returns without synchronising.
  *   Errors: argument errors are found on the host and returned before any
@@ -121,6 +121,42 @@ pkv_status pkv_paged_decode_attention(void *out, const void *q, const void *k_ca
                                       int head_dim, int block_size, float scale,
                                       void *workspace, size_t workspace_bytes, pkv_dtype dtype,
                                       pkv_stream_t stream);
+
+/* Size of the scratch buffer pkv_paged_decode_attention_noalloc keeps inside
+ * the library (32 MiB; held by every GPU that loads the library until exit). */
+#define PKV_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * paged_decode_attention_noalloc -- paged_decode_attention for callers that
+ * cannot allocate device memory.  The pages have no counterpart to this call.
+ *
+ * Who needs it: an engine that reserves all device memory in its own pool at
+ * start-up and allows no later cudaMalloc (a late allocation can fail under
+ * memory pressure, fragment the pool or synchronise the device mid-step), or
+ * a plugin interface that hands over only input and output pointers.  Such a
+ * caller has no workspace to pass, so this call uses a scratch array that
+ * lives in the library itself (PKV_NOALLOC_SCRATCH_BYTES) instead.
+ *   Arguments, layouts and results are those of pkv_paged_decode_attention
+ *   without workspace / workspace_bytes.  The caller still provides every
+ *   input and output buffer.
+ *   Returns PKV_ERANGE, before any launch, when
+ *   pkv_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len)
+ *   exceeds PKV_NOALLOC_SCRATCH_BYTES.
+ *   Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   The first call on a device looks up the scratch array's device address
+ *   (cudaGetSymbolAddress); make that first call before capturing any stream.
+ *   All calls share the one array, which keeps the last call's contents (no
+ *   part of it needs to start at zero).  Calls whose kernels overlap on the
+ *   GPU -- on different streams or from different host threads -- race on it
+ *   and produce wrong results; the caller must serialise them.
+ */
+pkv_status pkv_paged_decode_attention_noalloc(void *out, const void *q, const void *k_cache,
+                                              const void *v_cache, const int32_t *block_table,
+                                              const int32_t *seq_lens, int num_seqs,
+                                              int max_blocks_per_seq, int max_seq_len,
+                                              int64_t num_blocks, int num_q_heads,
+                                              int num_kv_heads, int head_dim, int block_size,
+                                              float scale, pkv_dtype dtype, pkv_stream_t stream);
 
 /*
  * chunked_prefill_attention -- a chunk of one sequence's prompt attends

@@ -23,8 +23,9 @@ PKV_F32, PKV_BF16 = 0, 1
 DEVERR = {0: "none", 1: "slot out of range", 2: "block id out of range",
           3: "sequence length out of range", 4: "internal wait timed out"}
 EXPORTS = ("pkv_kv_append", "pkv_decode_workspace_bytes", "pkv_paged_decode_attention",
-           "pkv_chunked_prefill_attention", "pkv_get_device_error", "pkv_status_str",
-           "pkv_abi_version")
+           "pkv_paged_decode_attention_noalloc", "pkv_chunked_prefill_attention",
+           "pkv_get_device_error", "pkv_status_str", "pkv_abi_version")
+NOALLOC_SCRATCH_BYTES = 32 << 20  # PKV_NOALLOC_SCRATCH_BYTES
 
 
 class PagedKVError(RuntimeError):
@@ -51,10 +52,13 @@ def load():
                                                    p, sz, i, p]
         lib.pkv_chunked_prefill_attention.argtypes = [p, p, p, p, p, i, i, i, i64, i, i, i, i, f,
                                                       i, p]
+        lib.pkv_paged_decode_attention_noalloc.argtypes = [p, p, p, p, p, p, i, i, i, i64, i, i,
+                                                           i, i, f, i, p]
         lib.pkv_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int), i]
         lib.pkv_status_str.argtypes = [i]
         lib.pkv_status_str.restype = ctypes.c_char_p
         for name in ("pkv_kv_append", "pkv_paged_decode_attention",
+                     "pkv_paged_decode_attention_noalloc",
                      "pkv_chunked_prefill_attention", "pkv_get_device_error", "pkv_abi_version"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -122,6 +126,21 @@ def paged_decode_attention(out, q, k_cache, v_cache, block_table, seq_lens, max_
         b, int(block_table.shape[1]), int(max_seq_len), nb, hq, hkv, d, bs, float(scale),
         _ptr(workspace), ws_bytes, _dtype_code(q), _stream(stream))
     _check("pkv_paged_decode_attention", st)
+
+
+def paged_decode_attention_noalloc(out, q, k_cache, v_cache, block_table, seq_lens,
+                                   max_seq_len: int, scale: float, stream=None) -> None:
+    """paged_decode_attention without a workspace argument: the split partials
+    go to a scratch array inside the library (NOALLOC_SCRATCH_BYTES, shared by
+    every call; calls that overlap on the GPU race).  For callers that may not
+    allocate device memory."""
+    b, hq, d = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    st = load().pkv_paged_decode_attention_noalloc(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
+        b, int(block_table.shape[1]), int(max_seq_len), nb, hq, hkv, d, bs, float(scale),
+        _dtype_code(q), _stream(stream))
+    _check("pkv_paged_decode_attention_noalloc", st)
 
 
 def chunked_prefill_attention(out, q, k_cache, v_cache, block_table_row, prior_len: int,
