@@ -356,7 +356,7 @@ def run_ours(args, w, lay, acct):
     hbm_peak, bf16_peak, peak_src = measured_peaks()
     dec_avg = sum(dec_ms) / len(dec_ms)
     dec_gbs = acct["decode_bytes_layer"] / (dec_avg / 1e3) / 1e9
-    traffic = profiled_traffic("decode_split_kernel", "decode.cu")
+    traffic = profiled_traffic("decode_mma_kernel", "decode_mma.cu")
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": n, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,

@@ -75,6 +75,7 @@ typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
 #define PKV_DEVERR_BLOCK_RANGE 2  /* block-table entry outside [0, num_blocks) (block 0 read instead) */
 #define PKV_DEVERR_SEQLEN_RANGE 3 /* sequence length < 1 or beyond its bound (sequence skipped) */
 #define PKV_DEVERR_TIMEOUT 4      /* an internal wait ran out of time (results unspecified) */
+#define PKV_DEVERR_SMEM_LAYOUT 5  /* shared memory not laid out as a kernel needs (call skipped) */
 
 /* Largest num_seqs accepted by paged_decode_attention. */
 #define PKV_MAX_SEQS 8192

@@ -21,7 +21,8 @@ _lock = threading.Lock()
 
 PKV_F32, PKV_BF16 = 0, 1
 DEVERR = {0: "none", 1: "slot out of range", 2: "block id out of range",
-          3: "sequence length out of range", 4: "internal wait timed out"}
+          3: "sequence length out of range", 4: "internal wait timed out",
+          5: "shared-memory layout check failed"}
 EXPORTS = ("pkv_kv_append", "pkv_decode_workspace_bytes", "pkv_paged_decode_attention",
            "pkv_paged_decode_attention_noalloc", "pkv_chunked_prefill_attention",
            "pkv_get_device_error", "pkv_status_str", "pkv_abi_version")

@@ -1,9 +1,9 @@
 // Device helpers shared by the paged-KV kernels: mbarriers with bounded
 // waits, 1-D bulk (TMA) copies, bf16 unpacking, error reporting.
 //
-// Every wait on an mbarrier is bounded: after kWaitLimitNs of wall time (or
-// kWaitLimitIters polls) it gives up, records PKV_DEVERR_TIMEOUT in the
-// caller's error word and returns false.  Kernels never trap.
+// Every wait on an mbarrier is bounded: after about a second (kWaitLimitCycles
+// SM cycles, or kWaitLimitIters polls) it gives up, records PKV_DEVERR_TIMEOUT
+// in the caller's error word and returns false.  Kernels never trap.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -19,9 +19,13 @@ enum DevErr : int {
   DEVERR_BLOCK_RANGE = 2,   // a block-table entry outside [0, num_blocks)
   DEVERR_SEQLEN_RANGE = 3,  // a sequence length < 1 or beyond its bound
   DEVERR_TIMEOUT = 4,       // an mbarrier wait ran out of time
+  DEVERR_SMEM_LAYOUT = 5,   // dynamic shared memory not 1 KiB aligned (kernel skipped)
 };
 
-constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+// Wait limits: 2^31 SM cycles (about 1 s at GB300 clocks), checked every 64
+// polls with the SM-local cycle counter (cheap, unlike %globaltimer), and at
+// most 2^28 polls in any case.
+constexpr long long kWaitLimitCycles = 1ll << 31;
 constexpr unsigned int kWaitLimitIters = 1u << 28;
 
 __device__ __forceinline__ void record_error(int* err, int code) {
@@ -30,12 +34,6 @@ __device__ __forceinline__ void record_error(int* err, int code) {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long globaltimer_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
 }
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -68,14 +66,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete, for at most
-// kWaitLimitNs.  Returns false (and records DEVERR_TIMEOUT) on time-out.
+// Wait for the phase with the given parity to complete, for at most about
+// one second.  Returns false (and records DEVERR_TIMEOUT) on time-out.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err) {
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
+  const long long t0 = clock64();
   for (unsigned int it = 0; it < kWaitLimitIters; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+    if ((it & 63u) == 63u && clock64() - t0 > kWaitLimitCycles) break;
   }
   record_error(err, DEVERR_TIMEOUT);
   return false;
