@@ -214,7 +214,10 @@ pkv_status pkv_chunked_prefill_attention(void* out, const void* q, const void* k
   if (dtype == PKV_BF16 && head_dim == 128) {
     pkv::PrefillArgs a{out, q, k_cache, v_cache, block_table_row, max_blocks, prior_len, chunk_len,
                        num_blocks, num_q_heads, num_kv_heads, scale, err};
-    return pkv::launch_prefill_tc(a, sms, s) == cudaSuccess ? PKV_OK : PKV_ECUDA;
+    const cudaError_t e = pkv::prefill_pair_supported(num_q_heads, num_kv_heads)
+                              ? pkv::launch_prefill_pair(a, s)
+                              : pkv::launch_prefill_tc(a, sms, s);
+    return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
   }
   // CUDA-core path: every chunk row is one query over its causal prefix, run
   // as a single split so no workspace is needed.

@@ -75,7 +75,10 @@ struct PrefillArgs {
   float scale;
   int* err;
 };
-// tcgen05 path: bf16, head_dim 128, block_size 16.
+// tcgen05 path, one query head per CTA: bf16, head_dim 128, block_size 16.
 cudaError_t launch_prefill_tc(const PrefillArgs& a, int num_sms, cudaStream_t stream);
+// tcgen05 path, two query heads of one GQA group per CTA (group size even).
+bool prefill_pair_supported(int num_q_heads, int num_kv_heads);
+cudaError_t launch_prefill_pair(const PrefillArgs& a, cudaStream_t stream);
 
 }  // namespace pkv

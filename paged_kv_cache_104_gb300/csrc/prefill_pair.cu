@@ -1,0 +1,412 @@
+// Chunked-prefill attention on tcgen05 for two query heads of one GQA group
+// per CTA (sm_103a).
+//
+// What it computes ("The KV cache is not your bottleneck", section "The fix
+// that mattered": prompts are admitted in capped chunks; "KV cache and
+// continuous batching: 1,000 people ask AI", section "What does a KV cache
+// keep?": prefill is matrix-matrix work): chunk row i of one sequence, at
+// absolute position prior + i, attends keys 0 .. prior + i of that sequence:
+// out[i][h] = softmax(scale * q[i][h] . K^T) V, K and V of KV head h / G.
+//
+// Why this shape.  A 16-token cache block is 16 rows; with the 128-byte
+// swizzle a TMA box can then carry at most 2 KiB, and the SM's TMA unit
+// delivers such boxes at only ~15-20 B/clk -- too little for a
+// tensor-bound kernel that re-reads K/V from L2 for every query tile.  So:
+//  * K/V are gathered through the block table with 16-byte cp.async copies by
+//    two producer warps, written straight into the 128B-swizzled K-major
+//    layout the MMAs read; rows past the sequence end are zero-filled by the
+//    copy itself (source size 0), so stale pool contents never enter.
+//  * Each CTA serves 128 query rows of two query heads of the same KV head,
+//    so every K/V tile feeds 256 rows (half the load per flop of one head).
+//  * A 4-stage K/V ring (32 KiB per 64-key stage) keeps several tiles in
+//    flight; one CTA per SM (224 KiB of shared memory, all 512 TMEM columns).
+// Roles (352 threads):
+//   warps 0-3 / 4-7   softmax of head A / head B: thread r owns query row r
+//                     (TMEM lane r); S row via tcgen05.ld, causal mask on the
+//                     diagonal tiles, lazily raised running max (only when it
+//                     grows by more than 2^8) and sum, p = 2^(s*scale*log2e - m)
+//                     with one FMA and ex2 per score, P (bf16) into the
+//                     swizzled A-operand tile, O row rescaled in TMEM when the
+//                     max moved; epilogue O / l.
+//   warps 8-9         K/V producers (cp.async, then a proxy fence and an
+//                     mbarrier arrive once their copies of a tile landed).
+//   warp 10           TMEM allocator and single-thread MMA issuer:
+//                     S[h][j%2] = Q_h K_j^T (M=128, N=64, K=128), then
+//                     O_h += P_h V_j (M=128, N=128, K=64, V MN-major).
+// Every mbarrier wait is bounded; on time-out the kernel records an error,
+// stops issuing work, lets its copies land, frees its TMEM and returns.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "tc_common.cuh"
+#include "tmap.h"
+
+namespace pkv {
+namespace {
+
+constexpr int BM = 128, BN = 64, HD = 128;
+constexpr int QHALF = BM * 128;               // one 64-column half of a Q tile, 16 KiB
+constexpr int Q_BYTES = 2 * QHALF;            // 32 KiB per head
+constexpr int KHALF = BN * 128;               // one 64-column half of a K/V tile, 8 KiB
+constexpr int KV_TILE = 2 * KHALF;            // 16 KiB
+constexpr int STAGE = 2 * KV_TILE;            // K + V of 64 keys
+constexpr int NST = 4;
+constexpr int P_BYTES = BM * 128;             // 128 rows x 64 keys bf16
+constexpr int OFF_Q = 0;                      // [head][Q tile]
+constexpr int OFF_KV = 2 * Q_BYTES;           // [stage][K | V]
+constexpr int OFF_P = OFF_KV + NST * STAGE;   // [head][P tile]
+constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+constexpr int SMEM_BYTES = OFF_BAR + 256;
+constexpr int kSoftThreads = 256;
+constexpr int kProdThreads = 64;
+constexpr int W_PROD = 8, W_MMA = 10;
+constexpr int kThreadsPair = kSoftThreads + kProdThreads + 32;
+constexpr uint32_t kTmemColsPair = 512;
+constexpr uint32_t COL_O = 4 * BN;            // S[head][buf] at (2*head + buf)*64, O[head] at 256 + 128*head
+constexpr float kLazyP = 8.0f;
+static_assert(SMEM_BYTES <= 227 * 1024, "one CTA per SM");
+
+// barrier slots
+enum {
+  PB_Q = 0,
+  PB_KVF = 1,                 // [NST]
+  PB_KVE = PB_KVF + NST,      // [NST]
+  PB_SF = PB_KVE + NST,       // [head][buf]
+  PB_SE = PB_SF + 4,          // [head][buf]
+  PB_PF = PB_SE + 4,          // [head]
+  PB_OD = PB_PF + 2,          // [head]
+  PB_COUNT = PB_OD + 2
+};
+static_assert(PB_COUNT * 8 + 8 <= 256, "barrier area");
+
+struct PairParams {
+  PrefillArgs a;
+  int total_len;
+  int kv_rows;
+  int q_tiles;
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__global__ void __launch_bounds__(kThreadsPair, 1)
+prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant__ CUtensorMap tm_q) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + PB_COUNT);
+  int* abort_i = reinterpret_cast<int*>(tmem_slot + 1);
+  volatile int* abort_flag = abort_i;
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+  const PrefillArgs& a = p.a;
+  if (sbase & 1023u) {  // swizzled operand tiles need a 1 KiB-aligned base
+    if (threadIdx.x == 0) record_error(a.err, DEVERR_SMEM_LAYOUT);
+    return;
+  }
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int group = a.num_q_heads / a.num_kv_heads;
+  const int h0 = 2 * blockIdx.x;                          // heads h0, h0 + 1
+  const int g = h0 / group;                               // their KV head
+  const int qt = p.q_tiles - 1 - (int)blockIdx.y;         // heaviest tiles first
+  const int q0 = qt * BM;
+  const int last_row_pos = a.prior_len + min(a.chunk_len, q0 + BM) - 1;
+  const int n_tiles = last_row_pos / BN + 1;
+
+  if (tid == 0) {
+    mbar_init(bar(PB_Q), 1);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(bar(PB_KVF + s), kProdThreads);
+      mbar_init(bar(PB_KVE + s), 1);
+    }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(bar(PB_SF + i), 1);
+      mbar_init(bar(PB_SE + i), 128);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(PB_PF + i), 128);
+      mbar_init(bar(PB_OD + i), 1);
+    }
+    *abort_i = 0;
+    fence_mbar_init();
+  }
+  if (warp == W_MMA) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemColsPair));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp >= W_PROD && warp < W_MMA) {
+    // ------------------------------------------------------------- K/V producers
+    const int pt = tid - kSoftThreads;          // 0..63
+    const int rsub = pt >> 4, cc = pt & 15;     // row within a group of 4, 16-byte chunk
+    const int half = cc >> 3, ch = cc & 7;
+    const __nv_bfloat16* kc = static_cast<const __nv_bfloat16*>(a.k_cache);
+    const __nv_bfloat16* vc = static_cast<const __nv_bfloat16*>(a.v_cache);
+    const int nblk_seq = (p.total_len + kBlockSize - 1) / kBlockSize;
+    // block ids of the sequence, 32 per window (one per lane), next window prefetched
+    auto load_ids = [&](int win) {
+      const int idx = win * 32 + lane;
+      int blk = 0;
+      if (idx < nblk_seq) {
+        blk = __ldg(a.block_table_row + idx);
+        if (blk < 0 || (int64_t)blk >= a.num_blocks) {
+          record_error(a.err, DEVERR_BLOCK_RANGE);
+          blk = 0;
+        }
+      }
+      return blk;
+    };
+    constexpr int kTilesPerWin = 32 / (BN / kBlockSize);
+    int cur_ids = load_ids(0), next_ids = load_ids(1);
+    int issued = 0;
+    for (int j = 0; j < n_tiles; ++j) {
+      if (j > 0 && j % kTilesPerWin == 0) {
+        cur_ids = next_ids;
+        next_ids = load_ids(j / kTilesPerWin + 1);
+      }
+      const int st = j % NST;
+      bool go = true;
+      if (j >= NST) go = wait_or_abort(bar(PB_KVE + st), ((j / NST) - 1) & 1, abort_flag, a.err);
+      if (!__all_sync(0xffffffffu, go && !*abort_flag)) break;  // leave the loop as a warp
+      const uint32_t kdst = sbase + OFF_KV + st * STAGE, vdst = kdst + KV_TILE;
+#pragma unroll
+      for (int bi = 0; bi < BN / kBlockSize; ++bi) {
+        const int blk = __shfl_sync(0xffffffffu, cur_ids, ((j % kTilesPerWin) * (BN / kBlockSize) + bi) & 31);
+        const int64_t tile = ((int64_t)blk * a.num_kv_heads + g) * (kBlockSize * HD);
+#pragma unroll
+        for (int rq = 0; rq < kBlockSize / 4; ++rq) {
+          const int rr = rq * 4 + rsub;               // row within the block
+          const int row = bi * kBlockSize + rr;       // row within the 64-key tile
+          const int tok = j * BN + row;
+          const uint32_t nbytes = tok < p.total_len ? 16u : 0u;   // zero-fill past the end
+          const int64_t src = tile + rr * HD + cc * 8;
+          const uint32_t doff = half * KHALF + row * 128 + ((ch ^ (row & 7)) << 4);
+          cp_async16(kdst + doff, kc + src, nbytes);
+          cp_async16(vdst + doff, vc + src, nbytes);
+        }
+      }
+      cp_async_commit();
+      if (j >= 1) {
+        cp_async_wait<1>();                 // this thread's copies of tile j-1 landed
+        fence_proxy_async_smem();           // make them visible to the tensor core
+        mbar_arrive(bar(PB_KVF + (j - 1) % NST));
+      }
+      issued = j + 1;
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    if (issued > 0 && !*abort_flag) mbar_arrive(bar(PB_KVF + (issued - 1) % NST));
+  } else if (warp == W_MMA) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
+      mbar_arrive_expect_tx(bar(PB_Q), 2 * Q_BYTES);
+      for (int hh = 0; hh < 2; ++hh) {
+        tma_load_3d(sbase + OFF_Q + hh * Q_BYTES, &tm_q, bar(PB_Q), 0, h0 + hh, q0);
+        tma_load_3d(sbase + OFF_Q + hh * Q_BYTES + QHALF, &tm_q, bar(PB_Q), 64, h0 + hh, q0);
+      }
+      constexpr uint32_t idesc_qk = make_idesc(false, BM, BN);
+      constexpr uint32_t idesc_pv = make_idesc(true, BM, HD);
+      bool ok = wait_or_abort(bar(PB_Q), 0, abort_flag, a.err);
+      tc_fence_after();
+      auto issue_pv = [&](int jj) {
+        const int st = jj % NST;
+        const uint32_t vb = sbase + OFF_KV + st * STAGE + KV_TILE;
+        for (int hh = 0; hh < 2; ++hh) {
+          if (!wait_or_abort(bar(PB_PF + hh), jj & 1, abort_flag, a.err)) return false;
+          tc_fence_after();
+          const uint32_t pa = sbase + OFF_P + hh * P_BYTES;
+#pragma unroll
+          for (int k = 0; k < BN / 16; ++k) {
+            const uint64_t ad = make_sw128_desc(pa + k * 32, 16, 1024);
+            const uint64_t bd = make_sw128_desc(vb + k * 16 * 128, KHALF, 1024);
+            mma_bf16(tmem + COL_O + hh * HD, ad, bd, idesc_pv, (jj > 0 || k > 0) ? 1u : 0u);
+          }
+          mma_commit(bar(PB_OD + hh));
+        }
+        mma_commit(bar(PB_KVE + st));
+        return true;
+      };
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int st = j % NST, sb = j & 1;
+        ok = wait_or_abort(bar(PB_KVF + st), (j / NST) & 1, abort_flag, a.err);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t kb = sbase + OFF_KV + st * STAGE;
+        for (int hh = 0; hh < 2 && ok; ++hh) {
+          if (j >= 2) ok = wait_or_abort(bar(PB_SE + 2 * hh + sb), ((j >> 1) - 1) & 1, abort_flag, a.err);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t qa = sbase + OFF_Q + hh * Q_BYTES;
+#pragma unroll
+          for (int k = 0; k < HD / 16; ++k) {
+            const uint64_t ad = make_sw128_desc(qa + (k >> 2) * QHALF + (k & 3) * 32, 16, 1024);
+            const uint64_t bd = make_sw128_desc(kb + (k >> 2) * KHALF + (k & 3) * 32, 16, 1024);
+            mma_bf16(tmem + (2 * hh + sb) * BN, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(PB_SF + 2 * hh + sb));
+        }
+        if (ok && j >= 1) ok = issue_pv(j - 1);
+      }
+      if (ok) issue_pv(n_tiles - 1);
+      if (*abort_flag) mbar_wait(bar(PB_Q), 0, nullptr);  // let the Q loads land
+    }
+  } else {
+    // ------------------------------------------------------------- softmax (head hh)
+    const int hh = warp >> 2;               // 0: warps 0-3, 1: warps 4-7
+    const int r = tid & 127;                // query row in the tile, TMEM lane
+    const int row_pos = a.prior_len + q0 + r;
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t col_o = COL_O + hh * HD;
+    const float sl2 = a.scale * 1.4426950408889634f;
+    float m_run = -INFINITY, l_run = 0.f;   // running max in scaled log2 units
+    unsigned char* prow = smem + OFF_P + hh * P_BYTES + r * 128;
+    const int sw = r & 7;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int sb = j & 1;
+      wait_or_abort(bar(PB_SF + 2 * hh + sb), (j >> 1) & 1, abort_flag, a.err);
+      __syncwarp();
+      tc_fence_after();
+      float s[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        float t[32];
+        tmem_ld32(lane_base + (2 * hh + sb) * BN + c * 32, t);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = t[i];
+      }
+      tmem_wait_ld();
+      reg_fence(s);
+      tc_fence_before();
+      mbar_arrive(bar(PB_SE + 2 * hh + sb));
+      const int k0 = j * BN;
+      if (k0 + BN - 1 > a.prior_len + q0) {   // causal mask on the diagonal tiles
+#pragma unroll
+        for (int c = 0; c < BN; ++c) s[c] = (k0 + c <= row_pos) ? s[c] : -INFINITY;
+      }
+      float mx0 = s[0], mx1 = s[1];
+#pragma unroll
+      for (int c = 2; c < BN; c += 2) {
+        mx0 = fmaxf(mx0, s[c]);
+        mx1 = fmaxf(mx1, s[c + 1]);
+      }
+      const float mx = fmaxf(mx0, mx1) * sl2;
+      float m_new = m_run;
+      if (mx > m_run + kLazyP || m_run == -INFINITY) m_new = mx;
+      const float alpha = (m_new == m_run) ? 1.f : fast_exp2(m_run - m_new);
+      float sum0 = 0.f, sum1 = 0.f;
+      uint32_t packed[BN / 2];
+#pragma unroll
+      for (int c = 0; c < BN; c += 2) {
+        const float p0 = fast_exp2(fmaf(s[c], sl2, -m_new));
+        const float p1 = fast_exp2(fmaf(s[c + 1], sl2, -m_new));
+        sum0 += p0;
+        sum1 += p1;
+        packed[c / 2] = pack_bf16(p0, p1);
+      }
+      if (j >= 1) {  // P_{j-1} V must be done before P is overwritten or O rescaled
+        wait_or_abort(bar(PB_OD + hh), (j - 1) & 1, abort_flag, a.err);
+        __syncwarp();
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+          for (int c = 0; c < HD / 32; ++c) {
+            float o[32];
+            tmem_ld32(lane_base + col_o + c * 32, o);
+            tmem_wait_ld();
+            reg_fence(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(lane_base + col_o + c * 32, o);
+          }
+          tmem_wait_st();
+        }
+      }
+      l_run = l_run * alpha + (sum0 + sum1);
+      m_run = m_new;
+#pragma unroll
+      for (int c8 = 0; c8 < BN / 8; ++c8) {
+        uint4 v = make_uint4(packed[c8 * 4 + 0], packed[c8 * 4 + 1], packed[c8 * 4 + 2],
+                             packed[c8 * 4 + 3]);
+        *reinterpret_cast<uint4*>(prow + ((c8 ^ sw) << 4)) = v;
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(PB_PF + hh));
+    }
+    wait_or_abort(bar(PB_OD + hh), (n_tiles - 1) & 1, abort_flag, a.err);
+    __syncwarp();
+    tc_fence_after();
+    const float inv = 1.f / l_run;
+    const bool row_ok = (q0 + r) < a.chunk_len;
+    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
+                          ((int64_t)(q0 + r) * a.num_q_heads + h0 + hh) * HD;
+#pragma unroll 1
+    for (int c = 0; c < HD / 32; ++c) {
+      float o[32];
+      tmem_ld32(lane_base + col_o + c * 32, o);
+      tmem_wait_ld();
+      reg_fence(o);
+      if (row_ok) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) {
+          uint4 v = make_uint4(pack_bf16(o[i] * inv, o[i + 1] * inv),
+                               pack_bf16(o[i + 2] * inv, o[i + 3] * inv),
+                               pack_bf16(o[i + 4] * inv, o[i + 5] * inv),
+                               pack_bf16(o[i + 6] * inv, o[i + 7] * inv));
+          *reinterpret_cast<uint4*>(orow + c * 32 + i) = v;
+        }
+      }
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (warp == W_MMA) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemColsPair));
+  }
+}
+
+}  // namespace
+
+bool prefill_pair_supported(int num_q_heads, int num_kv_heads) {
+  return (num_q_heads / num_kv_heads) % 2 == 0;
+}
+
+cudaError_t launch_prefill_pair(const PrefillArgs& a, cudaStream_t stream) {
+  PairParams p;
+  p.a = a;
+  p.total_len = a.prior_len + a.chunk_len;
+  const int64_t kv_rows = a.num_blocks * a.num_kv_heads * kBlockSize;
+  if (kv_rows >= (1ll << 31) - 1) return cudaErrorInvalidValue;
+  p.kv_rows = (int)kv_rows;
+  p.q_tiles = (a.chunk_len + BM - 1) / BM;
+  if (p.q_tiles == 0) return cudaSuccess;
+  CUtensorMap tm_q;
+  if (!encode_rows_map_bf16(&tm_q, a.q, a.chunk_len, a.num_q_heads)) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.num_q_heads / 2, p.q_tiles);
+  prefill_pair_kernel<<<grid, kThreadsPair, SMEM_BYTES, stream>>>(p, tm_q);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

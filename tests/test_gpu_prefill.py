@@ -41,6 +41,14 @@ def test_prefill_tcgen05_small_heads(prior, chunk):
     assert G.max_err(got, ref) <= 2e-2
 
 
+@pytest.mark.parametrize("prior,chunk", [(0, 200), (100, 300), (37, 513)])
+def test_prefill_tcgen05_one_head_per_cta(prior, chunk):
+    """Group size 1 (no pair of heads shares a KV head): one query head per CTA."""
+    got, ref = _prefill_case(torch.bfloat16, 4, 4, 128, prior, chunk)
+    assert torch.isfinite(got).all()
+    assert G.max_err(got, ref) <= 2e-2
+
+
 def test_prefill_tcgen05_gqa_heads():
     got, ref = _prefill_case(torch.bfloat16, 16, 4, 128, 300, 260)
     assert G.max_err(got, ref) <= 2e-2
