@@ -8,31 +8,36 @@
 // absolute position prior + i, attends keys 0 .. prior + i of that sequence:
 // out[i][h] = softmax(scale * q[i][h] . K^T) V, K and V of KV head h / G.
 //
-// Why this shape.  A 16-token cache block is 16 rows; with the 128-byte
-// swizzle a TMA box can then carry at most 2 KiB, and the SM's TMA unit
-// delivers such boxes at only ~15-20 B/clk -- too little for a
-// tensor-bound kernel that re-reads K/V from L2 for every query tile.  So:
-//  * K/V are gathered through the block table with 16-byte cp.async copies by
-//    two producer warps, written straight into the 128B-swizzled K-major
-//    layout the MMAs read; rows past the sequence end are zero-filled by the
-//    copy itself (source size 0), so stale pool contents never enter.
-//  * Each CTA serves 128 query rows of two query heads of the same KV head,
-//    so every K/V tile feeds 256 rows (half the load per flop of one head).
-//  * A 4-stage K/V ring (32 KiB per 64-key stage) keeps several tiles in
-//    flight; one CTA per SM (224 KiB of shared memory, all 512 TMEM columns).
+// Why this shape.
+//  * K/V gathers.  A 16-token cache block is 16 rows; with the 128-byte
+//    swizzle a TMA box then carries at most 2 KiB, and the SM's TMA unit
+//    moves such boxes at only ~15-20 B/clk.  K/V are instead gathered through
+//    the block table by two producer warps with 16-byte cp.async copies,
+//    written straight into the 128B-swizzled K-major layout the MMAs read;
+//    rows past the sequence end are zero-filled by the copy (source size 0),
+//    so stale pool contents never enter.
+//  * Shared-memory bandwidth.  Each CTA serves 128 query rows of two query
+//    heads of the same KV head (every K/V tile feeds 256 rows), key tiles are
+//    128 wide (Q K^T as M=128, N=128 instructions), and P never touches shared
+//    memory: the softmax writes it as bf16 into the TMEM columns of its own S,
+//    and P V reads its A operand from TMEM.
+//  * TMEM: S_h (128 columns, P_h aliased over its first 64) and O_h
+//    (128 columns) for the two heads = all 512 columns; one CTA per SM.  The
+//    two heads take turns on the tensor core: while one head's softmax runs,
+//    the other head's products execute.
 // Roles (352 threads):
-//   warps 0-3 / 4-7   softmax of head A / head B: thread r owns query row r
-//                     (TMEM lane r); S row via tcgen05.ld, causal mask on the
-//                     diagonal tiles, lazily raised running max (only when it
-//                     grows by more than 2^8) and sum, p = 2^(s*scale*log2e - m)
-//                     with one FMA and ex2 per score, P (bf16) into the
-//                     swizzled A-operand tile, O row rescaled in TMEM when the
-//                     max moved; epilogue O / l.
-//   warps 8-9         K/V producers (cp.async, then a proxy fence and an
-//                     mbarrier arrive once their copies of a tile landed).
+//   warps 0-3 / 4-7   softmax of head A / B: thread r owns query row r (TMEM
+//                     lane r).  Pass 1 reads its S row in 32-column pieces for
+//                     the row max (causal mask on the diagonal tiles); the max
+//                     is raised lazily, only when it grows by more than 2^8,
+//                     and then O is rescaled in TMEM.  Pass 2 re-reads S, forms
+//                     p = 2^(s*scale*log2e - m) with one FMA and ex2 per score,
+//                     sums it and stores it as bf16 into TMEM.  Epilogue O / l.
+//   warps 8-9         K/V producers (cp.async; once their copies of a tile
+//                     landed: proxy fence, mbarrier arrive).
 //   warp 10           TMEM allocator and single-thread MMA issuer:
-//                     S[h][j%2] = Q_h K_j^T (M=128, N=64, K=128), then
-//                     O_h += P_h V_j (M=128, N=128, K=64, V MN-major).
+//                     S_h = Q_h K_j^T    (A, B from shared memory)
+//                     O_h += P_h V_j     (A from TMEM, V as an MN-major B)
 // Every mbarrier wait is bounded; on time-out the kernel records an error,
 // stops issuing work, lets its copies land, frees its TMEM and returns.
 #include <cuda.h>
@@ -45,25 +50,24 @@
 namespace pkv {
 namespace {
 
-constexpr int BM = 128, BN = 64, HD = 128;
+constexpr int BM = 128, BN = 128, HD = 128;
 constexpr int QHALF = BM * 128;               // one 64-column half of a Q tile, 16 KiB
 constexpr int Q_BYTES = 2 * QHALF;            // 32 KiB per head
-constexpr int KHALF = BN * 128;               // one 64-column half of a K/V tile, 8 KiB
-constexpr int KV_TILE = 2 * KHALF;            // 16 KiB
-constexpr int STAGE = 2 * KV_TILE;            // K + V of 64 keys
-constexpr int NST = 4;
-constexpr int P_BYTES = BM * 128;             // 128 rows x 64 keys bf16
+constexpr int KHALF = BN * 128;               // one 64-column half of a K/V tile, 16 KiB
+constexpr int KV_TILE = 2 * KHALF;            // 32 KiB
+constexpr int STAGE = 2 * KV_TILE;            // K + V of 128 keys, 64 KiB
+constexpr int NST = 2;
 constexpr int OFF_Q = 0;                      // [head][Q tile]
 constexpr int OFF_KV = 2 * Q_BYTES;           // [stage][K | V]
-constexpr int OFF_P = OFF_KV + NST * STAGE;   // [head][P tile]
-constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+constexpr int OFF_BAR = OFF_KV + NST * STAGE;
 constexpr int SMEM_BYTES = OFF_BAR + 256;
 constexpr int kSoftThreads = 256;
 constexpr int kProdThreads = 64;
 constexpr int W_PROD = 8, W_MMA = 10;
 constexpr int kThreadsPair = kSoftThreads + kProdThreads + 32;
 constexpr uint32_t kTmemColsPair = 512;
-constexpr uint32_t COL_O = 4 * BN;            // S[head][buf] at (2*head + buf)*64, O[head] at 256 + 128*head
+constexpr uint32_t COL_S = 0;                 // S_h at 128*h (P_h in its first 64 columns)
+constexpr uint32_t COL_O = 2 * BN;            // O_h at 256 + 128*h
 constexpr float kLazyP = 8.0f;
 static_assert(SMEM_BYTES <= 227 * 1024, "one CTA per SM");
 
@@ -72,9 +76,8 @@ enum {
   PB_Q = 0,
   PB_KVF = 1,                 // [NST]
   PB_KVE = PB_KVF + NST,      // [NST]
-  PB_SF = PB_KVE + NST,       // [head][buf]
-  PB_SE = PB_SF + 4,          // [head][buf]
-  PB_PF = PB_SE + 4,          // [head]
+  PB_SF = PB_KVE + NST,       // [head]
+  PB_PF = PB_SF + 2,          // [head]
   PB_OD = PB_PF + 2,          // [head]
   PB_COUNT = PB_OD + 2
 };
@@ -129,11 +132,8 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
       mbar_init(bar(PB_KVF + s), kProdThreads);
       mbar_init(bar(PB_KVE + s), 1);
     }
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(bar(PB_SF + i), 1);
-      mbar_init(bar(PB_SE + i), 128);
-    }
     for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(PB_SF + i), 1);
       mbar_init(bar(PB_PF + i), 128);
       mbar_init(bar(PB_OD + i), 1);
     }
@@ -172,7 +172,8 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
       }
       return blk;
     };
-    constexpr int kTilesPerWin = 32 / (BN / kBlockSize);
+    constexpr int kBlkPerTile = BN / kBlockSize;   // 8
+    constexpr int kTilesPerWin = 32 / kBlkPerTile;  // 4
     int cur_ids = load_ids(0), next_ids = load_ids(1);
     int issued = 0;
     for (int j = 0; j < n_tiles; ++j) {
@@ -185,14 +186,14 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
       if (j >= NST) go = wait_or_abort(bar(PB_KVE + st), ((j / NST) - 1) & 1, abort_flag, a.err);
       if (!__all_sync(0xffffffffu, go && !*abort_flag)) break;  // leave the loop as a warp
       const uint32_t kdst = sbase + OFF_KV + st * STAGE, vdst = kdst + KV_TILE;
-#pragma unroll
-      for (int bi = 0; bi < BN / kBlockSize; ++bi) {
-        const int blk = __shfl_sync(0xffffffffu, cur_ids, ((j % kTilesPerWin) * (BN / kBlockSize) + bi) & 31);
+#pragma unroll 2
+      for (int bi = 0; bi < kBlkPerTile; ++bi) {
+        const int blk = __shfl_sync(0xffffffffu, cur_ids, ((j % kTilesPerWin) * kBlkPerTile + bi) & 31);
         const int64_t tile = ((int64_t)blk * a.num_kv_heads + g) * (kBlockSize * HD);
 #pragma unroll
         for (int rq = 0; rq < kBlockSize / 4; ++rq) {
           const int rr = rq * 4 + rsub;               // row within the block
-          const int row = bi * kBlockSize + rr;       // row within the 64-key tile
+          const int row = bi * kBlockSize + rr;       // row within the 128-key tile
           const int tok = j * BN + row;
           const uint32_t nbytes = tok < p.total_len ? 16u : 0u;   // zero-fill past the end
           const int64_t src = tile + rr * HD + cc * 8;
@@ -202,16 +203,15 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
         }
       }
       cp_async_commit();
-      if (j >= 1) {
-        cp_async_wait<1>();                 // this thread's copies of tile j-1 landed
-        fence_proxy_async_smem();           // make them visible to the tensor core
-        mbar_arrive(bar(PB_KVF + (j - 1) % NST));
-      }
+      // signal tile j as soon as this thread's copies of it landed (no lag:
+      // the MMA side may wait for tile j before releasing tile j-1's stage)
+      cp_async_wait<0>();
+      fence_proxy_async_smem();             // make them visible to the tensor core
+      mbar_arrive(bar(PB_KVF + st));
       issued = j + 1;
     }
     cp_async_wait<0>();
-    fence_proxy_async_smem();
-    if (issued > 0 && !*abort_flag) mbar_arrive(bar(PB_KVF + (issued - 1) % NST));
+    (void)issued;
   } else if (warp == W_MMA) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
@@ -224,47 +224,55 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
       constexpr uint32_t idesc_qk = make_idesc(false, BM, BN);
       constexpr uint32_t idesc_pv = make_idesc(true, BM, HD);
       bool ok = wait_or_abort(bar(PB_Q), 0, abort_flag, a.err);
-      tc_fence_after();
-      auto issue_pv = [&](int jj) {
-        const int st = jj % NST;
-        const uint32_t vb = sbase + OFF_KV + st * STAGE + KV_TILE;
-        for (int hh = 0; hh < 2; ++hh) {
-          if (!wait_or_abort(bar(PB_PF + hh), jj & 1, abort_flag, a.err)) return false;
-          tc_fence_after();
-          const uint32_t pa = sbase + OFF_P + hh * P_BYTES;
+      // S_h = Q_h K_j^T into the TMEM columns of S_h
+      auto issue_qk = [&](int hh, int j) {
+        const uint32_t kb = sbase + OFF_KV + (j % NST) * STAGE;
+        const uint32_t qa = sbase + OFF_Q + hh * Q_BYTES;
 #pragma unroll
-          for (int k = 0; k < BN / 16; ++k) {
-            const uint64_t ad = make_sw128_desc(pa + k * 32, 16, 1024);
-            const uint64_t bd = make_sw128_desc(vb + k * 16 * 128, KHALF, 1024);
-            mma_bf16(tmem + COL_O + hh * HD, ad, bd, idesc_pv, (jj > 0 || k > 0) ? 1u : 0u);
-          }
-          mma_commit(bar(PB_OD + hh));
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint64_t ad = make_sw128_desc(qa + (k >> 2) * QHALF + (k & 3) * 32, 16, 1024);
+          const uint64_t bd = make_sw128_desc(kb + (k >> 2) * KHALF + (k & 3) * 32, 16, 1024);
+          mma_bf16(tmem + COL_S + hh * BN, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
         }
-        mma_commit(bar(PB_KVE + st));
-        return true;
+        mma_commit(bar(PB_SF + hh));
       };
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const int st = j % NST, sb = j & 1;
-        ok = wait_or_abort(bar(PB_KVF + st), (j / NST) & 1, abort_flag, a.err);
-        if (!ok) break;
+      // O_h += P_h V_j, P_h from TMEM (16 keys = 8 columns per step)
+      auto issue_pv = [&](int hh, int j) {
+        const uint32_t vb = sbase + OFF_KV + (j % NST) * STAGE + KV_TILE;
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          const uint64_t bd = make_sw128_desc(vb + k * 16 * 128, KHALF, 1024);
+          mma_bf16_tmem_a(tmem + COL_O + hh * HD, tmem + COL_S + hh * BN + k * 8, bd, idesc_pv,
+                          (j > 0 || k > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(PB_OD + hh));
+      };
+      // The two heads alternate on the tensor core: while head A's softmax
+      // turns S_A into P_A, the products of head B run, and the other way
+      // round.  S_h (holding P_h) is rewritten only after P_h V has completed.
+      if (ok) ok = wait_or_abort(bar(PB_KVF + 0), 0, abort_flag, a.err);
+      if (ok) {
         tc_fence_after();
-        const uint32_t kb = sbase + OFF_KV + st * STAGE;
+        issue_qk(0, 0);
+        issue_qk(1, 0);
+      }
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const bool more = j + 1 < n_tiles;
         for (int hh = 0; hh < 2 && ok; ++hh) {
-          if (j >= 2) ok = wait_or_abort(bar(PB_SE + 2 * hh + sb), ((j >> 1) - 1) & 1, abort_flag, a.err);
+          ok = wait_or_abort(bar(PB_PF + hh), j & 1, abort_flag, a.err);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t qa = sbase + OFF_Q + hh * Q_BYTES;
-#pragma unroll
-          for (int k = 0; k < HD / 16; ++k) {
-            const uint64_t ad = make_sw128_desc(qa + (k >> 2) * QHALF + (k & 3) * 32, 16, 1024);
-            const uint64_t bd = make_sw128_desc(kb + (k >> 2) * KHALF + (k & 3) * 32, 16, 1024);
-            mma_bf16(tmem + (2 * hh + sb) * BN, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+          issue_pv(hh, j);
+          if (hh == 1) mma_commit(bar(PB_KVE + j % NST));   // tile j no longer needed
+          if (more) {
+            if (hh == 0) ok = wait_or_abort(bar(PB_KVF + (j + 1) % NST), ((j + 1) / NST) & 1, abort_flag, a.err);
+            if (ok) ok = wait_or_abort(bar(PB_OD + hh), j & 1, abort_flag, a.err);
+            if (!ok) break;
+            tc_fence_after();
+            issue_qk(hh, j + 1);
           }
-          mma_commit(bar(PB_SF + 2 * hh + sb));
         }
-        if (ok && j >= 1) ok = issue_pv(j - 1);
       }
-      if (ok) issue_pv(n_tiles - 1);
       if (*abort_flag) mbar_wait(bar(PB_Q), 0, nullptr);  // let the Q loads land
     }
   } else {
@@ -273,80 +281,85 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
     const int r = tid & 127;                // query row in the tile, TMEM lane
     const int row_pos = a.prior_len + q0 + r;
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const uint32_t col_o = COL_O + hh * HD;
+    const uint32_t col_s = COL_S + hh * BN, col_o = COL_O + hh * HD;
     const float sl2 = a.scale * 1.4426950408889634f;
     float m_run = -INFINITY, l_run = 0.f;   // running max in scaled log2 units
-    unsigned char* prow = smem + OFF_P + hh * P_BYTES + r * 128;
-    const int sw = r & 7;
     for (int j = 0; j < n_tiles; ++j) {
-      const int sb = j & 1;
-      wait_or_abort(bar(PB_SF + 2 * hh + sb), (j >> 1) & 1, abort_flag, a.err);
+      wait_or_abort(bar(PB_SF + hh), j & 1, abort_flag, a.err);
       __syncwarp();
       tc_fence_after();
-      float s[BN];
+      const int k0 = j * BN;
+      const bool diag = k0 + BN - 1 > a.prior_len + q0;   // causal mask needed
+      // pass 1: row max over 128 scores, 32 columns at a time
+      float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) {
         float t[32];
-        tmem_ld32(lane_base + (2 * hh + sb) * BN + c * 32, t);
+        tmem_ld32(lane_base + col_s + c * 32, t);
+        tmem_wait_ld();
+        reg_fence(t);
+        if (diag) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = t[i];
-      }
-      tmem_wait_ld();
-      reg_fence(s);
-      tc_fence_before();
-      mbar_arrive(bar(PB_SE + 2 * hh + sb));
-      const int k0 = j * BN;
-      if (k0 + BN - 1 > a.prior_len + q0) {   // causal mask on the diagonal tiles
+          for (int i = 0; i < 32; ++i)
+            if (k0 + c * 32 + i > row_pos) t[i] = -INFINITY;
+        }
 #pragma unroll
-        for (int c = 0; c < BN; ++c) s[c] = (k0 + c <= row_pos) ? s[c] : -INFINITY;
+        for (int i = 0; i < 32; i += 2) {
+          mx0 = fmaxf(mx0, t[i]);
+          mx1 = fmaxf(mx1, t[i + 1]);
+        }
       }
-      float mx0 = s[0], mx1 = s[1];
-#pragma unroll
-      for (int c = 2; c < BN; c += 2) {
-        mx0 = fmaxf(mx0, s[c]);
-        mx1 = fmaxf(mx1, s[c + 1]);
-      }
-      const float mx = fmaxf(mx0, mx1) * sl2;
+      const float mx = fmaxf(mx0, mx1) * sl2;   // scale > 0 commutes with max
       float m_new = m_run;
       if (mx > m_run + kLazyP || m_run == -INFINITY) m_new = mx;
       const float alpha = (m_new == m_run) ? 1.f : fast_exp2(m_run - m_new);
-      float sum0 = 0.f, sum1 = 0.f;
-      uint32_t packed[BN / 2];
-#pragma unroll
-      for (int c = 0; c < BN; c += 2) {
-        const float p0 = fast_exp2(fmaf(s[c], sl2, -m_new));
-        const float p1 = fast_exp2(fmaf(s[c + 1], sl2, -m_new));
-        sum0 += p0;
-        sum1 += p1;
-        packed[c / 2] = pack_bf16(p0, p1);
-      }
-      if (j >= 1) {  // P_{j-1} V must be done before P is overwritten or O rescaled
+      if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        // O holds P V of the tiles before; its last product is done (S_h of
+        // this tile was only computed after it), so rescale it in place
         wait_or_abort(bar(PB_OD + hh), (j - 1) & 1, abort_flag, a.err);
         __syncwarp();
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-          for (int c = 0; c < HD / 32; ++c) {
-            float o[32];
-            tmem_ld32(lane_base + col_o + c * 32, o);
-            tmem_wait_ld();
-            reg_fence(o);
+        for (int c = 0; c < HD / 32; ++c) {
+          float o[32];
+          tmem_ld32(lane_base + col_o + c * 32, o);
+          tmem_wait_ld();
+          reg_fence(o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tmem_st32(lane_base + col_o + c * 32, o);
-          }
-          tmem_wait_st();
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32(lane_base + col_o + c * 32, o);
         }
+        tmem_wait_st();
       }
+      // pass 2: p = 2^(s*scale*log2e - m), written as bf16 pairs over the
+      // columns of S already read (32 scores -> 16 columns)
+      float2 sum2 = make_float2(0.f, 0.f);
+      const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-m_new, -m_new);
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        float t[32];
+        tmem_ld32(lane_base + col_s + c * 32, t);
+        tmem_wait_ld();
+        reg_fence(t);
+        if (diag) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (k0 + c * 32 + i > row_pos) t[i] = -INFINITY;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float2 x = ffma2(make_float2(t[i], t[i + 1]), sl2x2, negm);
+          const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+          sum2 = fadd2(sum2, pp);
+          pk[i / 2] = pack_bf16(pp.x, pp.y);
+        }
+        tmem_st16(lane_base + col_s + c * 16, pk);
+      }
+      const float sum0 = sum2.x, sum1 = sum2.y;
+      tmem_wait_st();
       l_run = l_run * alpha + (sum0 + sum1);
       m_run = m_new;
-#pragma unroll
-      for (int c8 = 0; c8 < BN / 8; ++c8) {
-        uint4 v = make_uint4(packed[c8 * 4 + 0], packed[c8 * 4 + 1], packed[c8 * 4 + 2],
-                             packed[c8 * 4 + 3]);
-        *reinterpret_cast<uint4*>(prow + ((c8 ^ sw) << 4)) = v;
-      }
-      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(PB_PF + hh));
     }
