@@ -313,27 +313,67 @@ def run_ours(args, w, lay, acct):
     out_pre = [torch.empty_like(inputs[li].q_prefill) for li in range(L)]
     split_launch = 2 if max_seq > 512 else 1  # decode main (+ reduce when any sequence splits)
 
-    def step(ev=None):
+    nd = lay.num_decode_tokens
+    fused = args.fused_append and w.dtype == torch.bfloat16 and w.head_dim == 128
+    k_new_dec = [inputs[li].k_new[:nd] for li in range(L)]
+    v_new_dec = [inputs[li].v_new[:nd] for li in range(L)]
+    k_new_pre = [inputs[li].k_new[nd:] for li in range(L)]
+    v_new_pre = [inputs[li].v_new[nd:] for li in range(L)]
+    slot_pre = slot[nd:]
+
+    def step(ev=None, s=None):
+        s = stream if s is None else s
         for li in range(L):
             x = inputs[li]
             kc, vc = pools[li % n_pools]
-            B.kv_append(x.k_new, x.v_new, kc, vc, slot, stream=stream)
+            if fused:
+                # decode tokens are appended inside the decode launch; the
+                # prefill chunk's tokens by kv_append
+                if w.prefill_chunk:
+                    B.kv_append(k_new_pre[li], v_new_pre[li], kc, vc, slot_pre, stream=s)
+                if ev is not None:
+                    ev[li][0].record(s)
+                B.paged_decode_attention_append(out_dec[li], x.q_decode, k_new_dec[li],
+                                                v_new_dec[li], kc, vc, bt_dec, seq_lens, max_seq,
+                                                w.scale, wsp, stream=s)
+            else:
+                B.kv_append(x.k_new, x.v_new, kc, vc, slot, stream=s)
+                if ev is not None:
+                    ev[li][0].record(s)
+                B.paged_decode_attention(out_dec[li], x.q_decode, kc, vc, bt_dec, seq_lens,
+                                         max_seq, w.scale, wsp, stream=s)
             if ev is not None:
-                ev[li][0].record(stream)
-            B.paged_decode_attention(out_dec[li], x.q_decode, kc, vc, bt_dec, seq_lens, max_seq,
-                                     w.scale, wsp, stream=stream)
-            if ev is not None:
-                ev[li][1].record(stream)
+                ev[li][1].record(s)
             if w.prefill_chunk:
                 B.chunked_prefill_attention(out_pre[li], x.q_prefill, kc, vc, bt_pre,
-                                            w.prefill_prior, w.scale, stream=stream)
+                                            w.prefill_prior, w.scale, stream=s)
                 if ev is not None:
-                    ev[li][2].record(stream)
+                    ev[li][2].record(s)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
     assert B.get_device_error() == 0, "device error word set during warm-up"
+    graph = None
+    if args.graph:
+        # one CUDA graph per step (all layers); the per-kernel events are
+        # captured into it as well
+        # timing events inside a graph must be external event-record nodes
+        try:
+            graph_events = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)]
+                            for _ in range(L)]
+        except TypeError:
+            graph_events = None
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph, stream=cap):
+                step(graph_events, s=cap)
+        stream.wait_stream(cap)
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize(dev)
 
     evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(L)]
            for _ in range(args.steps)]
@@ -343,15 +383,28 @@ def run_ours(args, w, lay, acct):
     with ClockSampler(local) as clk:
         t_start.record(stream)
         for k in range(args.steps):
-            step(evs[k])
+            if graph is not None:
+                graph.replay()
+            else:
+                step(evs[k])
         t_end.record(stream)
         torch.cuda.synchronize(dev)
     barrier(dist)
     total_ms = t_start.elapsed_time(t_end)
     total_ms = max_over_ranks(dist, total_ms)
     assert B.get_device_error() == 0, "device error word set during the timed steps"
-    dec_ms = [evs[k][li][0].elapsed_time(evs[k][li][1]) for k in range(args.steps) for li in range(L)]
-    pre_ms = ([evs[k][li][1].elapsed_time(evs[k][li][2]) for k in range(args.steps)
+    if graph is not None:
+        if graph_events is not None:   # the last replay's event nodes
+            evs = [graph_events]
+        else:
+            # no external events in this torch: the per-kernel breakdown
+            # comes from one eager step right after the timed region
+            evs = [evs[0]]
+            step(evs[0])
+            torch.cuda.synchronize(dev)
+    nsteps_ev = len(evs)
+    dec_ms = [evs[k][li][0].elapsed_time(evs[k][li][1]) for k in range(nsteps_ev) for li in range(L)]
+    pre_ms = ([evs[k][li][1].elapsed_time(evs[k][li][2]) for k in range(nsteps_ev)
                for li in range(L)] if w.prefill_chunk else [])
     ms_step = total_ms / args.steps
     n = ws
@@ -398,7 +451,9 @@ def run_ours(args, w, lay, acct):
                             else "fallback 1.7 PFLOP/s sustained"),
         } if pre_ms else None),
         "clocks": clk.summary(),
-        "gpu_launches": args.steps * L * (1 + split_launch + (1 if w.prefill_chunk else 0)),
+        "gpu_launches": args.steps * L * ((0 if fused and not w.prefill_chunk else 1) + split_launch
+                                          + (1 if w.prefill_chunk else 0)),
+        "mode": {"fused_append": bool(fused), "cuda_graph": graph is not None},
     }
 
     # ---- end to end through the C ABI with host buffers (pinned), same step
@@ -476,6 +531,10 @@ def main():
                     help="distinct layer pools to allocate (0 = one per layer); the step always "
                          "runs every layer, cycling the pools")
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--fused-append", type=int, default=1,
+                    help="1: decode tokens are appended inside the decode launch")
+    ap.add_argument("--graph", type=int, default=1,
+                    help="1: replay the whole step as one captured CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-decode-seqs", type=int, default=128,
                     help="decode sequences in the oracle sample of cpu_baseline")

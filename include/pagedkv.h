@@ -123,6 +123,32 @@ pkv_status pkv_paged_decode_attention(void *out, const void *q, const void *k_ca
                                       void *workspace, size_t workspace_bytes, pkv_dtype dtype,
                                       pkv_stream_t stream);
 
+/*
+ * paged_decode_attention_append -- kv_append of each sequence's new token
+ * fused into paged_decode_attention ("KV cache and continuous batching:
+ * 1,000 people ask AI", section "What does a KV cache keep?": a decode step
+ * appends the new key and value, then attends over everything stored).
+ *   k_new, v_new  [num_seqs][num_kv_heads][head_dim], device: the new token of
+ *                 sequence b, written at position seq_lens[b] - 1, i.e. into
+ *                 physical block block_table[b][(seq_lens[b]-1)/block_size],
+ *                 row (seq_lens[b]-1) % block_size, of both pools
+ *   every other argument as for pkv_paged_decode_attention; the pools are
+ *   written (that one row per sequence and KV head) as well as read.
+ * Equivalent to pkv_kv_append of those rows followed by
+ * pkv_paged_decode_attention, in one launch: the new row is placed into the
+ * staged tile in shared memory and stored to the pool by the same CTA.
+ * bf16 with head_dim 128 only (PKV_EUNSUPPORTED otherwise).
+ */
+pkv_status pkv_paged_decode_attention_append(void *out, const void *q, const void *k_new,
+                                             const void *v_new, void *k_cache, void *v_cache,
+                                             const int32_t *block_table, const int32_t *seq_lens,
+                                             int num_seqs, int max_blocks_per_seq,
+                                             int max_seq_len, int64_t num_blocks,
+                                             int num_q_heads, int num_kv_heads, int head_dim,
+                                             int block_size, float scale, void *workspace,
+                                             size_t workspace_bytes, pkv_dtype dtype,
+                                             pkv_stream_t stream);
+
 /* Size of the scratch buffer pkv_paged_decode_attention_noalloc keeps inside
  * the library (32 MiB; held by every GPU that loads the library until exit). */
 #define PKV_NOALLOC_SCRATCH_BYTES (32u << 20)
@@ -178,6 +204,55 @@ pkv_status pkv_chunked_prefill_attention(void *out, const void *q, const void *k
                                          int64_t num_blocks, int num_q_heads, int num_kv_heads,
                                          int head_dim, int block_size, float scale,
                                          pkv_dtype dtype, pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Prefix caching (host-only): chained block hashes and a hash -> block index.
+ * "The KV cache and prefix caching", section "A prefix already in the cache
+ * can skip its prefill": the prompt is hashed block by block; a block's
+ * identifier covers its tokens together with the identifier of the block
+ * before it, so two sequences share a block identifier only if they agree on
+ * every token up to and including that block; a hit is a contiguous prefix
+ * starting at position 0, counted in whole blocks, so the last partial block
+ * is always recomputed.  The pages name no hash; this library uses 64-bit
+ * FNV-1a: h_b = FNV1a(le64(h_{b-1}) || le32(token_0) .. le32(token_{bs-1})),
+ * h_{-1} = parent (0 for a fresh prompt).  These calls touch no GPU; the
+ * index is host memory owned by the handle and is not thread-safe.
+ * ------------------------------------------------------------------------- */
+
+/* 64-bit FNV-1a of len bytes (offset basis 0xcbf29ce484222325, prime 0x100000001b3). */
+uint64_t pkv_fnv1a64(const void *data, size_t len);
+
+/* Chained hashes of the floor(num_tokens / block_size) full blocks of tokens
+ * (host arrays) into out_hashes.  Returns that count, or -1 on bad arguments. */
+int64_t pkv_prefix_hash_blocks(const int32_t *tokens, int64_t num_tokens, int block_size,
+                               uint64_t parent, uint64_t *out_hashes);
+
+typedef struct pkv_prefix_cache pkv_prefix_cache;
+
+/* New empty index (NULL if host memory runs out); free with _destroy. */
+pkv_prefix_cache *pkv_prefix_cache_create(void);
+void pkv_prefix_cache_destroy(pkv_prefix_cache *cache);
+/* Number of cached blocks, or -1 for a NULL handle. */
+int64_t pkv_prefix_cache_size(const pkv_prefix_cache *cache);
+/* Record that block hashes[i] is held in physical block block_ids[i] (>= 0);
+ * an identifier already present keeps its block. */
+pkv_status pkv_prefix_cache_insert(pkv_prefix_cache *cache, const uint64_t *hashes,
+                                   const int32_t *block_ids, int64_t n);
+/* Forget the given identifiers (absent ones are ignored). */
+pkv_status pkv_prefix_cache_evict(pkv_prefix_cache *cache, const uint64_t *hashes, int64_t n);
+/* Length of the longest prefix of hashes[0..n) that is cached; the matching
+ * physical blocks go to out_block_ids (may be NULL).  -1 on bad arguments. */
+int64_t pkv_prefix_cache_match(const pkv_prefix_cache *cache, const uint64_t *hashes, int64_t n,
+                               int32_t *out_block_ids);
+/* Plan a prefill: hashes every full block of the prompt into out_hashes
+ * (floor(num_tokens / block_size) entries), matches the cached prefix, and
+ * returns the number of prompt tokens whose keys and values can be reused --
+ * whole blocks only, and at most num_tokens - 1 so the last token is always
+ * computed.  The reused physical blocks go to out_block_ids.  The caller then
+ * runs chunked_prefill_attention with prior_len = that count.  -1 on bad
+ * arguments. */
+int64_t pkv_prefix_plan(const pkv_prefix_cache *cache, const int32_t *tokens, int64_t num_tokens,
+                        int block_size, int32_t *out_block_ids, uint64_t *out_hashes);
 
 /*
  * Read the device error word of the current device into *code (host) and,

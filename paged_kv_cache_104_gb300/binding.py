@@ -24,8 +24,11 @@ DEVERR = {0: "none", 1: "slot out of range", 2: "block id out of range",
           3: "sequence length out of range", 4: "internal wait timed out",
           5: "shared-memory layout check failed"}
 EXPORTS = ("pkv_kv_append", "pkv_decode_workspace_bytes", "pkv_paged_decode_attention",
-           "pkv_paged_decode_attention_noalloc", "pkv_chunked_prefill_attention",
-           "pkv_get_device_error", "pkv_status_str", "pkv_abi_version")
+           "pkv_paged_decode_attention_append", "pkv_paged_decode_attention_noalloc", "pkv_chunked_prefill_attention",
+           "pkv_get_device_error", "pkv_status_str", "pkv_abi_version",
+           "pkv_fnv1a64", "pkv_prefix_hash_blocks", "pkv_prefix_cache_create",
+           "pkv_prefix_cache_destroy", "pkv_prefix_cache_size", "pkv_prefix_cache_insert",
+           "pkv_prefix_cache_evict", "pkv_prefix_cache_match", "pkv_prefix_plan")
 NOALLOC_SCRATCH_BYTES = 32 << 20  # PKV_NOALLOC_SCRATCH_BYTES
 
 
@@ -55,11 +58,33 @@ def load():
                                                       i, p]
         lib.pkv_paged_decode_attention_noalloc.argtypes = [p, p, p, p, p, p, i, i, i, i64, i, i,
                                                            i, i, f, i, p]
+        lib.pkv_paged_decode_attention_append.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i64, i,
+                                                          i, i, i, f, p, sz, i, p]
         lib.pkv_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int), i]
         lib.pkv_status_str.argtypes = [i]
         lib.pkv_status_str.restype = ctypes.c_char_p
+        u64p = ctypes.POINTER(ctypes.c_uint64)
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        lib.pkv_fnv1a64.argtypes = [p, sz]
+        lib.pkv_fnv1a64.restype = ctypes.c_uint64
+        lib.pkv_prefix_hash_blocks.argtypes = [i32p, i64, i, ctypes.c_uint64, u64p]
+        lib.pkv_prefix_hash_blocks.restype = i64
+        lib.pkv_prefix_cache_create.argtypes = []
+        lib.pkv_prefix_cache_create.restype = p
+        lib.pkv_prefix_cache_destroy.argtypes = [p]
+        lib.pkv_prefix_cache_destroy.restype = None
+        lib.pkv_prefix_cache_size.argtypes = [p]
+        lib.pkv_prefix_cache_size.restype = i64
+        lib.pkv_prefix_cache_insert.argtypes = [p, u64p, i32p, i64]
+        lib.pkv_prefix_cache_insert.restype = ctypes.c_int
+        lib.pkv_prefix_cache_evict.argtypes = [p, u64p, i64]
+        lib.pkv_prefix_cache_evict.restype = ctypes.c_int
+        lib.pkv_prefix_cache_match.argtypes = [p, u64p, i64, i32p]
+        lib.pkv_prefix_cache_match.restype = i64
+        lib.pkv_prefix_plan.argtypes = [p, i32p, i64, i, i32p, u64p]
+        lib.pkv_prefix_plan.restype = i64
         for name in ("pkv_kv_append", "pkv_paged_decode_attention",
-                     "pkv_paged_decode_attention_noalloc",
+                     "pkv_paged_decode_attention_noalloc", "pkv_paged_decode_attention_append",
                      "pkv_chunked_prefill_attention", "pkv_get_device_error", "pkv_abi_version"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -129,6 +154,21 @@ def paged_decode_attention(out, q, k_cache, v_cache, block_table, seq_lens, max_
     _check("pkv_paged_decode_attention", st)
 
 
+def paged_decode_attention_append(out, q, k_new, v_new, k_cache, v_cache, block_table, seq_lens,
+                                  max_seq_len: int, scale: float, workspace=None,
+                                  stream=None) -> None:
+    """Append each sequence's new key/value (k_new, v_new [B, Hkv, D]) at
+    position seq_lens[b] - 1 and attend, in one launch."""
+    b, hq, d = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().pkv_paged_decode_attention_append(
+        _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_table), _ptr(seq_lens), b, int(block_table.shape[1]), int(max_seq_len), nb, hq,
+        hkv, d, bs, float(scale), _ptr(workspace), ws_bytes, _dtype_code(q), _stream(stream))
+    _check("pkv_paged_decode_attention_append", st)
+
+
 def paged_decode_attention_noalloc(out, q, k_cache, v_cache, block_table, seq_lens,
                                    max_seq_len: int, scale: float, stream=None) -> None:
     """paged_decode_attention without a workspace argument: the split partials
@@ -162,3 +202,83 @@ def get_device_error(clear: bool = True) -> int:
     code = ctypes.c_int(0)
     _check("pkv_get_device_error", load().pkv_get_device_error(ctypes.byref(code), int(clear)))
     return code.value
+
+
+# ----------------------------------------------------------------- prefix cache
+def fnv1a64(data: bytes) -> int:
+    return int(load().pkv_fnv1a64(ctypes.c_char_p(bytes(data)), len(data)))
+
+
+def _i32(a):
+    import numpy as np
+    arr = np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+    return arr, arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+def _u64(a):
+    import numpy as np
+    arr = np.ascontiguousarray(np.asarray(a, dtype=np.uint64))
+    return arr, arr.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64))
+
+
+def prefix_hash_blocks(tokens, block_size: int = 16, parent: int = 0):
+    """Chained FNV-1a identifiers of the full blocks of a token list."""
+    import numpy as np
+    toks, tp = _i32(tokens)
+    out = np.zeros(max(len(toks) // block_size, 1), dtype=np.uint64)
+    n = load().pkv_prefix_hash_blocks(tp, len(toks), block_size, ctypes.c_uint64(parent),
+                                      out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)))
+    if n < 0:
+        raise PagedKVError("pkv_prefix_hash_blocks", 1, "invalid argument")
+    return [int(x) for x in out[:n]]
+
+
+class PrefixCache:
+    """Host-side index from chained block identifiers to physical blocks."""
+
+    def __init__(self):
+        self._h = load().pkv_prefix_cache_create()
+        if not self._h:
+            raise MemoryError("pkv_prefix_cache_create")
+
+    def __del__(self):
+        if getattr(self, "_h", None):
+            load().pkv_prefix_cache_destroy(self._h)
+            self._h = None
+
+    def __len__(self):
+        return int(load().pkv_prefix_cache_size(self._h))
+
+    def insert(self, hashes, block_ids):
+        h, hp = _u64(hashes)
+        b, bp = _i32(block_ids)
+        assert len(h) == len(b)
+        _check("pkv_prefix_cache_insert", load().pkv_prefix_cache_insert(self._h, hp, bp, len(h)))
+
+    def evict(self, hashes):
+        h, hp = _u64(hashes)
+        _check("pkv_prefix_cache_evict", load().pkv_prefix_cache_evict(self._h, hp, len(h)))
+
+    def match(self, hashes):
+        """(number of leading identifiers cached, their physical blocks)."""
+        import numpy as np
+        h, hp = _u64(hashes)
+        out = np.zeros(max(len(h), 1), dtype=np.int32)
+        m = load().pkv_prefix_cache_match(self._h, hp, len(h),
+                                          out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)))
+        return int(m), [int(x) for x in out[:m]]
+
+    def plan(self, tokens, block_size: int = 16):
+        """(reusable prompt tokens, reused physical blocks, every full-block identifier)."""
+        import numpy as np
+        toks, tp = _i32(tokens)
+        nb = max(len(toks) // block_size, 1)
+        blocks = np.zeros(nb, dtype=np.int32)
+        hashes = np.zeros(nb, dtype=np.uint64)
+        m = load().pkv_prefix_plan(self._h, tp, len(toks), block_size,
+                                   blocks.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                   hashes.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)))
+        if m < 0:
+            raise PagedKVError("pkv_prefix_plan", 1, "invalid argument")
+        nfull = len(toks) // block_size
+        return int(m), [int(x) for x in blocks[: m // block_size]], [int(x) for x in hashes[:nfull]]

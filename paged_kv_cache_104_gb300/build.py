@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpagedkv.so")
 SOURCES = ["abi.cu", "append.cu", "decode.cu", "decode_mma.cu", "decode_noalloc.cu",
-           "prefill_pair.cu", "prefill_tc.cu", "tmap.cu"]
+           "prefill_pair.cu", "prefill_tc.cu", "prefix_cache.cpp", "tmap.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -41,7 +41,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     procs, objs = [], []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
         objs.append(o)
         if not force and os.path.exists(o) and os.path.getmtime(o) >= max(os.path.getmtime(s), dep_time):
             continue

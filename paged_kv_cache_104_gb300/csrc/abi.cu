@@ -127,14 +127,17 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, i
   return align256(rows * head_dim * sizeof(float)) + align256(rows * 2 * sizeof(float));
 }
 
-pkv_status pkv_paged_decode_attention(void* out, const void* q, const void* k_cache,
-                                      const void* v_cache, const int32_t* block_table,
-                                      const int32_t* seq_lens, int num_seqs,
-                                      int max_blocks_per_seq, int max_seq_len,
-                                      int64_t num_blocks, int num_q_heads, int num_kv_heads,
-                                      int head_dim, int block_size, float scale,
-                                      void* workspace, size_t workspace_bytes, pkv_dtype dtype,
-                                      pkv_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared by paged_decode_attention and its fused-append form (k_new != null).
+pkv_status decode_impl(void* out, const void* q, const void* k_new, const void* v_new,
+                       const void* k_cache, const void* v_cache, const int32_t* block_table,
+                       const int32_t* seq_lens, int num_seqs, int max_blocks_per_seq,
+                       int max_seq_len, int64_t num_blocks, int num_q_heads, int num_kv_heads,
+                       int head_dim, int block_size, float scale, void* workspace,
+                       size_t workspace_bytes, pkv_dtype dtype, pkv_stream_t stream) {
   pkv_status st = check_heads(num_q_heads, num_kv_heads, head_dim, block_size, dtype);
   if (st != PKV_OK) return st;
   if (num_seqs < 0 || max_blocks_per_seq < 1 || max_seq_len < 1 || num_blocks < 1)
@@ -183,11 +186,50 @@ pkv_status pkv_paged_decode_attention(void* out, const void* q, const void* k_ca
   a.scale = scale;
   a.chunk_prior = -1;
   a.is_bf16 = dtype == PKV_BF16;
+  a.k_new = k_new;
+  a.v_new = v_new;
   cudaStream_t s_ = reinterpret_cast<cudaStream_t>(stream);
   const cudaError_t e = pkv::decode_mma_supported(a.is_bf16, head_dim, num_q_heads / num_kv_heads)
                             ? pkv::launch_paged_decode_mma(a, sms, s_)
                             : pkv::launch_paged_decode(a, sms, s_);
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_paged_decode_attention(void* out, const void* q, const void* k_cache,
+                                      const void* v_cache, const int32_t* block_table,
+                                      const int32_t* seq_lens, int num_seqs,
+                                      int max_blocks_per_seq, int max_seq_len,
+                                      int64_t num_blocks, int num_q_heads, int num_kv_heads,
+                                      int head_dim, int block_size, float scale,
+                                      void* workspace, size_t workspace_bytes, pkv_dtype dtype,
+                                      pkv_stream_t stream) {
+  return decode_impl(out, q, nullptr, nullptr, k_cache, v_cache, block_table, seq_lens, num_seqs,
+                     max_blocks_per_seq, max_seq_len, num_blocks, num_q_heads, num_kv_heads,
+                     head_dim, block_size, scale, workspace, workspace_bytes, dtype, stream);
+}
+
+pkv_status pkv_paged_decode_attention_append(void* out, const void* q, const void* k_new,
+                                             const void* v_new, void* k_cache, void* v_cache,
+                                             const int32_t* block_table, const int32_t* seq_lens,
+                                             int num_seqs, int max_blocks_per_seq,
+                                             int max_seq_len, int64_t num_blocks,
+                                             int num_q_heads, int num_kv_heads, int head_dim,
+                                             int block_size, float scale, void* workspace,
+                                             size_t workspace_bytes, pkv_dtype dtype,
+                                             pkv_stream_t stream) {
+  if (!dtype_ok(dtype)) return PKV_EDTYPE;
+  if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads != 0) return PKV_EINVAL;
+  if (!pkv::decode_mma_supported(dtype == PKV_BF16, head_dim, num_q_heads / num_kv_heads))
+    return PKV_EUNSUPPORTED;
+  if (num_seqs > 0 && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)))
+    return PKV_EINVAL;
+  return decode_impl(out, q, k_new, v_new, k_cache, v_cache, block_table, seq_lens, num_seqs,
+                     max_blocks_per_seq, max_seq_len, num_blocks, num_q_heads, num_kv_heads,
+                     head_dim, block_size, scale, workspace, workspace_bytes, dtype, stream);
 }
 
 pkv_status pkv_chunked_prefill_attention(void* out, const void* q, const void* k_cache,

@@ -115,7 +115,7 @@ __device__ __forceinline__ uint32_t sw_off(int row, int c) {
   return (uint32_t)((c >> 3) * kHalfB + row * 128 + (((c & 7) ^ (row & 7)) << 4));
 }
 
-template <int G>
+template <int G, bool FUSE>
 __global__ void __launch_bounds__(kThreadsM, 2)
 decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v) {
@@ -264,6 +264,29 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
       if (valid > 0) {
         const uint32_t kt = sbase + buf * kStageB + warp * kTileB;
         const uint32_t vt = kt + kBPS * kTileB;
+        if (FUSE && u.s == u.ns - 1 && tok0 + valid == u.tok_end) {
+          // this block holds the sequence's new token (position tok_end - 1):
+          // the staged tile still has the pool's old row there, so put the new
+          // key and value into shared memory and into the pool.  Lanes 0-15
+          // move the 16-byte chunks of K, lanes 16-31 those of V.
+          const int r = valid - 1;
+          const int c = lane & 15;
+          const bool is_v = lane >= 16;
+          const int64_t src = (((int64_t)u.b * a.num_kv_heads + u.g) * kHD) + c * 8;
+          const uint4 val = __ldg(reinterpret_cast<const uint4*>(
+              static_cast<const __nv_bfloat16*>(is_v ? a.v_new : a.k_new) + src));
+          unsigned char* tile = smem + buf * kStageB + (is_v ? kBPS * kTileB : 0) + warp * kTileB;
+          *reinterpret_cast<uint4*>(tile + sw_off(r, c)) = val;
+          const int blk = __ldg(a.block_table + (int64_t)u.b * a.bt_stride + (tok0 / kBlockSize));
+          if (blk >= 0 && (int64_t)blk < a.num_blocks) {
+            __nv_bfloat16* pool = const_cast<__nv_bfloat16*>(
+                static_cast<const __nv_bfloat16*>(is_v ? a.v_cache : a.k_cache));
+            const int64_t dst = (((int64_t)blk * a.num_kv_heads + u.g) * kBlockSize + r) * kHD + c * 8;
+            *reinterpret_cast<uint4*>(pool + dst) = val;
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+        }
         if (valid < kBlockSize) {
           // zero the V rows past the sequence end (whole rows, so the swizzle does not matter)
           unsigned char* vrow = smem + buf * kStageB + kBPS * kTileB + warp * kTileB;
@@ -402,7 +425,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
   }
 }
 
-template <int G>
+template <int G, bool FUSE>
 cudaError_t launch_g(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
   using C = MCfg<G>;
   CUtensorMap tm_k, tm_v;
@@ -411,13 +434,13 @@ cudaError_t launch_g(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   const size_t smem = C::OFF_CU + sizeof(int) * (size_t)(a.num_seqs + 1) + 1024;
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<G>,
+  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<G, FUSE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int per_sm = smem <= 113 * 1024 ? 2 : 1;
   const int64_t upper = (int64_t)a.num_seqs * a.num_kv_heads * a.max_splits;
   const int grid = (int)(upper < (int64_t)num_sms * per_sm ? upper : (int64_t)num_sms * per_sm);
-  decode_mma_kernel<G><<<grid, kThreadsM, smem, stream>>>(a, tm_k, tm_v);
+  decode_mma_kernel<G, FUSE><<<grid, kThreadsM, smem, stream>>>(a, tm_k, tm_v);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.max_splits <= 1) return e;
   return launch_decode_reduce_bf16_128(a, stream);
@@ -432,12 +455,13 @@ bool decode_mma_supported(int is_bf16, int head_dim, int group) {
 
 cudaError_t launch_paged_decode_mma(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
   if (a.chunk_prior >= 0 || a.split_tokens % kStageTok != 0) return cudaErrorInvalidValue;
+  const bool fuse = a.k_new != nullptr;
   switch (a.num_q_heads / a.num_kv_heads) {
-    case 1: return launch_g<1>(a, num_sms, stream);
-    case 2: return launch_g<2>(a, num_sms, stream);
-    case 4: return launch_g<4>(a, num_sms, stream);
-    case 8: return launch_g<8>(a, num_sms, stream);
-    case 16: return launch_g<16>(a, num_sms, stream);
+    case 1: return fuse ? launch_g<1, true>(a, num_sms, stream) : launch_g<1, false>(a, num_sms, stream);
+    case 2: return fuse ? launch_g<2, true>(a, num_sms, stream) : launch_g<2, false>(a, num_sms, stream);
+    case 4: return fuse ? launch_g<4, true>(a, num_sms, stream) : launch_g<4, false>(a, num_sms, stream);
+    case 8: return fuse ? launch_g<8, true>(a, num_sms, stream) : launch_g<8, false>(a, num_sms, stream);
+    case 16: return fuse ? launch_g<16, true>(a, num_sms, stream) : launch_g<16, false>(a, num_sms, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -49,6 +49,10 @@ struct DecodeArgs {
   float scale;
   int chunk_prior;          // -1: decode; >= 0: row b has length chunk_prior + b + 1
   int is_bf16;
+  // fused append (decode_mma only): each sequence's new key/value [B][Hkv][D],
+  // written at position seq_lens[b] - 1 before attending; null = no append
+  const void* k_new;
+  const void* v_new;
 };
 // True if (dtype, head_dim, group) has a compiled decode kernel.
 bool decode_supported(int is_bf16, int head_dim, int group);

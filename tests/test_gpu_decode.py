@@ -142,3 +142,48 @@ def test_decode_reports_length_beyond_bound():
     G.gpu_decode(w, x.q_decode, kc, vc, lay.decode_block_table, lay.seq_lens, max_seq_len=64,
                  check_err=False)
     assert B.get_device_error() == 3
+
+
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (8, 8), (16, 1)])
+def test_fused_append_decode_matches_append_then_decode(hq, hkv):
+    """The fused call writes the same pool bytes as kv_append (bit-exact
+    against the oracle's scatter) and returns bit-identical attention to
+    kv_append followed by paged_decode_attention; within tolerance of the oracle."""
+    w = G.custom_workload(torch.bfloat16, hq, hkv, 128, seed=71)
+    lens = [1, 2, 16, 17, 33, 511, 512, 513, 1025, 1600]
+    lay = W.make_layout(w, seq_lens_after=lens, prefill=(0, 0))
+    x = W.draw_layer(w, lay, 0)
+    G.poison_unused(x.k_cache, x.v_cache, G.used_slot_mask(lay, w.block_size))
+    bt = lay.decode_block_table.cuda().contiguous()
+    sl = lay.seq_lens.cuda()
+    msl = int(lay.seq_lens.max())
+    ws = B.decode_workspace(len(lens), hq, 128, msl)
+    # fused
+    kc, vc = x.k_cache.cuda(), x.v_cache.cuda()
+    out_f = torch.empty_like(x.q_decode).cuda()
+    B.paged_decode_attention_append(out_f, x.q_decode.cuda(), x.k_new.cuda(), x.v_new.cuda(), kc, vc,
+                                    bt, sl, msl, w.scale, ws)
+    torch.cuda.synchronize()
+    assert B.get_device_error() == 0
+    # separate
+    kc2, vc2 = G.gpu_append(lay, x)
+    out_s = G.gpu_decode(w, x.q_decode, kc2, vc2, lay.decode_block_table, lay.seq_lens)
+    rk, rv = G.oracle_append(lay, x)
+    bits = lambda t: t.cpu().view(torch.int16)
+    assert torch.equal(bits(kc), bits(rk)) and torch.equal(bits(vc), bits(rv))
+    assert torch.equal(bits(out_f), bits(out_s))
+    ref = oracle.paged_decode(x.q_decode, rk, rv, lay.decode_block_table, lay.seq_lens, w.scale)
+    assert G.max_err(out_f, ref) <= 2e-2
+
+
+def test_fused_append_decode_rejects_fp32():
+    w = G.custom_workload(torch.float32, 4, 2, 16)
+    lay = W.make_layout(w, seq_lens_after=[5], prefill=(0, 0))
+    x = W.draw_layer(w, lay, 0)
+    kc, vc = x.k_cache.cuda(), x.v_cache.cuda()
+    with pytest.raises(B.PagedKVError) as e:
+        B.paged_decode_attention_append(torch.empty_like(x.q_decode).cuda(), x.q_decode.cuda(),
+                                        x.k_new.cuda(), x.v_new.cuda(), kc, vc,
+                                        lay.decode_block_table.cuda(), lay.seq_lens.cuda(), 5,
+                                        w.scale)
+    assert e.value.status == 5
