@@ -206,6 +206,37 @@ pkv_status pkv_chunked_prefill_attention(void *out, const void *q, const void *k
                                          pkv_dtype dtype, pkv_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * fp8 KV cache (E4M3 codes with a float scale per KV head).  "The KV cache is
+ * not your bottleneck", section "What the profile said", names cache
+ * quantisation; the pages give no format.  This library stores a key or value
+ * element x of KV head h as code = E4M3(x / scale[h]) -- the OCP FP8 E4M3
+ * format (bias 7, 3 mantissa bits, largest finite 448, no infinity), x/scale
+ * computed in fp32, rounded to nearest even, finite values beyond 448 clamped
+ * to 448 -- and reads it back as decode(code) * scale[h].  Pools are bytes
+ * [num_blocks][num_kv_heads][block_size][head_dim]; scales are device float
+ * [num_kv_heads]; new keys/values, q and out are bf16.
+ * ------------------------------------------------------------------------- */
+
+/* Quantise and scatter new keys and values (as pkv_kv_append otherwise;
+ * head_dim a multiple of 16). */
+pkv_status pkv_kv_append_fp8(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                             const float *k_scale, const float *v_scale,
+                             const int64_t *slot_mapping, int64_t num_tokens, int64_t num_blocks,
+                             int num_kv_heads, int head_dim, int block_size, pkv_stream_t stream);
+
+/* Decode attention over the fp8 pools (as pkv_paged_decode_attention with
+ * q/out in bf16; head_dim 128; the same workspace size). */
+pkv_status pkv_paged_decode_attention_fp8(void *out, const void *q, const void *k_cache,
+                                          const void *v_cache, const float *k_scale,
+                                          const float *v_scale, const int32_t *block_table,
+                                          const int32_t *seq_lens, int num_seqs,
+                                          int max_blocks_per_seq, int max_seq_len,
+                                          int64_t num_blocks, int num_q_heads, int num_kv_heads,
+                                          int head_dim, int block_size, float scale,
+                                          void *workspace, size_t workspace_bytes,
+                                          pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Prefix caching (host-only): chained block hashes and a hash -> block index.
  * "The KV cache and prefix caching", section "A prefix already in the cache
  * can skip its prefill": the prompt is hashed block by block; a block's

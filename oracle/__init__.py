@@ -31,7 +31,7 @@ _LIB_PATH = os.path.join(_BUILD_DIR, "libpkv_oracle.so")
 _lib = None
 _lock = threading.Lock()
 
-_DTYPE_CODE = {torch.float32: 0, torch.bfloat16: 1}
+_DTYPE_CODE = {torch.float32: 0, torch.bfloat16: 1, torch.float64: 3}
 
 
 def build(force: bool = False) -> str:

@@ -44,9 +44,11 @@
 #define ORACLE_ENOMEM 7
 
 /* Storage element -> fp64.  dtype 0: IEEE binary32; dtype 1: bfloat16, the
- * upper 16 bits of a binary32, so widening is exact. */
+ * upper 16 bits of a binary32, so widening is exact; dtype 3: IEEE binary64
+ * (used for pools already dequantised from another storage format). */
 static double load_elem(const void *base, int64_t idx, int dtype) {
   if (dtype == 0) return (double)((const float *)base)[idx];
+  if (dtype == 3) return ((const double *)base)[idx];
   uint32_t u = (uint32_t)((const uint16_t *)base)[idx] << 16;
   float f;
   memcpy(&f, &u, sizeof f);

@@ -26,6 +26,7 @@ DEVERR = {0: "none", 1: "slot out of range", 2: "block id out of range",
 EXPORTS = ("pkv_kv_append", "pkv_decode_workspace_bytes", "pkv_paged_decode_attention",
            "pkv_paged_decode_attention_append", "pkv_paged_decode_attention_noalloc", "pkv_chunked_prefill_attention",
            "pkv_get_device_error", "pkv_status_str", "pkv_abi_version",
+           "pkv_kv_append_fp8", "pkv_paged_decode_attention_fp8",
            "pkv_fnv1a64", "pkv_prefix_hash_blocks", "pkv_prefix_cache_create",
            "pkv_prefix_cache_destroy", "pkv_prefix_cache_size", "pkv_prefix_cache_insert",
            "pkv_prefix_cache_evict", "pkv_prefix_cache_match", "pkv_prefix_plan")
@@ -63,6 +64,11 @@ def load():
         lib.pkv_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int), i]
         lib.pkv_status_str.argtypes = [i]
         lib.pkv_status_str.restype = ctypes.c_char_p
+        lib.pkv_kv_append_fp8.argtypes = [p, p, p, p, p, p, p, i64, i64, i, i, i, p]
+        lib.pkv_kv_append_fp8.restype = ctypes.c_int
+        lib.pkv_paged_decode_attention_fp8.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i64, i, i,
+                                                       i, i, f, p, sz, p]
+        lib.pkv_paged_decode_attention_fp8.restype = ctypes.c_int
         u64p = ctypes.POINTER(ctypes.c_uint64)
         i32p = ctypes.POINTER(ctypes.c_int32)
         lib.pkv_fnv1a64.argtypes = [p, sz]
@@ -167,6 +173,30 @@ def paged_decode_attention_append(out, q, k_new, v_new, k_cache, v_cache, block_
         _ptr(block_table), _ptr(seq_lens), b, int(block_table.shape[1]), int(max_seq_len), nb, hq,
         hkv, d, bs, float(scale), _ptr(workspace), ws_bytes, _dtype_code(q), _stream(stream))
     _check("pkv_paged_decode_attention_append", st)
+
+
+def kv_append_fp8(k_new, v_new, k_cache, v_cache, k_scale, v_scale, slot_mapping,
+                  stream=None) -> None:
+    """bf16 k_new, v_new [T, Hkv, D] -> E4M3 codes of x / scale[h] in uint8
+    pools [NB, Hkv, bs, D]; k_scale, v_scale float32 [Hkv] on the device."""
+    nb, hkv, bs, d = k_cache.shape
+    st = load().pkv_kv_append_fp8(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                  _ptr(k_scale), _ptr(v_scale), _ptr(slot_mapping),
+                                  int(slot_mapping.shape[0]), nb, hkv, d, bs, _stream(stream))
+    _check("pkv_kv_append_fp8", st)
+
+
+def paged_decode_attention_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
+                               max_seq_len: int, scale: float, workspace=None, stream=None) -> None:
+    """Decode over uint8 E4M3 pools; q/out bf16 [B, Hq, D]."""
+    b, hq, d = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().pkv_paged_decode_attention_fp8(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+        _ptr(block_table), _ptr(seq_lens), b, int(block_table.shape[1]), int(max_seq_len), nb, hq,
+        hkv, d, bs, float(scale), _ptr(workspace), ws_bytes, _stream(stream))
+    _check("pkv_paged_decode_attention_fp8", st)
 
 
 def paged_decode_attention_noalloc(out, q, k_cache, v_cache, block_table, seq_lens,

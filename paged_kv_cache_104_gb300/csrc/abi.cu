@@ -232,6 +232,100 @@ pkv_status pkv_paged_decode_attention_append(void* out, const void* q, const voi
                      head_dim, block_size, scale, workspace, workspace_bytes, dtype, stream);
 }
 
+pkv_status pkv_kv_append_fp8(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                             const float* k_scale, const float* v_scale,
+                             const int64_t* slot_mapping, int64_t num_tokens, int64_t num_blocks,
+                             int num_kv_heads, int head_dim, int block_size, pkv_stream_t stream) {
+  if (num_tokens < 0 || num_blocks < 1 || num_kv_heads < 1 || head_dim < 1 || block_size < 1)
+    return PKV_EINVAL;
+  if (block_size != pkv::kBlockSize || head_dim % 16 != 0) return PKV_EUNSUPPORTED;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_new || !v_new || !k_cache || !v_cache || !slot_mapping || !k_scale || !v_scale)
+    return PKV_EINVAL;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) ||
+      (reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u))
+    return PKV_EINVAL;
+  int* err = nullptr;
+  int sms = 0;
+  pkv_status st = device_state(&err, &sms);
+  if (st != PKV_OK) return st;
+  pkv::AppendFp8Args a{k_new, v_new, k_cache, v_cache, k_scale, v_scale, slot_mapping,
+                       num_tokens, num_blocks, num_kv_heads, head_dim, err};
+  return pkv::launch_kv_append_fp8(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PKV_OK
+             : PKV_ECUDA;
+}
+
+pkv_status pkv_paged_decode_attention_fp8(void* out, const void* q, const void* k_cache,
+                                          const void* v_cache, const float* k_scale,
+                                          const float* v_scale, const int32_t* block_table,
+                                          const int32_t* seq_lens, int num_seqs,
+                                          int max_blocks_per_seq, int max_seq_len,
+                                          int64_t num_blocks, int num_q_heads, int num_kv_heads,
+                                          int head_dim, int block_size, float scale,
+                                          void* workspace, size_t workspace_bytes,
+                                          pkv_stream_t stream) {
+  if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads != 0 || head_dim < 1 ||
+      block_size < 1)
+    return PKV_EINVAL;
+  if (block_size != pkv::kBlockSize ||
+      !pkv::decode_mma_supported(1, head_dim, num_q_heads / num_kv_heads))
+    return PKV_EUNSUPPORTED;
+  if (num_seqs < 0 || max_blocks_per_seq < 1 || max_seq_len < 1 || num_blocks < 1)
+    return PKV_EINVAL;
+  if (num_seqs == 0) return PKV_OK;
+  if (num_seqs > PKV_MAX_SEQS) return PKV_ERANGE;
+  if ((int64_t)max_seq_len > (int64_t)max_blocks_per_seq * block_size) return PKV_EINVAL;
+  if (!isfinite(scale)) return PKV_EINVAL;
+  if (!out || !q || !k_cache || !v_cache || !block_table || !seq_lens || !k_scale || !v_scale)
+    return PKV_EINVAL;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(block_table) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u))
+    return PKV_EINVAL;
+  const size_t need = pkv_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len);
+  if (workspace_bytes < need) return PKV_ERANGE;
+  if (need > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))) return PKV_EINVAL;
+  int* err = nullptr;
+  int sms = 0;
+  pkv_status st = device_state(&err, &sms);
+  if (st != PKV_OK) return st;
+  const int s = max_splits_for(max_seq_len);
+  const size_t rows = (size_t)num_seqs * num_q_heads * s;
+  pkv::DecodeArgs a{};
+  a.out = out;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.ws_acc = static_cast<float*>(workspace);
+  a.ws_ml = need ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                            align256(rows * head_dim * sizeof(float)))
+                 : nullptr;
+  a.err = err;
+  a.num_seqs = num_seqs;
+  a.bt_stride = max_blocks_per_seq;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.max_seq_len = max_seq_len;
+  a.max_splits = s;
+  a.split_tokens = pkv::kSplitTokens;
+  a.num_blocks = num_blocks;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.scale = scale;
+  a.chunk_prior = -1;
+  a.is_bf16 = 1;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  return pkv::launch_paged_decode_fp8(a, sms, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PKV_OK
+             : PKV_ECUDA;
+}
+
 pkv_status pkv_chunked_prefill_attention(void* out, const void* q, const void* k_cache,
                                          const void* v_cache, const int32_t* block_table_row,
                                          int max_blocks, int prior_len, int chunk_len,

@@ -114,6 +114,20 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
 __device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
+// fp8 (E4M3) conversions, hardware rounding: f32 -> e4m3 rounds to nearest
+// even and saturates finite values at +-448; e4m3 -> f16 is exact.
+// Element order follows memory order: `lo` is the byte / half at the lower address.
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(v));
+  return d;
+}
+
 template <typename T>
 struct Elem;
 template <>

@@ -25,6 +25,22 @@ struct AppendArgs {
   int* err;
 };
 cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream);
+// bf16 rows -> fp8 E4M3 codes of x / scale[head] (head_dim a multiple of 16)
+struct AppendFp8Args {
+  const void* k_new;   // bf16 [T][Hkv][D]
+  const void* v_new;
+  void* k_cache;       // uint8 [NB][Hkv][16][D]
+  void* v_cache;
+  const float* k_scale;  // [Hkv]
+  const float* v_scale;
+  const int64_t* slot_mapping;
+  int64_t num_tokens;
+  int64_t num_blocks;
+  int num_kv_heads;
+  int head_dim;
+  int* err;
+};
+cudaError_t launch_kv_append_fp8(const AppendFp8Args& a, cudaStream_t stream);
 
 struct DecodeArgs {
   void* out;
@@ -53,6 +69,9 @@ struct DecodeArgs {
   // written at position seq_lens[b] - 1 before attending; null = no append
   const void* k_new;
   const void* v_new;
+  // fp8 cache only: per-KV-head dequantisation scales [Hkv]
+  const float* k_scale;
+  const float* v_scale;
 };
 // True if (dtype, head_dim, group) has a compiled decode kernel.
 bool decode_supported(int is_bf16, int head_dim, int group);
@@ -61,6 +80,9 @@ cudaError_t launch_paged_decode(const DecodeArgs& a, int num_sms, cudaStream_t s
 // decode mode only (chunk_prior < 0).  Launches the split reduce when needed.
 bool decode_mma_supported(int is_bf16, int head_dim, int group);
 cudaError_t launch_paged_decode_mma(const DecodeArgs& a, int num_sms, cudaStream_t stream);
+// fp8 (E4M3) cache, bf16 q/out, head_dim 128, group in {1,2,4,8,16}; uses
+// DecodeArgs with k_scale / v_scale set.
+cudaError_t launch_paged_decode_fp8(const DecodeArgs& a, int num_sms, cudaStream_t stream);
 // Merge of split partials for bf16 / head_dim 128 (used by the mma decode).
 cudaError_t launch_decode_reduce_bf16_128(const DecodeArgs& a, cudaStream_t stream);
 

@@ -38,6 +38,18 @@ bool encode_pool_map_bf16(CUtensorMap* map, const void* base, int64_t rows) {
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_pool_map_u8(CUtensorMap* map, const void* base, int64_t rows) {
+  EncodeTiledFn f = encode_fn();
+  if (!f || rows <= 0 || rows >= (1ll << 31) - 1) return false;
+  cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, 16};
+  cuuint32_t estr[2] = {1, 1};
+  return f(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_rows_map_bf16(CUtensorMap* map, const void* base, int64_t n, int heads) {
   EncodeTiledFn f = encode_fn();
   if (!f || n <= 0 || heads <= 0) return false;

@@ -216,3 +216,25 @@ def sample_pairs(n_rows: int, n_heads: int, count: int, seed: int, must=()) -> l
         h = int(torch.randint(0, n_heads, (1,), generator=g))
         pairs.add((r, h))
     return sorted(pairs)
+
+
+def fp8_scales(w: Workload, layer: int = 0) -> tuple:
+    """Seeded per-KV-head float32 scales (k_scale, v_scale) for an fp8 cache:
+    a head's N(0,1) entries beyond 4 to 6 standard deviations saturate."""
+    g = torch.Generator().manual_seed(50_000 + 100 * w.seed + layer)
+    k = (4.0 + 2.0 * torch.rand(w.num_kv_heads, generator=g)) / 448.0
+    v = (4.0 + 2.0 * torch.rand(w.num_kv_heads, generator=g)) / 448.0
+    return k.to(torch.float32), v.to(torch.float32)
+
+
+def draw_fp8_pool(w: Workload, lay: Layout, scales: torch.Tensor, layer: int = 0, which: int = 0,
+                  device="cpu") -> torch.Tensor:
+    """uint8 E4M3 codes [NB, Hkv, bs, D] standing for a cache of N(0,1)
+    entries stored at ``scales`` [Hkv] (codes drawn through torch's own
+    float8_e4m3fn cast, clamped to the finite range)."""
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev).manual_seed(20_000 * (w.seed + 1) + 2 * layer + which)
+    x = torch.randn((lay.num_blocks, w.num_kv_heads, w.block_size, w.head_dim), generator=gen,
+                    device=dev, dtype=torch.float32)
+    x = (x / scales.to(dev)[None, :, None, None]).clamp_(-448.0, 448.0)
+    return x.to(torch.float8_e4m3fn).view(torch.uint8)
