@@ -275,6 +275,104 @@ def run_reference(args, w, lay, acct):
 
 
 # --------------------------------------------------------------------------- our arm
+def run_fp8_decode(args, w, lay, inputs, dev, stream, dist, n):
+    """Time the decode path over an fp8 (E4M3, per-KV-head scales) cache:
+    per layer kv_append_fp8 of the decode tokens, then decode attention
+    (split-K main + reduce), every layer with its own pools, as one CUDA
+    graph per step.  Algorithmic bytes: the codes of every stored K and V row
+    once, q read and out written (bf16), and the append (bf16 in, codes out)."""
+    from paged_kv_cache_104_gb300 import binding as B
+
+    L, hq, hkv, d = w.layers, w.num_q_heads, w.num_kv_heads, w.head_dim
+    nd = lay.num_decode_tokens
+    tokens = int(lay.seq_lens.to(torch.int64).sum())
+    dec_bytes = tokens * hkv * d * 2 + 2 * nd * hq * d * 2
+    app_bytes = nd * hkv * d * 2 * (2 + 1)
+    pool_bytes = 2 * lay.num_blocks * hkv * w.block_size * d
+    free, _ = torch.cuda.mem_get_info(dev)
+    n_pools = min(L, max(2, int((free - 8 * 2 ** 30) // max(pool_bytes, 1))))
+    if args.layer_pools > 0:
+        n_pools = min(n_pools, args.layer_pools)
+    scales = [tuple(t.to(dev) for t in W.fp8_scales(w, li)) for li in range(L)]
+    pools = [(W.draw_fp8_pool(w, lay, scales[li][0], li, 0, device=dev),
+              W.draw_fp8_pool(w, lay, scales[li][1], li, 1, device=dev)) for li in range(n_pools)]
+    slot_dec = lay.slot_mapping[:nd].to(dev)
+    bt = lay.decode_block_table.to(dev).contiguous()
+    sl = lay.seq_lens.to(dev)
+    msl = int(lay.seq_lens.max())
+    wsp = B.decode_workspace(nd, hq, d, msl, device=dev)
+    outs = [torch.empty_like(inputs[li].q_decode) for li in range(L)]
+
+    def step(ev=None, s=None):
+        s = stream if s is None else s
+        for li in range(L):
+            x = inputs[li]
+            kc, vc = pools[li % n_pools]
+            ks, vs = scales[li]
+            B.kv_append_fp8(x.k_new[:nd], x.v_new[:nd], kc, vc, ks, vs, slot_dec, stream=s)
+            if ev is not None:
+                ev[li][0].record(s)
+            B.paged_decode_attention_fp8(outs[li], x.q_decode, kc, vc, ks, vs, bt, sl, msl,
+                                         w.scale, wsp, stream=s)
+            if ev is not None:
+                ev[li][1].record(s)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    assert B.get_device_error() == 0, "device error word set during the fp8 warm-up"
+    try:
+        gev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+               for _ in range(L)]
+    except TypeError:
+        gev = None
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            step(gev, s=cap)
+    stream.wait_stream(cap)
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    t0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(dist)
+    ms_step = max_over_ranks(dist, t0.elapsed_time(t1)) / args.steps
+    assert B.get_device_error() == 0, "device error word set during the fp8 steps"
+    if gev is None:
+        gev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(L)]
+        step(gev)
+        torch.cuda.synchronize(dev)
+    dec_ms = sum(gev[li][0].elapsed_time(gev[li][1]) for li in range(L)) / L
+    hbm_peak, _, peak_src = measured_peaks()
+    dec_gbs = dec_bytes / (dec_ms / 1e3) / 1e9
+    return {
+        "what": "decode path over an fp8 E4M3 cache with per-KV-head scales: kv_append_fp8 of "
+                "the decode tokens + decode attention (main + reduce), all layers, one CUDA graph",
+        "ms_per_step": ms_step,
+        "value": n * L * (dec_bytes + app_bytes) / (ms_step / 1e3) / 1e9, "unit": "GB/s",
+        "decode_tokens_per_s": n * nd / (ms_step / 1e3),
+        "decode_ms_per_layer": dec_ms,
+        "distinct_layer_pools": n_pools, "pool_gb_per_layer": pool_bytes / 1e9,
+        "gpu_launches": args.steps * L * (2 + (1 if msl > 512 else 0)),
+        "roofline": {
+            "kernel": "paged_decode_attention_fp8 (split-K main + reduce)", "bound": "hbm",
+            "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": dec_gbs / hbm_peak,
+            "traffic": profiled_traffic("decode_fp8_kernel", "decode_fp8.cu"),
+            "algorithmic_bytes_per_launch": dec_bytes,
+            "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+            else "fallback 6.8 TB/s",
+        },
+    }
+
+
 def run_ours(args, w, lay, acct):
     from paged_kv_cache_104_gb300 import binding as B
 
@@ -501,8 +599,15 @@ def run_ours(args, w, lay, acct):
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "ms_per_step": e_ms, "steps": args.e2e_steps}
 
+    # ---- fp8 (E4M3) cache variant of the decode path: append + decode + reduce
+    if args.fp8_decode and w.head_dim == 128 and w.dtype == torch.bfloat16:
+        del pools
+        torch.cuda.empty_cache()
+        line["fp8_decode"] = run_fp8_decode(args, w, lay, inputs, dev, stream, dist, n)
+
     # ---- the oracle on this host's cores, bounded sample, rank 0 at N=1 only
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        pools = None
         del pools, inputs, out_dec, out_pre
         torch.cuda.empty_cache()
         os.environ.setdefault("OMP_NUM_THREADS", str(cpu_cores()))
@@ -535,6 +640,9 @@ def main():
                     help="1: decode tokens are appended inside the decode launch")
     ap.add_argument("--graph", type=int, default=1,
                     help="1: replay the whole step as one captured CUDA graph")
+    ap.add_argument("--fp8-decode", type=int, default=1,
+                    help="1: also time the decode path over an fp8 (E4M3) cache (reported "
+                         "under fp8_decode, after the bf16 step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-decode-seqs", type=int, default=128,
                     help="decode sequences in the oracle sample of cpu_baseline")
