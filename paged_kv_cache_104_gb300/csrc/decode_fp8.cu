@@ -115,6 +115,13 @@ __device__ __forceinline__ uint32_t movm_t(uint32_t x) {
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(x));
   return d;
 }
+// 2^x by the MUFU approximation (flushes subnormal results to zero); x is
+// never above the lazy-rescale threshold here
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ uint4 lds128(const unsigned char* p) {
   return *reinterpret_cast<const uint4*>(p);
 }
@@ -286,9 +293,11 @@ decode_fp8_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
       if (valid <= 0) continue;
 
       // ---- S^T = K . Q^T over 8 k-steps of 16 (permuted) head dimensions
-      float s[NT][4];
+      float s[NT][4], s2[NT][4];   // even and odd k-steps: two short dependency chains
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s[nt][i] = s2[nt][i] = 0.f;
       const uint32_t kgw[8] = {kg0.x, kg0.y, kg0.z, kg0.w, kg1.x, kg1.y, kg1.z, kg1.w};
       const uint32_t khw[8] = {kh0.x, kh0.y, kh0.z, kh0.w, kh1.x, kh1.y, kh1.z, kh1.w};
 #pragma unroll
@@ -297,52 +306,71 @@ decode_fp8_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
         const uint32_t a1 = lo16_to_f16x2(khw[ks]), a3 = hi16_to_f16x2(khw[ks]);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
-          mma16816_f16(s[nt], a0, a1, a2, a3, qf[nt][ks][0], qf[nt][ks][1]);
+          mma16816_f16((ks & 1) ? s2[nt] : s[nt], a0, a1, a2, a3, qf[nt][ks][0], qf[nt][ks][1]);
       }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s[nt][i] += s2[nt][i];
 
-      // ---- online softmax per head (column); this lane holds keys g, g+8
+      // ---- online softmax per head (column); this lane holds keys g, g+8.
+      // The running max m only has to bound the scores to within the lazy
+      // threshold (p = 2^(s - m) <= 2^8 stays in f16), so a warp vote decides
+      // whether any score exceeds it; only then is the exact max reduced over
+      // the block's keys (every unit's first block, and rarely later).
       const bool k0ok = g < valid, k1ok = g + 8 < valid;
-      uint32_t pb0[NT], pb1[NT];
-      bool rescale = false;
-      float alpha[NT][2];
+      float v[NT][4];
+      bool grow = false;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        float p[4];
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const float v0 = k0ok ? s[nt][j] * sl2 : -INFINITY;
-          const float v1 = k1ok ? s[nt][j + 2] * sl2 : -INFINITY;
-          float mx = fmaxf(v0, v1);
-          mx = fmaxf(mx, __shfl_xor_sync(kAll8, mx, 4));
-          mx = fmaxf(mx, __shfl_xor_sync(kAll8, mx, 8));
-          mx = fmaxf(mx, __shfl_xor_sync(kAll8, mx, 16));
-          float m_new = m_run[nt][j];
-          if (mx > m_new + kLazy8 || m_new == -INFINITY) m_new = mx;
-          alpha[nt][j] = (m_new == m_run[nt][j]) ? 1.f : exp2f(m_run[nt][j] - m_new);
-          rescale |= alpha[nt][j] != 1.f;
-          m_run[nt][j] = m_new;
-          p[j] = exp2f(v0 - m_new);
-          p[j + 2] = exp2f(v1 - m_new);
+        for (int i = 0; i < 4; ++i) {
+          v[nt][i] = (i < 2 ? k0ok : k1ok) ? s[nt][i] * sl2 : -INFINITY;
+          grow |= v[nt][i] > m_run[nt][i & 1] + kLazy8;
         }
-        const uint32_t x0 = pack2_f16(p[0], p[1]);   // key g,     heads 2t, 2t+1
-        const uint32_t x1 = pack2_f16(p[2], p[3]);   // key g + 8, heads 2t, 2t+1
-        const __half2 h0 = *reinterpret_cast<const __half2*>(&x0);
-        const __half2 h1 = *reinterpret_cast<const __half2*>(&x1);
-        l_run[nt][0] = l_run[nt][0] * alpha[nt][0] + (__low2float(h0) + __low2float(h1));
-        l_run[nt][1] = l_run[nt][1] * alpha[nt][1] + (__high2float(h0) + __high2float(h1));
-        pb0[nt] = movm_t(x0);                          // head g: keys 2t, 2t+1
-        pb1[nt] = movm_t(x1);                          // head g: keys 2t+8, 2t+9
-      }
-      if (__any_sync(kAll8, rescale)) {
+      if (__any_sync(kAll8, grow)) {
+        bool rescale = false;
+        float alpha[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int mt = 0; mt < 8; ++mt) {
-            o[nt][mt][0] *= alpha[nt][0];
-            o[nt][mt][1] *= alpha[nt][1];
-            o[nt][mt][2] *= alpha[nt][0];
-            o[nt][mt][3] *= alpha[nt][1];
+          for (int j = 0; j < 2; ++j) {
+            float mx = fmaxf(v[nt][j], v[nt][j + 2]);
+            mx = fmaxf(mx, __shfl_xor_sync(kAll8, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(kAll8, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(kAll8, mx, 16));
+            float m_new = m_run[nt][j];
+            if (mx > m_new + kLazy8 || m_new == -INFINITY) m_new = mx;
+            alpha[nt][j] = (m_new == m_run[nt][j]) ? 1.f : ex2(m_run[nt][j] - m_new);
+            rescale |= alpha[nt][j] != 1.f;
+            m_run[nt][j] = m_new;
           }
+        if (__any_sync(kAll8, rescale)) {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            l_run[nt][0] *= alpha[nt][0];
+            l_run[nt][1] *= alpha[nt][1];
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+              o[nt][mt][0] *= alpha[nt][0];
+              o[nt][mt][1] *= alpha[nt][1];
+              o[nt][mt][2] *= alpha[nt][0];
+              o[nt][mt][3] *= alpha[nt][1];
+            }
+          }
+        }
+      }
+      uint32_t pb0[NT], pb1[NT];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint32_t x0 = pack2_f16(ex2(v[nt][0] - m_run[nt][0]), ex2(v[nt][1] - m_run[nt][1]));
+        const uint32_t x1 = pack2_f16(ex2(v[nt][2] - m_run[nt][0]), ex2(v[nt][3] - m_run[nt][1]));
+        const __half2 h0 = *reinterpret_cast<const __half2*>(&x0);   // key g,     heads 2t, 2t+1
+        const __half2 h1 = *reinterpret_cast<const __half2*>(&x1);   // key g + 8, heads 2t, 2t+1
+        l_run[nt][0] += __low2float(h0) + __low2float(h1);
+        l_run[nt][1] += __high2float(h0) + __high2float(h1);
+        pb0[nt] = movm_t(x0);                          // head g: keys 2t, 2t+1
+        pb1[nt] = movm_t(x1);                          // head g: keys 2t+8, 2t+9
       }
 
       // ---- O^T += V^T . P^T; V codes of keys past the end become +0
@@ -397,32 +425,38 @@ decode_fp8_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
         }
       }
     named_bar_sync(1, kConsumers8);
+    // warp w merges heads w, w + 4, ...: the combine weights once per head,
+    // then 4 dims per lane
     const bool direct = (u.ns == 1);
-    for (int oi = tid; oi < G * kHD; oi += kConsumers8) {
-      const int h = oi / kHD, d = oi - h * kHD;
-      const int dp = (d & ~15) | ((((d & 15) >> 1) ^ (d >> 4)) << 1) | (d & 1);
+    for (int h = warp; h < G; h += kCW) {
       float M = -INFINITY;
 #pragma unroll
       for (int k = 0; k < kCW; ++k) M = fmaxf(M, comb_ml[(k * G + h) * 2]);
-      float L = 0.f, O = 0.f;
+      float wk[kCW], L = 0.f;
 #pragma unroll
       for (int k = 0; k < kCW; ++k) {
         const float mk = comb_ml[(k * G + h) * 2];
-        const float wk = (mk == -INFINITY) ? 0.f : exp2f(mk - M);
-        L = fmaf(wk, comb_ml[(k * G + h) * 2 + 1], L);
-        O = fmaf(wk, comb[(k * G + h) * kCombRow + dp], O);
+        wk[k] = (mk == -INFINITY) ? 0.f : ex2(mk - M);
+        L = fmaf(wk[k], comb_ml[(k * G + h) * 2 + 1], L);
       }
-      O *= vscale;
+      const float rl = vscale / L;
       const int64_t row = (int64_t)u.b * a.num_q_heads + hq0 + h;
-      if (direct) {
-        outp[row * kHD + d] = __float2bfloat16_rn(O / L);
-      } else {
-        const int64_t pidx = row * a.max_splits + u.s;
-        a.ws_acc[pidx * kHD + d] = O;
-        if (d == 0) {
-          a.ws_ml[pidx * 2 + 0] = M;
-          a.ws_ml[pidx * 2 + 1] = L;
-        }
+      const int64_t pidx = row * a.max_splits + u.s;
+#pragma unroll
+      for (int i = 0; i < kHD / 32; ++i) {
+        const int d = lane + 32 * i;
+        const int dp = (d & ~15) | ((((d & 15) >> 1) ^ (d >> 4)) << 1) | (d & 1);
+        float O = 0.f;
+#pragma unroll
+        for (int k = 0; k < kCW; ++k) O = fmaf(wk[k], comb[(k * G + h) * kCombRow + dp], O);
+        if (direct)
+          outp[row * kHD + d] = __float2bfloat16_rn(O * rl);
+        else
+          a.ws_acc[pidx * kHD + d] = O * vscale;
+      }
+      if (!direct && lane == 0) {
+        a.ws_ml[pidx * 2 + 0] = M;
+        a.ws_ml[pidx * 2 + 1] = L;
       }
     }
     named_bar_sync(1, kConsumers8);
