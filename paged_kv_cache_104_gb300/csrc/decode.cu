@@ -369,6 +369,48 @@ decode_reduce_kernel(const DecodeArgs a) {
   for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(kFull, L, o);
   const float inv = 1.f / L;
   T* outp = static_cast<T*>(a.out) + (int64_t)warp_global * D;
+  if (D == 128) {
+    // lane = 4-column group; split weights are computed once per lane (32
+    // splits at a time) and broadcast, and 8 partial rows are loaded before
+    // their FMAs so the L2 latency of the walk over splits overlaps
+    const float4* acc4 = reinterpret_cast<const float4*>(a.ws_acc) + base * (D / 4) + lane;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < ns; s0 += 32) {
+      float wl = 0.f;
+      if (s0 + lane < ns) {
+        const float ms = a.ws_ml[(base + s0 + lane) * 2];
+        wl = ms == -INFINITY ? 0.f : exp2f(ms - M);
+      }
+      const int cnt = min(32, ns - s0);
+      int k = 0;
+      for (; k + 8 <= cnt; k += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = acc4[(int64_t)(s0 + k + i) * (D / 4)];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float wgt = __shfl_sync(kFull, wl, k + i);
+          o.x = fmaf(wgt, v[i].x, o.x);
+          o.y = fmaf(wgt, v[i].y, o.y);
+          o.z = fmaf(wgt, v[i].z, o.z);
+          o.w = fmaf(wgt, v[i].w, o.w);
+        }
+      }
+      for (; k < cnt; ++k) {
+        const float wgt = __shfl_sync(kFull, wl, k);
+        const float4 v = acc4[(int64_t)(s0 + k) * (D / 4)];
+        o.x = fmaf(wgt, v.x, o.x);
+        o.y = fmaf(wgt, v.y, o.y);
+        o.z = fmaf(wgt, v.z, o.z);
+        o.w = fmaf(wgt, v.w, o.w);
+      }
+    }
+    Elem<T>::store(outp + lane * 4 + 0, o.x * inv);
+    Elem<T>::store(outp + lane * 4 + 1, o.y * inv);
+    Elem<T>::store(outp + lane * 4 + 2, o.z * inv);
+    Elem<T>::store(outp + lane * 4 + 3, o.w * inv);
+    return;
+  }
   for (int d4 = lane; d4 < D / 4; d4 += 32) {
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s = 0; s < ns; ++s) {
