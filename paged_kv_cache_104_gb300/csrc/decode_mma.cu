@@ -8,35 +8,39 @@
 // key and value the sequence has stored, with K_b, V_b those of KV head
 // h / G, read through the sequence's block table.
 //
-// The work is HBM-bound: every cached byte is read once and used for
-// 2*G multiply-adds.  For a GQA group the score and value products are small
-// dense contractions -- [G x 128] . [128 x 16 keys] and [G x 16] . [16 x 128]
-// per 16-token block -- so one warp does each block with 32 m16n8k16 tiles
-// (the G query heads are the M rows, zero-padded to 16).  That leaves the
-// warps far below their issue limit, so the kernel is free to run at the
-// speed of the memory system; doing the same products on CUDA cores needs
-// about eight times as many instructions (shuffle reductions, unpacking).
+// The work is HBM-bound: every cached byte is read once and used for 2*G
+// multiply-adds.  For a GQA group the score and value products are small
+// dense contractions, done per 16-token block on warp-level m16n8k16 tiles
+// with the keys as the M side and the G query heads as the N side (8 columns,
+// or 16 for G = 16):
+//   S^T = K . Q^T   (A = K, 16 keys x 16 dims; B = Q^T)
+//   O^T = V^T . P^T (A = V^T, 16 dims x 16 keys; B = P^T)
+// which is 8 + 8 products per block for G <= 8.
 //
-// Structure (per CTA: one TMA producer warp + four consumer warps, two CTAs
-// per SM, persistent over a flat list of (sequence, KV head, 512-token
-// split) units):
+// Structure (per CTA: one TMA producer warp + four consumer warps,
+// persistent over a flat list of (sequence, KV head, 512-token split) units):
 //  * The producer streams, for each 16-token block, its K and V tiles with
 //    2-D TMA tensor copies (two 64-column halves each, 128-byte swizzle) into
-//    a 3-stage ring of 4 blocks per stage, completing on mbarriers.  It runs
-//    ahead across unit boundaries.
-//  * Consumer warp w takes block w of every stage: ldmatrix (non-transposed
-//    for K, transposed for V; the swizzle makes both conflict-free), 16 MMAs
-//    for S = Q K^T, an online softmax on the S fragments in registers (running
-//    max in the log2 domain, raised lazily only when it grows by more than 8;
-//    max over the 4 lanes of a row by two shuffles), the S accumulators
-//    repacked as bf16 A fragments, then 16 MMAs for O += P V.
+//    a 2-stage ring of 4 blocks per stage, completing on mbarriers.  It runs
+//    ahead across unit boundaries.  With 128 registers per thread and 75 KB of
+//    shared memory, three CTAs (12 consumer warps) share an SM for G <= 4.
+//  * Consumer warp w takes block w of every stage.  Each lane loads its share
+//    of K straight into A fragments with 16-byte shared loads: the order of
+//    the contraction over head dims is permuted per lane (q is loaded with
+//    the same permutation) so that the loads are contiguous and free of bank
+//    conflicts.  The V pairs of the transposed A fragment are assembled from
+//    two key rows with byte permutes, the output dims being permuted to match.
+//    P moves from the S^T accumulator layout to the B layout with movmatrix.
+//  * Online softmax per head: the running max (log2 domain) only has to bound
+//    the scores to within 2^8, so a warp vote decides whether any score
+//    exceeds it; only then is the exact max reduced over the block's keys.
 //  * Each warp keeps its own (m, l, O) for its blocks; at the end of a unit
 //    the four warps merge through shared memory.  A unit that covers its
 //    whole sequence writes the output; otherwise it writes (m, l, O) partials
 //    that the reduce kernel merges.
 //  * Keys past the end of a sequence are masked before the softmax, and the
-//    matching V rows of the last (partial) block are zeroed in shared memory
-//    before P.V, so stale pool contents (even NaN) never reach the output.
+//    matching V values are zeroed in registers, so stale pool contents (even
+//    NaN) never reach the output.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -55,9 +59,10 @@ constexpr int kStageTok = kBPS * kBlockSize;     // 64 tokens
 constexpr int kHalfB = kBlockSize * 128;         // 16 rows x 128 B: one 64-column half
 constexpr int kTileB = 2 * kHalfB;               // one block of K (or V), 4 KiB
 constexpr int kStageB = 2 * kBPS * kTileB;       // K and V of a stage, 32 KiB
-constexpr int kNST = 3;
+constexpr int kNST = 2;
 constexpr int kRingB = kNST * kStageB;
 constexpr int kHD = 128;
+constexpr int kCombRowM = kHD + 4;               // padded row of the merge buffer
 constexpr float kLazyM = 8.0f;
 constexpr unsigned kAllM = 0xffffffffu;
 
@@ -66,7 +71,8 @@ static_assert(32 % kBPS == 0, "a stage never straddles two block-id windows");
 
 template <int G>
 struct MCfg {
-  static constexpr int COMB_B = kCW * G * kHD * 4;            // merged O per warp
+  static constexpr int NT = (G + 7) / 8;                      // head tiles of 8
+  static constexpr int COMB_B = kCW * G * kCombRowM * 4;      // merged O per warp
   static constexpr int ML_B = kCW * G * 2 * 4;
   static constexpr int OFF_COMB = kRingB;
   static constexpr int OFF_ML = OFF_COMB + COMB_B;
@@ -75,15 +81,29 @@ struct MCfg {
   static_assert(G >= 1 && G <= 16 && (G & (G - 1)) == 0, "group of 1..16 heads");
 };
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
+// transpose of an 8x8 16-bit tile held as one m8n8 fragment per lane
+__device__ __forceinline__ uint32_t movm_t16(uint32_t x) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(x));
+  return d;
 }
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+__device__ __forceinline__ uint32_t prmt16(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+// 2^x by the MUFU approximation (subnormal results flush to zero)
+__device__ __forceinline__ float ex2m(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint4 lds128m(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "r"(addr));
+  return v;
 }
 
 // D (16x8 fp32) += A (16x16 bf16, row) . B (16x8 bf16, col)
@@ -116,7 +136,7 @@ __device__ __forceinline__ uint32_t sw_off(int row, int c) {
 }
 
 template <int G, bool FUSE>
-__global__ void __launch_bounds__(kThreadsM, 2)
+__global__ void __launch_bounds__(kThreadsM, G <= 8 ? 3 : 2)
 decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v) {
   using C = MCfg<G>;
@@ -211,45 +231,49 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
   }
 
   // -------------------------------------------------------------- consumers
+  constexpr int NT = C::NT;
   const int g = lane >> 2, t = lane & 3;
-  const bool row_real = g < G;                  // row g of the M tile is a real head
   const float sl2 = a.scale * 1.4426950408889634f;
-  const uint32_t* q32 = static_cast<const uint32_t*>(a.q);
   __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(a.out);
-  // ldmatrix lane roles: matrix mi = lane >> 3, row-in-matrix rr = lane & 7
-  const int mi = lane >> 3, rr = lane & 7;
+  // this lane's K / q pieces: load step i takes the 16-byte chunk kc(i) of
+  // the 64-column half (t >> 1); dims 64 * (t >> 1) + 8 * kc(i) + 0..7 feed
+  // the k-steps 2i and 2i + 1
+  const int khalf = t >> 1;
+  const int kc0 = 4 * (t & 1), kx = (t >> 1) << 1;
+  // V pieces: half g >> 2, chunk 2 * (g & 3) + (j ^ (g & 1)), i.e. dims
+  // 16g + 8 * (j ^ (g & 1)) + 0..7 of the key rows 2t, 2t+1, 2t+8, 2t+9
+  const int vhalf = g >> 2;
   uint32_t consumed = 0;
 
   for (int w = blockIdx.x; w < total; w += gridDim.x) {
     const Unit u = find_unit(a, cu, w);
     const int hq0 = u.g * G;
-    // Q as A fragments: a0 = (row g, d 16ks+2t..+1), a2 = (row g, d 16ks+8+2t..+1);
-    // rows g+8 (a1, a3) are real only when G == 16.
-    uint32_t qa[8][2], qb[8][2];
+    // Q^T as B fragments of head 8nt + g, in the lane's K order
+    uint4 qf[NT][4];
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      qa[ks][0] = qa[ks][1] = qb[ks][0] = qb[ks][1] = 0u;
+    for (int nt = 0; nt < NT; ++nt) {
+      const int hh = 8 * nt + g;
+      const __nv_bfloat16* qrow =
+          static_cast<const __nv_bfloat16*>(a.q) + ((int64_t)u.b * a.num_q_heads + hq0 + hh) * kHD;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        qf[nt][i] = hh < G ? __ldg(reinterpret_cast<const uint4*>(qrow + 64 * khalf + 8 * (kc0 + (i ^ kx))))
+                           : make_uint4(0, 0, 0, 0);
     }
-    if (row_real) {
-      const uint32_t* qrow = q32 + ((int64_t)u.b * a.num_q_heads + hq0 + g) * (kHD / 2);
+    // O^T accumulators: o[nt][mt] holds dims d(mt), d(mt) + 1 (c0/c1, c2/c3)
+    // with d(mt) = 16g + 8 * ((mt >> 2) ^ (g & 1)) + 2 * (mt & 3), for heads
+    // 8nt + 2t (c0, c2) and 8nt + 2t + 1 (c1, c3)
+    float o[NT][8][4];
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        qa[ks][0] = __ldg(qrow + ks * 8 + t);
-        qa[ks][1] = __ldg(qrow + ks * 8 + 4 + t);
-      }
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) o[nt][mt][0] = o[nt][mt][1] = o[nt][mt][2] = o[nt][mt][3] = 0.f;
+    float m_run[NT][2], l_run[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      m_run[nt][0] = m_run[nt][1] = -INFINITY;
+      l_run[nt][0] = l_run[nt][1] = 0.f;
     }
-    if (G == 16) {
-      const uint32_t* qrow = q32 + ((int64_t)u.b * a.num_q_heads + hq0 + g + 8) * (kHD / 2);
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        qb[ks][0] = __ldg(qrow + ks * 8 + t);
-        qb[ks][1] = __ldg(qrow + ks * 8 + 4 + t);
-      }
-    }
-    float o[16][4];
-#pragma unroll
-    for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
 
     const int nblk = (u.tok_end - 1) / kBlockSize - u.tok_begin / kBlockSize + 1;
     const int nst = (nblk + kBPS - 1) / kBPS;
@@ -261,164 +285,217 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
       }
       const int tok0 = u.tok_begin + (st * kBPS + warp) * kBlockSize;
       const int valid = min(kBlockSize, u.tok_end - tok0);   // keys of this warp's block
-      if (valid > 0) {
-        const uint32_t kt = sbase + buf * kStageB + warp * kTileB;
-        const uint32_t vt = kt + kBPS * kTileB;
-        if (FUSE && u.s == u.ns - 1 && tok0 + valid == u.tok_end) {
-          // this block holds the sequence's new token (position tok_end - 1):
-          // the staged tile still has the pool's old row there, so put the new
-          // key and value into shared memory and into the pool.  Lanes 0-15
-          // move the 16-byte chunks of K, lanes 16-31 those of V.
-          const int r = valid - 1;
-          const int c = lane & 15;
-          const bool is_v = lane >= 16;
-          const int64_t src = (((int64_t)u.b * a.num_kv_heads + u.g) * kHD) + c * 8;
-          const uint4 val = __ldg(reinterpret_cast<const uint4*>(
-              static_cast<const __nv_bfloat16*>(is_v ? a.v_new : a.k_new) + src));
-          unsigned char* tile = smem + buf * kStageB + (is_v ? kBPS * kTileB : 0) + warp * kTileB;
-          *reinterpret_cast<uint4*>(tile + sw_off(r, c)) = val;
-          const int blk = __ldg(a.block_table + (int64_t)u.b * a.bt_stride + (tok0 / kBlockSize));
-          if (blk >= 0 && (int64_t)blk < a.num_blocks) {
-            __nv_bfloat16* pool = const_cast<__nv_bfloat16*>(
-                static_cast<const __nv_bfloat16*>(is_v ? a.v_cache : a.k_cache));
-            const int64_t dst = (((int64_t)blk * a.num_kv_heads + u.g) * kBlockSize + r) * kHD + c * 8;
-            *reinterpret_cast<uint4*>(pool + dst) = val;
-          }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
+      if (valid <= 0) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * buf);
+        continue;
+      }
+      const uint32_t kt = sbase + buf * kStageB + warp * kTileB;
+      const uint32_t vt = kt + kBPS * kTileB;
+      if (FUSE && u.s == u.ns - 1 && tok0 + valid == u.tok_end) {
+        // this block holds the sequence's new token (position tok_end - 1):
+        // the staged tile still has the pool's old row there, so put the new
+        // key and value into shared memory and into the pool.  Lanes 0-15
+        // move the 16-byte chunks of K, lanes 16-31 those of V.
+        const int r = valid - 1;
+        const int c = lane & 15;
+        const bool is_v = lane >= 16;
+        const int64_t src = (((int64_t)u.b * a.num_kv_heads + u.g) * kHD) + c * 8;
+        const uint4 val = __ldg(reinterpret_cast<const uint4*>(
+            static_cast<const __nv_bfloat16*>(is_v ? a.v_new : a.k_new) + src));
+        unsigned char* tile = smem + buf * kStageB + (is_v ? kBPS * kTileB : 0) + warp * kTileB;
+        *reinterpret_cast<uint4*>(tile + sw_off(r, c)) = val;
+        const int blk = __ldg(a.block_table + (int64_t)u.b * a.bt_stride + (tok0 / kBlockSize));
+        if (blk >= 0 && (int64_t)blk < a.num_blocks) {
+          __nv_bfloat16* pool = const_cast<__nv_bfloat16*>(
+              static_cast<const __nv_bfloat16*>(is_v ? a.v_cache : a.k_cache));
+          const int64_t dst = (((int64_t)blk * a.num_kv_heads + u.g) * kBlockSize + r) * kHD + c * 8;
+          *reinterpret_cast<uint4*>(pool + dst) = val;
         }
-        if (valid < kBlockSize) {
-          // zero the V rows past the sequence end (whole rows, so the swizzle does not matter)
-          unsigned char* vrow = smem + buf * kStageB + kBPS * kTileB + warp * kTileB;
-          for (int i = lane; i < (kBlockSize - valid) * 16; i += 32) {
-            const int row = valid + (i >> 4), c = i & 15;
-            *reinterpret_cast<uint4*>(vrow + (c >> 3) * kHalfB + row * 128 + (c & 7) * 16) =
-                make_uint4(0, 0, 0, 0);
-          }
-          // order these generic-proxy writes before the TMA refill of this slot
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
+        // order these generic-proxy writes before the TMA refill of this slot
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+      }
+      // ---- K of keys g and g + 8, straight into A fragments
+      uint4 kg[4], kh[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int c = kc0 + (i ^ kx);
+        kg[i] = lds128m(kt + khalf * kHalfB + g * 128 + ((c ^ g) << 4));
+        kh[i] = lds128m(kt + khalf * kHalfB + (g + 8) * 128 + ((c ^ g) << 4));
+      }
+      // ---- S^T = K . Q^T: two dependent chains of four products
+      float s[NT][4], s2[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s[nt][i] = s2[nt][i] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          mma16816(s[nt], kg[i].x, kh[i].x, kg[i].y, kh[i].y, qf[nt][i].x, qf[nt][i].y);
+          mma16816(s2[nt], kg[i].z, kh[i].z, kg[i].w, kh[i].w, qf[nt][i].z, qf[nt][i].w);
         }
-        // ---- S = Q K^T : two n-tiles of 8 keys
-        float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        const int krow = ((mi >> 1) << 3) + rr;   // key row this lane addresses
+      // ---- V of keys 2t, 2t+1, 2t+8, 2t+9; then the slot is free
+      uint4 va[2], vb[2], vc[2], vd[2];
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          uint32_t kb[4];
-          ldsm_x4(kt + sw_off(krow, 2 * ks + (mi & 1)), kb);
-          mma16816(s[0], qa[ks][0], qb[ks][0], qa[ks][1], qb[ks][1], kb[0], kb[1]);
-          mma16816(s[1], qa[ks][0], qb[ks][0], qa[ks][1], qb[ks][1], kb[2], kb[3]);
-        }
-        // ---- online softmax on the fragments: row g holds keys 8nt+2t, +1 (c0, c1),
-        // row g+8 the same keys (c2, c3)
-        float p[2][4];
-        float alpha[2];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          float v[4];
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              const int key = nt * 8 + 2 * t + j;
-              v[nt * 2 + j] = key < valid ? s[nt][2 * r + j] * sl2 : -INFINITY;
-            }
-          float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
-          mx = fmaxf(mx, __shfl_xor_sync(kAllM, mx, 1));
-          mx = fmaxf(mx, __shfl_xor_sync(kAllM, mx, 2));
-          float m_new = m_run[r];
-          if (mx > m_run[r] + kLazyM || m_run[r] == -INFINITY) m_new = mx;
-          alpha[r] = (m_new == m_run[r]) ? 1.f : exp2f(m_run[r] - m_new);
-          m_run[r] = m_new;
-          float sum = 0.f;
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              const float e = exp2f(v[nt * 2 + j] - m_new);
-              p[nt][2 * r + j] = e;
-            }
-          // the sum uses the bf16-rounded weights that P.V multiplies
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            const uint32_t pk = pack2_bf16(p[nt][2 * r], p[nt][2 * r + 1]);
-            sum += bf16lo(pk) + bf16hi(pk);
-          }
-          l_run[r] = l_run[r] * alpha[r] + sum;
-        }
-        if (__any_sync(kAllM, alpha[0] != 1.f || alpha[1] != 1.f)) {
-#pragma unroll
-          for (int n = 0; n < 16; ++n) {
-            o[n][0] *= alpha[0];
-            o[n][1] *= alpha[0];
-            o[n][2] *= alpha[1];
-            o[n][3] *= alpha[1];
-          }
-        }
-        // S accumulators -> A fragments of P (keys 0-7 from n-tile 0, 8-15 from n-tile 1)
-        const uint32_t pa0 = pack2_bf16(p[0][0], p[0][1]);
-        const uint32_t pa1 = pack2_bf16(p[0][2], p[0][3]);
-        const uint32_t pa2 = pack2_bf16(p[1][0], p[1][1]);
-        const uint32_t pa3 = pack2_bf16(p[1][2], p[1][3]);
-        // ---- O += P V : 16 n-tiles of 8 columns, V through transposed ldmatrix
-        const int vrow = ((mi & 1) << 3) + rr;
-#pragma unroll
-        for (int np = 0; np < 8; ++np) {
-          uint32_t vb[4];
-          ldsm_x4_t(vt + sw_off(vrow, 2 * np + (mi >> 1)), vb);
-          mma16816(o[2 * np], pa0, pa1, pa2, pa3, vb[0], vb[1]);
-          mma16816(o[2 * np + 1], pa0, pa1, pa2, pa3, vb[2], vb[3]);
-        }
+      for (int j = 0; j < 2; ++j) {
+        const int c = 2 * (g & 3) + (j ^ (g & 1));
+        const uint32_t base = vt + vhalf * kHalfB;
+        va[j] = lds128m(base + (2 * t) * 128 + ((c ^ (2 * t)) << 4));
+        vb[j] = lds128m(base + (2 * t + 1) * 128 + ((c ^ (2 * t + 1)) << 4));
+        vc[j] = lds128m(base + (2 * t + 8) * 128 + ((c ^ (2 * t)) << 4));
+        vd[j] = lds128m(base + (2 * t + 9) * 128 + ((c ^ (2 * t + 1)) << 4));
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * buf);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s[nt][i] += s2[nt][i];
+
+      // ---- online softmax per head; this lane holds keys g, g+8 of heads 2t, 2t+1
+      const bool k0ok = g < valid, k1ok = g + 8 < valid;
+      float v[NT][4];
+      bool grow = false;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          v[nt][i] = (i < 2 ? k0ok : k1ok) ? s[nt][i] * sl2 : -INFINITY;
+          grow |= v[nt][i] > m_run[nt][i & 1] + kLazyM;
+        }
+      if (__any_sync(kAllM, grow)) {
+        bool rescale = false;
+        float alpha[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            float mx = fmaxf(v[nt][j], v[nt][j + 2]);
+            mx = fmaxf(mx, __shfl_xor_sync(kAllM, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(kAllM, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(kAllM, mx, 16));
+            float m_new = m_run[nt][j];
+            if (mx > m_new + kLazyM || m_new == -INFINITY) m_new = mx;
+            alpha[nt][j] = (m_new == m_run[nt][j]) ? 1.f : ex2m(m_run[nt][j] - m_new);
+            rescale |= alpha[nt][j] != 1.f;
+            m_run[nt][j] = m_new;
+          }
+        if (__any_sync(kAllM, rescale)) {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            l_run[nt][0] *= alpha[nt][0];
+            l_run[nt][1] *= alpha[nt][1];
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+              o[nt][mt][0] *= alpha[nt][0];
+              o[nt][mt][1] *= alpha[nt][1];
+              o[nt][mt][2] *= alpha[nt][0];
+              o[nt][mt][3] *= alpha[nt][1];
+            }
+          }
+        }
+      }
+      uint32_t pb0[NT], pb1[NT];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        // bf16 weights (what P.V multiplies; the sum uses the same values)
+        const uint32_t x0 = pack2_bf16(ex2m(v[nt][0] - m_run[nt][0]), ex2m(v[nt][1] - m_run[nt][1]));
+        const uint32_t x1 = pack2_bf16(ex2m(v[nt][2] - m_run[nt][0]), ex2m(v[nt][3] - m_run[nt][1]));
+        l_run[nt][0] += bf16lo(x0) + bf16lo(x1);
+        l_run[nt][1] += bf16hi(x0) + bf16hi(x1);
+        pb0[nt] = movm_t16(x0);   // head g: keys 2t, 2t+1
+        pb1[nt] = movm_t16(x1);   // head g: keys 2t+8, 2t+9
+      }
+
+      // ---- O^T += V^T . P^T; V of keys past the end becomes +0
+      if (valid < kBlockSize) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          if (2 * t >= valid) va[j] = make_uint4(0, 0, 0, 0);
+          if (2 * t + 1 >= valid) vb[j] = make_uint4(0, 0, 0, 0);
+          if (2 * t + 8 >= valid) vc[j] = make_uint4(0, 0, 0, 0);
+          if (2 * t + 9 >= valid) vd[j] = make_uint4(0, 0, 0, 0);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const uint32_t aw[4] = {va[j].x, va[j].y, va[j].z, va[j].w};
+        const uint32_t bw[4] = {vb[j].x, vb[j].y, vb[j].z, vb[j].w};
+        const uint32_t cw[4] = {vc[j].x, vc[j].y, vc[j].z, vc[j].w};
+        const uint32_t dw[4] = {vd[j].x, vd[j].y, vd[j].z, vd[j].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t a0 = prmt16(aw[e], bw[e], 0x5410u);   // keys 2t, 2t+1 at dim d
+          const uint32_t a1 = prmt16(aw[e], bw[e], 0x7632u);   // ... at dim d + 1
+          const uint32_t a2 = prmt16(cw[e], dw[e], 0x5410u);   // keys 2t+8, 2t+9 at dim d
+          const uint32_t a3 = prmt16(cw[e], dw[e], 0x7632u);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma16816(o[nt][4 * j + e], a0, a1, a2, a3, pb0[nt], pb1[nt]);
+        }
+      }
     }
 
     // ---- merge the four warps of this unit
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      l_run[r] += __shfl_xor_sync(kAllM, l_run[r], 1);
-      l_run[r] += __shfl_xor_sync(kAllM, l_run[r], 2);
-    }
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int row = g + 8 * r;
-      if (row < G) {
-        if (t == 0) {
-          comb_ml[(warp * G + row) * 2 + 0] = m_run[r];
-          comb_ml[(warp * G + row) * 2 + 1] = l_run[r];
-        }
-#pragma unroll
-        for (int n = 0; n < 16; ++n)
-          *reinterpret_cast<float2*>(comb + (warp * G + row) * kHD + n * 8 + 2 * t) =
-              make_float2(o[n][2 * r], o[n][2 * r + 1]);
+      for (int j = 0; j < 2; ++j) {
+        l_run[nt][j] += __shfl_xor_sync(kAllM, l_run[nt][j], 4);
+        l_run[nt][j] += __shfl_xor_sync(kAllM, l_run[nt][j], 8);
+        l_run[nt][j] += __shfl_xor_sync(kAllM, l_run[nt][j], 16);
       }
-    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int hh = 8 * nt + 2 * t + j;
+        if (hh < G) {
+          if (g == 0) {
+            comb_ml[(warp * G + hh) * 2 + 0] = m_run[nt][j];
+            comb_ml[(warp * G + hh) * 2 + 1] = l_run[nt][j];
+          }
+          float* crow = comb + (warp * G + hh) * kCombRowM + 16 * g;
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt)
+            *reinterpret_cast<float2*>(crow + 8 * ((mt >> 2) ^ (g & 1)) + 2 * (mt & 3)) =
+                make_float2(o[nt][mt][j], o[nt][mt][j + 2]);
+        }
+      }
     named_bar_sync(1, kConsumersM);
+    // warp w merges heads w, w + 4, ...: the combine weights once per head,
+    // then 4 dims per lane
     const bool direct = (u.ns == 1);
-    for (int oi = tid; oi < G * kHD; oi += kConsumersM) {
-      const int h = oi / kHD, d = oi - h * kHD;
+    for (int h = warp; h < G; h += kCW) {
       float M = -INFINITY;
 #pragma unroll
       for (int k = 0; k < kCW; ++k) M = fmaxf(M, comb_ml[(k * G + h) * 2]);
-      float L = 0.f, O = 0.f;
+      float wk[kCW], L = 0.f;
 #pragma unroll
       for (int k = 0; k < kCW; ++k) {
         const float mk = comb_ml[(k * G + h) * 2];
-        const float wk = (mk == -INFINITY) ? 0.f : exp2f(mk - M);
-        L = fmaf(wk, comb_ml[(k * G + h) * 2 + 1], L);
-        O = fmaf(wk, comb[(k * G + h) * kHD + d], O);
+        wk[k] = (mk == -INFINITY) ? 0.f : ex2m(mk - M);
+        L = fmaf(wk[k], comb_ml[(k * G + h) * 2 + 1], L);
       }
+      const float rl = 1.f / L;
       const int64_t row = (int64_t)u.b * a.num_q_heads + hq0 + h;
-      if (direct) {
-        outp[row * kHD + d] = __float2bfloat16_rn(O / L);
-      } else {
-        const int64_t pidx = row * a.max_splits + u.s;
-        a.ws_acc[pidx * kHD + d] = O;
-        if (d == 0) {
-          a.ws_ml[pidx * 2 + 0] = M;
-          a.ws_ml[pidx * 2 + 1] = L;
-        }
+      const int64_t pidx = row * a.max_splits + u.s;
+#pragma unroll
+      for (int i = 0; i < kHD / 32; ++i) {
+        const int d = lane + 32 * i;
+        float O = 0.f;
+#pragma unroll
+        for (int k = 0; k < kCW; ++k) O = fmaf(wk[k], comb[(k * G + h) * kCombRowM + d], O);
+        if (direct)
+          outp[row * kHD + d] = __float2bfloat16_rn(O * rl);
+        else
+          a.ws_acc[pidx * kHD + d] = O;
+      }
+      if (!direct && lane == 0) {
+        a.ws_ml[pidx * 2 + 0] = M;
+        a.ws_ml[pidx * 2 + 1] = L;
       }
     }
     named_bar_sync(1, kConsumersM);
@@ -437,7 +514,8 @@ cudaError_t launch_g(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<G, FUSE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const int per_sm = smem <= 113 * 1024 ? 2 : 1;
+  const int by_smem = (int)((228 * 1024) / (smem + 1024));
+  const int per_sm = by_smem < 1 ? 1 : (by_smem > (G <= 8 ? 3 : 2) ? (G <= 8 ? 3 : 2) : by_smem);
   const int64_t upper = (int64_t)a.num_seqs * a.num_kv_heads * a.max_splits;
   const int grid = (int)(upper < (int64_t)num_sms * per_sm ? upper : (int64_t)num_sms * per_sm);
   decode_mma_kernel<G, FUSE><<<grid, kThreadsM, smem, stream>>>(a, tm_k, tm_v);
