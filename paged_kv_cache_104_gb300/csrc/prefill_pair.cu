@@ -27,12 +27,13 @@
 //    the other head's products execute.
 // Roles (352 threads):
 //   warps 0-3 / 4-7   softmax of head A / B: thread r owns query row r (TMEM
-//                     lane r).  Pass 1 reads its S row in 32-column pieces for
-//                     the row max (causal mask on the diagonal tiles); the max
-//                     is raised lazily, only when it grows by more than 2^8,
-//                     and then O is rescaled in TMEM.  Pass 2 re-reads S, forms
-//                     p = 2^(s*scale*log2e - m) with one FMA and ex2 per score,
-//                     sums it and stores it as bf16 into TMEM.  Epilogue O / l.
+//                     lane r).  It loads its whole S row into registers (four
+//                     TMEM loads in flight), takes the row max (causal mask on
+//                     the diagonal tiles); the max is raised lazily, only when
+//                     it grows by more than 2^8, and then O is rescaled in
+//                     TMEM.  It forms p = 2^(s*scale*log2e - m) with one FMA and
+//                     ex2 per score, sums it and stores it as bf16 into TMEM.
+//                     Epilogue O / l.
 //   warps 8-9         K/V producers (cp.async; once their copies of a tile
 //                     landed: proxy fence, mbarrier arrive).
 //   warp 10           TMEM allocator and single-thread MMA issuer:
@@ -249,7 +250,10 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
       };
       // The two heads alternate on the tensor core: while head A's softmax
       // turns S_A into P_A, the products of head B run, and the other way
-      // round.  S_h (holding P_h) is rewritten only after P_h V has completed.
+      // round.  Q_h K_{j+1}^T rewrites S_h, which holds P_h, right behind
+      // P_h V_j: tcgen05.mma operations issued by one thread execute in issue
+      // order, so the earlier product has read P_h before the later one
+      // writes there, and no wait for its completion is needed.
       if (ok) ok = wait_or_abort(bar(PB_KVF + 0), 0, abort_flag, a.err);
       if (ok) {
         tc_fence_after();
@@ -266,9 +270,7 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
           if (hh == 1) mma_commit(bar(PB_KVE + j % NST));   // tile j no longer needed
           if (more) {
             if (hh == 0) ok = wait_or_abort(bar(PB_KVF + (j + 1) % NST), ((j + 1) / NST) & 1, abort_flag, a.err);
-            if (ok) ok = wait_or_abort(bar(PB_OD + hh), j & 1, abort_flag, a.err);
             if (!ok) break;
-            tc_fence_after();
             issue_qk(hh, j + 1);
           }
         }
@@ -290,26 +292,31 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
       tc_fence_after();
       const int k0 = j * BN;
       const bool diag = k0 + BN - 1 > a.prior_len + q0;   // causal mask needed
-      // pass 1: row max over 128 scores, 32 columns at a time
-      float mx0 = -INFINITY, mx1 = -INFINITY;
+      // the whole S row into registers: four loads in flight, one wait
+      float t[BN / 32][32];
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        float t[32];
-        tmem_ld32(lane_base + col_s + c * 32, t);
-        tmem_wait_ld();
-        reg_fence(t);
-        if (diag) {
+      for (int c = 0; c < BN / 32; ++c) tmem_ld32(lane_base + col_s + c * 32, t[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) reg_fence(t[c]);
+      if (diag) {
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if (k0 + c * 32 + i > row_pos) t[i] = -INFINITY;
-        }
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          mx0 = fmaxf(mx0, t[i]);
-          mx1 = fmaxf(mx1, t[i + 1]);
-        }
+            if (k0 + c * 32 + i > row_pos) t[c][i] = -INFINITY;
       }
-      const float mx = fmaxf(mx0, mx1) * sl2;   // scale > 0 commutes with max
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          mx4[0] = fmaxf(mx4[0], t[c][i]);
+          mx4[1] = fmaxf(mx4[1], t[c][i + 1]);
+          mx4[2] = fmaxf(mx4[2], t[c][i + 2]);
+          mx4[3] = fmaxf(mx4[3], t[c][i + 3]);
+        }
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
       float m_new = m_run;
       if (mx > m_run + kLazyP || m_run == -INFINITY) m_new = mx;
       const float alpha = (m_new == m_run) ? 1.f : fast_exp2(m_run - m_new);
@@ -331,25 +338,16 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
         }
         tmem_wait_st();
       }
-      // pass 2: p = 2^(s*scale*log2e - m), written as bf16 pairs over the
-      // columns of S already read (32 scores -> 16 columns)
+      // p = 2^(s*scale*log2e - m), written as bf16 pairs over the first 64
+      // columns of S
       float2 sum2 = make_float2(0.f, 0.f);
       const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-m_new, -m_new);
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) {
-        float t[32];
-        tmem_ld32(lane_base + col_s + c * 32, t);
-        tmem_wait_ld();
-        reg_fence(t);
-        if (diag) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (k0 + c * 32 + i > row_pos) t[i] = -INFINITY;
-        }
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float2 x = ffma2(make_float2(t[i], t[i + 1]), sl2x2, negm);
+          const float2 x = ffma2(make_float2(t[c][i], t[c][i + 1]), sl2x2, negm);
           const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
           sum2 = fadd2(sum2, pp);
           pk[i / 2] = pack_bf16(pp.x, pp.y);
