@@ -283,14 +283,12 @@ decode_fp8_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
         kg1 = lds128(k8 + sw8(g, 2 * t + 1));
         kh0 = lds128(k8 + sw8(g + 8, 2 * t));
         kh1 = lds128(k8 + sw8(g + 8, 2 * t + 1));
-        va = lds128(v8 + sw8(2 * t, g));
-        vb = lds128(v8 + sw8(2 * t + 1, g));
-        vc = lds128(v8 + sw8(2 * t + 8, g));
-        vd = lds128(v8 + sw8(2 * t + 9, g));
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * buf);   // codes are in registers: free the slot
-      if (valid <= 0) continue;
+      if (valid <= 0) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * buf);
+        continue;
+      }
 
       // ---- S^T = K . Q^T over 8 k-steps of 16 (permuted) head dimensions
       float s[NT][4], s2[NT][4];   // even and odd k-steps: two short dependency chains
@@ -313,6 +311,15 @@ decode_fp8_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
         for (int i = 0; i < 4; ++i) s[nt][i] += s2[nt][i];
 
+      {
+        const unsigned char* v8 = smem + buf * kStage8 + warp * kTile8 + kBPS * kTile8;
+        va = lds128(v8 + sw8(2 * t, g));
+        vb = lds128(v8 + sw8(2 * t + 1, g));
+        vc = lds128(v8 + sw8(2 * t + 8, g));
+        vd = lds128(v8 + sw8(2 * t + 9, g));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * buf);   // codes are in registers: free the slot
       // ---- online softmax per head (column); this lane holds keys g, g+8.
       // The running max m only has to bound the scores to within the lazy
       // threshold (p = 2^(s - m) <= 2^8 stays in f16), so a warp vote decides
