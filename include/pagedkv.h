@@ -237,6 +237,42 @@ pkv_status pkv_paged_decode_attention_fp8(void *out, const void *q, const void *
                                           pkv_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Latent (MLA-style) cache.  "The KV cache and prefix caching", section "What
+ * prefill stores and decode reads", names multi-head latent attention: the
+ * cache stores a low-rank projection instead of the keys and values.  This
+ * library's reading: per token and layer one latent c of rank r (bf16) in a
+ * pool [num_blocks][block_size][rank]; query head h sees the key W_K[h] c and
+ * the value W_V[h] c, with W_K, W_V bf16 [num_q_heads][head_dim][rank].
+ * ------------------------------------------------------------------------- */
+
+/* Scatter c_new [T][rank] (bf16, device) into the latent pool at
+ * slot_mapping (int64 [T]; slot = block * block_size + row; negative = skip;
+ * beyond the pool = skipped and reported in the device error word).
+ * rank * 2 bytes must be a multiple of 16.  Byte-exact copy. */
+pkv_status pkv_latent_append(const void *c_new, void *c_cache, const int64_t *slot_mapping,
+                             int64_t num_tokens, int64_t num_blocks, int rank, int block_size,
+                             pkv_stream_t stream);
+
+/* Device scratch pkv_mla_decode_attention needs (absorbed queries, the
+ * attention over the latent, split partials). */
+size_t pkv_mla_workspace_bytes(int num_seqs, int num_q_heads, int rank, int max_seq_len);
+
+/* Decode over the latent cache: out[b][h] = sum_j softmax_j(scale * q[b][h] .
+ * W_K[h] c_j) W_V[h] c_j over the seq_lens[b] latents of sequence b, read
+ * through block_table (int32 [num_seqs][max_blocks_per_seq]).  q, out bf16
+ * [num_seqs][num_q_heads][head_dim].  Computed with the projections absorbed:
+ * q~ = W_K^T q, attention of q~ over the latents, then W_V applied to the
+ * result.  Supported: num_q_heads 32, head_dim 128, rank 128, block_size 16
+ * (PKV_EUNSUPPORTED otherwise).  workspace: 256-byte aligned, at least
+ * pkv_mla_workspace_bytes(...) bytes (PKV_ERANGE if smaller). */
+pkv_status pkv_mla_decode_attention(void *out, const void *q, const void *w_k, const void *w_v,
+                                    const void *c_cache, const int32_t *block_table,
+                                    const int32_t *seq_lens, int num_seqs, int max_blocks_per_seq,
+                                    int max_seq_len, int64_t num_blocks, int num_q_heads,
+                                    int head_dim, int rank, int block_size, float scale,
+                                    void *workspace, size_t workspace_bytes, pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Prefix caching (host-only): chained block hashes and a hash -> block index.
  * "The KV cache and prefix caching", section "A prefix already in the cache
  * can skip its prefill": the prompt is hashed block by block; a block's

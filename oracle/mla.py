@@ -52,13 +52,15 @@ def mla_decode(q, w_k, w_v, pool, block_table, seq_lens, scale, seqs=None) -> to
     for b in seqs:
         n = int(seq_lens[b])
         c = gather_latents(pool, block_table[b], n)              # [n, r]
-        k = torch.einsum("hdr,jr->hjd", wk, c)                   # [Hq, n, D]
-        v = torch.einsum("hdr,jr->hjd", wv, c)
-        s = torch.einsum("hd,hjd->hj", q[b].to(torch.float64), k) * scale
-        s = s - s.max(dim=1, keepdim=True).values
-        p = torch.exp(s)
-        p = p / p.sum(dim=1, keepdim=True)
-        outs.append(torch.einsum("hj,hjd->hd", p, v))
+        qb = q[b].to(torch.float64)
+        o = torch.empty(q.shape[1], q.shape[2], dtype=torch.float64)
+        for h in range(q.shape[1]):
+            k = c @ wk[h].T                                      # [n, D]: k_j = W_K[h] c_j
+            v = c @ wv[h].T
+            s = (k @ qb[h]) * scale
+            p = torch.exp(s - s.max())
+            o[h] = (p / p.sum()) @ v
+        outs.append(o)
     return torch.stack(outs)
 
 

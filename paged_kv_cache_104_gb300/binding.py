@@ -27,6 +27,7 @@ EXPORTS = ("pkv_kv_append", "pkv_decode_workspace_bytes", "pkv_paged_decode_atte
            "pkv_paged_decode_attention_append", "pkv_paged_decode_attention_noalloc", "pkv_chunked_prefill_attention",
            "pkv_get_device_error", "pkv_status_str", "pkv_abi_version",
            "pkv_kv_append_fp8", "pkv_paged_decode_attention_fp8",
+           "pkv_latent_append", "pkv_mla_workspace_bytes", "pkv_mla_decode_attention",
            "pkv_fnv1a64", "pkv_prefix_hash_blocks", "pkv_prefix_cache_create",
            "pkv_prefix_cache_destroy", "pkv_prefix_cache_size", "pkv_prefix_cache_insert",
            "pkv_prefix_cache_evict", "pkv_prefix_cache_match", "pkv_prefix_plan")
@@ -69,6 +70,13 @@ def load():
         lib.pkv_paged_decode_attention_fp8.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i64, i, i,
                                                        i, i, f, p, sz, p]
         lib.pkv_paged_decode_attention_fp8.restype = ctypes.c_int
+        lib.pkv_latent_append.argtypes = [p, p, p, i64, i64, i, i, p]
+        lib.pkv_latent_append.restype = ctypes.c_int
+        lib.pkv_mla_workspace_bytes.argtypes = [i, i, i, i]
+        lib.pkv_mla_workspace_bytes.restype = sz
+        lib.pkv_mla_decode_attention.argtypes = [p, p, p, p, p, p, p, i, i, i, i64, i, i, i, i, f,
+                                                 p, sz, p]
+        lib.pkv_mla_decode_attention.restype = ctypes.c_int
         u64p = ctypes.POINTER(ctypes.c_uint64)
         i32p = ctypes.POINTER(ctypes.c_int32)
         lib.pkv_fnv1a64.argtypes = [p, sz]
@@ -197,6 +205,35 @@ def paged_decode_attention_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block
         _ptr(block_table), _ptr(seq_lens), b, int(block_table.shape[1]), int(max_seq_len), nb, hq,
         hkv, d, bs, float(scale), _ptr(workspace), ws_bytes, _stream(stream))
     _check("pkv_paged_decode_attention_fp8", st)
+
+
+def latent_append(c_new, c_cache, slot_mapping, stream=None) -> None:
+    """bf16 c_new [T, r] -> latent pool [NB, bs, r] at slot_mapping (int64)."""
+    nb, bs, r = c_cache.shape
+    st = load().pkv_latent_append(_ptr(c_new), _ptr(c_cache), _ptr(slot_mapping),
+                                  int(slot_mapping.shape[0]), nb, r, bs, _stream(stream))
+    _check("pkv_latent_append", st)
+
+
+def mla_workspace(num_seqs: int, num_q_heads: int, rank: int, max_seq_len: int, device=None):
+    n = int(load().pkv_mla_workspace_bytes(num_seqs, num_q_heads, rank, max_seq_len))
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def mla_decode_attention(out, q, w_k, w_v, c_cache, block_table, seq_lens, max_seq_len: int,
+                         scale: float, workspace=None, stream=None) -> None:
+    """Decode over the latent pool [NB, bs, r]; q/out bf16 [B, Hq, D];
+    w_k, w_v bf16 [Hq, D, r]."""
+    b, hq, d = q.shape
+    nb, bs, r = c_cache.shape
+    if workspace is None:
+        workspace = mla_workspace(b, hq, r, max_seq_len, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = load().pkv_mla_decode_attention(
+        _ptr(out), _ptr(q), _ptr(w_k), _ptr(w_v), _ptr(c_cache), _ptr(block_table),
+        _ptr(seq_lens), b, int(block_table.shape[1]), int(max_seq_len), nb, hq, d, r, bs,
+        float(scale), _ptr(workspace), ws_bytes, _stream(stream))
+    _check("pkv_mla_decode_attention", st)
 
 
 def paged_decode_attention_noalloc(out, q, k_cache, v_cache, block_table, seq_lens,

@@ -326,6 +326,101 @@ pkv_status pkv_paged_decode_attention_fp8(void* out, const void* q, const void* 
              : PKV_ECUDA;
 }
 
+pkv_status pkv_latent_append(const void* c_new, void* c_cache, const int64_t* slot_mapping,
+                             int64_t num_tokens, int64_t num_blocks, int rank, int block_size,
+                             pkv_stream_t stream) {
+  if (num_tokens < 0 || num_blocks < 1 || rank < 1 || block_size < 1) return PKV_EINVAL;
+  if (block_size != pkv::kBlockSize || (rank * 2) % 16 != 0) return PKV_EUNSUPPORTED;
+  if (num_tokens == 0) return PKV_OK;
+  if (!c_new || !c_cache || !slot_mapping) return PKV_EINVAL;
+  if (!aligned16(c_new) || !aligned16(c_cache) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return PKV_EINVAL;
+  int* err = nullptr;
+  int sms = 0;
+  pkv_status st = device_state(&err, &sms);
+  if (st != PKV_OK) return st;
+  pkv::AppendArgs a{c_new, nullptr, c_cache, nullptr, slot_mapping, num_tokens, num_blocks, 1,
+                    rank * 2, err};
+  return pkv::launch_kv_append(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PKV_OK
+             : PKV_ECUDA;
+}
+
+size_t pkv_mla_workspace_bytes(int num_seqs, int num_q_heads, int rank, int max_seq_len) {
+  if (num_seqs < 1 || num_q_heads < 1 || rank < 1 || max_seq_len < 1) return 0;
+  const size_t vec = align256((size_t)num_seqs * num_q_heads * rank * 2);
+  return 2 * vec + pkv_decode_workspace_bytes(num_seqs, num_q_heads, rank, max_seq_len);
+}
+
+pkv_status pkv_mla_decode_attention(void* out, const void* q, const void* w_k, const void* w_v,
+                                    const void* c_cache, const int32_t* block_table,
+                                    const int32_t* seq_lens, int num_seqs, int max_blocks_per_seq,
+                                    int max_seq_len, int64_t num_blocks, int num_q_heads,
+                                    int head_dim, int rank, int block_size, float scale,
+                                    void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+  if (num_q_heads < 1 || head_dim < 1 || rank < 1 || block_size < 1) return PKV_EINVAL;
+  if (block_size != pkv::kBlockSize || num_q_heads != 32 || head_dim != 128 || rank != 128)
+    return PKV_EUNSUPPORTED;
+  if (num_seqs < 0 || max_blocks_per_seq < 1 || max_seq_len < 1 || num_blocks < 1) return PKV_EINVAL;
+  if (num_seqs == 0) return PKV_OK;
+  if (num_seqs > PKV_MAX_SEQS) return PKV_ERANGE;
+  if ((int64_t)max_seq_len > (int64_t)max_blocks_per_seq * block_size) return PKV_EINVAL;
+  if (!isfinite(scale)) return PKV_EINVAL;
+  if (!out || !q || !w_k || !w_v || !c_cache || !block_table || !seq_lens || !workspace)
+    return PKV_EINVAL;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(w_k) || !aligned16(w_v) ||
+      !aligned16(c_cache) || (reinterpret_cast<uintptr_t>(block_table) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return PKV_EINVAL;
+  if (workspace_bytes < pkv_mla_workspace_bytes(num_seqs, num_q_heads, rank, max_seq_len))
+    return PKV_ERANGE;
+  int* err = nullptr;
+  int sms = 0;
+  pkv_status st = device_state(&err, &sms);
+  if (st != PKV_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t vec = align256((size_t)num_seqs * num_q_heads * rank * 2);
+  char* ws = static_cast<char*>(workspace);
+  void* q_lat = ws;          // absorbed queries [B][Hq][rank] bf16
+  void* z = ws + vec;        // attention over the latent [B][Hq][rank] bf16
+  char* part = ws + 2 * vec;
+  // 1) q~_h = W_K[h]^T q_h
+  if (pkv::launch_gemm_heads(q_lat, q, w_k, num_seqs, num_q_heads, false, s) != cudaSuccess)
+    return PKV_ECUDA;
+  // 2) z_h = softmax(scale q~_h . C^T) C over the latent pool
+  const int splits = max_splits_for(max_seq_len);
+  const size_t rows = (size_t)num_seqs * num_q_heads * splits;
+  pkv::DecodeArgs a{};
+  a.out = z;
+  a.q = q_lat;
+  a.k_cache = c_cache;
+  a.v_cache = c_cache;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.ws_acc = reinterpret_cast<float*>(part);
+  a.ws_ml = reinterpret_cast<float*>(part + align256(rows * rank * sizeof(float)));
+  a.err = err;
+  a.num_seqs = num_seqs;
+  a.bt_stride = max_blocks_per_seq;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.max_seq_len = max_seq_len;
+  a.max_splits = splits;
+  a.split_tokens = pkv::kSplitTokens;
+  a.num_blocks = num_blocks;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = 1;
+  a.head_dim = rank;
+  a.scale = scale;
+  a.chunk_prior = -1;
+  a.is_bf16 = 1;
+  if (pkv::launch_decode_mla(a, sms, s) != cudaSuccess) return PKV_ECUDA;
+  // 3) o_h = W_V[h] z_h
+  if (pkv::launch_gemm_heads(out, z, w_v, num_seqs, num_q_heads, true, s) != cudaSuccess)
+    return PKV_ECUDA;
+  return PKV_OK;
+}
+
 pkv_status pkv_chunked_prefill_attention(void* out, const void* q, const void* k_cache,
                                          const void* v_cache, const int32_t* block_table_row,
                                          int max_blocks, int prior_len, int chunk_len,

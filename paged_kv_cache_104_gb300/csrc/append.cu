@@ -8,7 +8,8 @@
 // K and the same chunk of V, so reads of k_new/v_new are fully coalesced and
 // every destination row is written by D*size/16 adjacent threads.  The copy
 // is bit-exact.  slot < 0 is padding and is skipped; a slot beyond the pool
-// is skipped and reported in the error word.
+// is skipped and reported in the error word.  With v_new null only the first
+// pool is written (the latent cache has one pool).
 #include "common.cuh"
 #include "launch.h"
 
@@ -35,9 +36,11 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const AppendArgs a) {
     const int64_t dst = ((blk * a.num_kv_heads + h) * kBlockSize + r) * a.row_bytes + c * 16;
     const int64_t src = row * a.row_bytes + c * 16;
     const uint4 kv = __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(a.k_new) + src));
-    const uint4 vv = __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(a.v_new) + src));
     *reinterpret_cast<uint4*>(static_cast<char*>(a.k_cache) + dst) = kv;
-    *reinterpret_cast<uint4*>(static_cast<char*>(a.v_cache) + dst) = vv;
+    if (a.v_new) {   // null for a single pool (the latent cache)
+      const uint4 vv = __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(a.v_new) + src));
+      *reinterpret_cast<uint4*>(static_cast<char*>(a.v_cache) + dst) = vv;
+    }
   }
 }
 

@@ -238,3 +238,29 @@ def draw_fp8_pool(w: Workload, lay: Layout, scales: torch.Tensor, layer: int = 0
                     device=dev, dtype=torch.float32)
     x = (x / scales.to(dev)[None, :, None, None]).clamp_(-448.0, 448.0)
     return x.to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+@dataclass
+class LatentInputs:
+    q: torch.Tensor        # [B, Hq, D] bf16 (the decode queries)
+    c_new: torch.Tensor    # [B, r] bf16 (each sequence's new token's latent)
+    pool: torch.Tensor     # [NB, bs, r] bf16 latent pool before the append
+    w_k: torch.Tensor      # [Hq, D, r] bf16 key up-projections
+    w_v: torch.Tensor      # [Hq, D, r] bf16 value up-projections
+
+
+def draw_latent(w: Workload, lay: Layout, rank: int = 128, layer: int = 0,
+                device="cpu") -> LatentInputs:
+    """Seeded inputs of the latent (MLA-style) cache for the decode batch of
+    ``lay``: N(0,1) queries and latents, and up-projections with N(0, 1/r)
+    entries, so reconstructed keys and values have unit variance."""
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev).manual_seed(30_000 * (w.seed + 1) + layer)
+    b = lay.num_decode_tokens
+    q = _randn((b, w.num_q_heads, w.head_dim), torch.bfloat16, dev, gen)
+    c_new = _randn((b, rank), torch.bfloat16, dev, gen)
+    pool = _randn((lay.num_blocks, w.block_size, rank), torch.bfloat16, dev, gen)
+    s = 1.0 / math.sqrt(rank)
+    w_k = (torch.randn((w.num_q_heads, w.head_dim, rank), generator=gen, device=dev) * s).to(torch.bfloat16)
+    w_v = (torch.randn((w.num_q_heads, w.head_dim, rank), generator=gen, device=dev) * s).to(torch.bfloat16)
+    return LatentInputs(q, c_new, pool, w_k, w_v)
