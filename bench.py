@@ -373,6 +373,109 @@ def run_fp8_decode(args, w, lay, inputs, dev, stream, dist, n):
     }
 
 
+def run_mla_decode(args, w, lay, dev, stream, dist, n):
+    """Time decode over a latent (MLA-style) cache on the decode batch of the
+    workload: per layer latent_append of the decode tokens' latents, then the
+    decode call (query absorption, attention over the latents, split merge,
+    up-projection), every layer with its own pool, as one CUDA graph.
+    Algorithmic bytes: every stored latent once, the two projections, q read
+    and out written, and the append."""
+    from paged_kv_cache_104_gb300 import binding as B
+
+    L, hq, d, r = w.layers, w.num_q_heads, w.head_dim, 128
+    lw = W.Workload("latent_" + w.name, torch.bfloat16, L, hq, 1, d, w.block_size, w.num_seqs,
+                    seed=w.seed, context=w.context, context_loguniform=w.context_loguniform)
+    llay = W.make_layout(lw, prefill=(0, 0))
+    nd = llay.num_decode_tokens
+    tokens = int(llay.seq_lens.to(torch.int64).sum())
+    dec_bytes = tokens * r * 2 + 2 * hq * d * r * 2 + 2 * nd * hq * d * 2
+    app_bytes = nd * r * 2 * 2
+    pool_bytes = llay.num_blocks * w.block_size * r * 2
+    free, _ = torch.cuda.mem_get_info(dev)
+    n_pools = min(L, max(2, int((free - 8 * 2 ** 30) // max(pool_bytes, 1))))
+    if args.layer_pools > 0:
+        n_pools = min(n_pools, args.layer_pools)
+    xs = [W.draw_latent(lw, llay, r, layer=li, device=dev) for li in range(L)]
+    pools = [xs[li].pool for li in range(n_pools)]
+    for li in range(L):
+        xs[li].pool = None
+    slot = llay.slot_mapping[:nd].to(dev)
+    bt = llay.decode_block_table.to(dev).contiguous()
+    sl = llay.seq_lens.to(dev)
+    msl = int(llay.seq_lens.max())
+    wsp = B.mla_workspace(nd, hq, r, msl, device=dev)
+    outs = [torch.empty_like(xs[li].q) for li in range(L)]
+
+    def step(ev=None, s=None):
+        s = stream if s is None else s
+        for li in range(L):
+            x = xs[li]
+            c = pools[li % n_pools]
+            B.latent_append(x.c_new, c, slot, stream=s)
+            if ev is not None:
+                ev[li][0].record(s)
+            B.mla_decode_attention(outs[li], x.q, x.w_k, x.w_v, c, bt, sl, msl, lw.scale, wsp,
+                                   stream=s)
+            if ev is not None:
+                ev[li][1].record(s)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    assert B.get_device_error() == 0, "device error word set during the latent warm-up"
+    try:
+        gev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+               for _ in range(L)]
+    except TypeError:
+        gev = None
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            step(gev, s=cap)
+    stream.wait_stream(cap)
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    t0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(dist)
+    ms_step = max_over_ranks(dist, t0.elapsed_time(t1)) / args.steps
+    assert B.get_device_error() == 0, "device error word set during the latent steps"
+    if gev is None:
+        gev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(L)]
+        step(gev)
+        torch.cuda.synchronize(dev)
+    dec_ms = sum(gev[li][0].elapsed_time(gev[li][1]) for li in range(L)) / L
+    hbm_peak, _, peak_src = measured_peaks()
+    dec_gbs = dec_bytes / (dec_ms / 1e3) / 1e9
+    return {
+        "what": "decode over a latent (MLA-style) cache, rank 128, 32 query heads with per-head "
+                "up-projections: latent_append of the decode tokens + decode call (absorb, "
+                "attend over the latents, merge, up-project), all layers, one CUDA graph",
+        "ms_per_step": ms_step,
+        "value": n * L * (dec_bytes + app_bytes) / (ms_step / 1e3) / 1e9, "unit": "GB/s",
+        "decode_tokens_per_s": n * nd / (ms_step / 1e3),
+        "decode_ms_per_layer": dec_ms,
+        "distinct_layer_pools": n_pools, "pool_gb_per_layer": pool_bytes / 1e9,
+        "gpu_launches": args.steps * L * (1 + 3 + (1 if msl > 512 else 0)),
+        "roofline": {
+            "kernel": "mla_decode_attention (absorb GEMM + attention over the latent + merge + "
+                      "up-projection GEMM)", "bound": "hbm",
+            "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": dec_gbs / hbm_peak,
+            "traffic": None, "algorithmic_bytes_per_launch": dec_bytes,
+            "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+            else "fallback 6.8 TB/s",
+        },
+    }
+
+
 def run_ours(args, w, lay, acct):
     from paged_kv_cache_104_gb300 import binding as B
 
@@ -632,6 +735,11 @@ def run_ours(args, w, lay, acct):
         torch.cuda.empty_cache()
         line["fp8_decode"] = run_fp8_decode(args, w, lay, inputs, dev, stream, dist, n)
 
+    # ---- latent (MLA-style) cache variant of the decode path
+    if args.mla_decode and w.head_dim == 128 and w.num_q_heads == 32 and w.dtype == torch.bfloat16:
+        torch.cuda.empty_cache()
+        line["mla_decode"] = run_mla_decode(args, w, lay, dev, stream, dist, n)
+
     # ---- the oracle on this host's cores, bounded sample, rank 0 at N=1 only
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         pools = None
@@ -670,6 +778,9 @@ def main():
     ap.add_argument("--fp8-decode", type=int, default=1,
                     help="1: also time the decode path over an fp8 (E4M3) cache (reported "
                          "under fp8_decode, after the bf16 step)")
+    ap.add_argument("--mla-decode", type=int, default=1,
+                    help="1: also time decode over a latent (MLA-style) cache (reported under "
+                         "mla_decode)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-decode-seqs", type=int, default=128,
                     help="decode sequences in the oracle sample of cpu_baseline")
