@@ -369,7 +369,7 @@ decode_reduce_kernel(const DecodeArgs a) {
   for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(kFull, L, o);
   const float inv = 1.f / L;
   T* outp = static_cast<T*>(a.out) + (int64_t)warp_global * D;
-  if (D == 128) {
+  if constexpr (D == 128) {
     // lane = 4-column group; split weights are computed once per lane (32
     // splits at a time) and broadcast, and 8 partial rows are loaded before
     // their FMAs so the L2 latency of the walk over splits overlaps
@@ -409,8 +409,7 @@ decode_reduce_kernel(const DecodeArgs a) {
     Elem<T>::store(outp + lane * 4 + 1, o.y * inv);
     Elem<T>::store(outp + lane * 4 + 2, o.z * inv);
     Elem<T>::store(outp + lane * 4 + 3, o.w * inv);
-    return;
-  }
+  } else {
   for (int d4 = lane; d4 < D / 4; d4 += 32) {
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s = 0; s < ns; ++s) {
@@ -426,6 +425,7 @@ decode_reduce_kernel(const DecodeArgs a) {
     Elem<T>::store(outp + d4 * 4 + 1, o.y * inv);
     Elem<T>::store(outp + d4 * 4 + 2, o.z * inv);
     Elem<T>::store(outp + d4 * 4 + 3, o.w * inv);
+  }
   }
 }
 

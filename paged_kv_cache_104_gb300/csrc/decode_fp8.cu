@@ -278,7 +278,6 @@ decode_fp8_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
       uint4 kg0, kg1, kh0, kh1, va, vb, vc, vd;
       if (valid > 0) {
         const unsigned char* k8 = smem + buf * kStage8 + warp * kTile8;
-        const unsigned char* v8 = k8 + kBPS * kTile8;
         kg0 = lds128(k8 + sw8(g, 2 * t));
         kg1 = lds128(k8 + sw8(g, 2 * t + 1));
         kh0 = lds128(k8 + sw8(g + 8, 2 * t));

@@ -176,7 +176,6 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
     constexpr int kBlkPerTile = BN / kBlockSize;   // 8
     constexpr int kTilesPerWin = 32 / kBlkPerTile;  // 4
     int cur_ids = load_ids(0), next_ids = load_ids(1);
-    int issued = 0;
     for (int j = 0; j < n_tiles; ++j) {
       if (j > 0 && j % kTilesPerWin == 0) {
         cur_ids = next_ids;
@@ -209,10 +208,8 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
       cp_async_wait<0>();
       fence_proxy_async_smem();             // make them visible to the tensor core
       mbar_arrive(bar(PB_KVF + st));
-      issued = j + 1;
     }
     cp_async_wait<0>();
-    (void)issued;
   } else if (warp == W_MMA) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
