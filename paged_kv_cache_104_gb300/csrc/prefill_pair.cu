@@ -35,10 +35,18 @@
 //                     ex2 per score, sums it and stores it as bf16 into TMEM.
 //                     Epilogue O / l.
 //   warps 8-9         K/V producers (cp.async; once their copies of a tile
-//                     landed: proxy fence, mbarrier arrive).
-//   warp 10           TMEM allocator and single-thread MMA issuer:
+//                     landed: proxy fence, mbarrier arrive).  K and V sit in
+//                     separate two-stage rings: a K stage is released once
+//                     both heads' Q K^T have read it, a tile before its V
+//                     stage, so the next K tile is in flight earlier.
+//   warp 10           TMEM allocator and MMA issuer:
 //                     S_h = Q_h K_j^T    (A, B from shared memory)
 //                     O_h += P_h V_j     (A from TMEM, V as an MN-major B)
+//                     The whole warp runs the issue loop and computes the
+//                     (warp-uniform) descriptors; one elected lane issues each
+//                     tcgen05 instruction.  Issuing from a lone lane inside a
+//                     divergent branch starved the tensor core: the same
+//                     instruction stream ran about 25% slower.
 // Every mbarrier wait is bounded; on time-out the kernel records an error,
 // stops issuing work, lets its copies land, frees its TMEM and returns.
 #include <cuda.h>
@@ -56,11 +64,11 @@ constexpr int QHALF = BM * 128;               // one 64-column half of a Q tile,
 constexpr int Q_BYTES = 2 * QHALF;            // 32 KiB per head
 constexpr int KHALF = BN * 128;               // one 64-column half of a K/V tile, 16 KiB
 constexpr int KV_TILE = 2 * KHALF;            // 32 KiB
-constexpr int STAGE = 2 * KV_TILE;            // K + V of 128 keys, 64 KiB
-constexpr int NST = 2;
+constexpr int NSK = 2, NSV = 2;               // K ring and V ring, released separately
 constexpr int OFF_Q = 0;                      // [head][Q tile]
-constexpr int OFF_KV = 2 * Q_BYTES;           // [stage][K | V]
-constexpr int OFF_BAR = OFF_KV + NST * STAGE;
+constexpr int OFF_K = 2 * Q_BYTES;            // [K stage]
+constexpr int OFF_V = OFF_K + NSK * KV_TILE;  // [V stage]
+constexpr int OFF_BAR = OFF_V + NSV * KV_TILE;
 constexpr int SMEM_BYTES = OFF_BAR + 256;
 constexpr int kSoftThreads = 256;
 constexpr int kProdThreads = 64;
@@ -75,9 +83,11 @@ static_assert(SMEM_BYTES <= 227 * 1024, "one CTA per SM");
 // barrier slots
 enum {
   PB_Q = 0,
-  PB_KVF = 1,                 // [NST]
-  PB_KVE = PB_KVF + NST,      // [NST]
-  PB_SF = PB_KVE + NST,       // [head]
+  PB_KF = 1,                  // [NSK]
+  PB_KE = PB_KF + NSK,        // [NSK]
+  PB_VF = PB_KE + NSK,        // [NSV]
+  PB_VE = PB_VF + NSV,        // [NSV]
+  PB_SF = PB_VE + NSV,        // [head]
   PB_PF = PB_SF + 2,          // [head]
   PB_OD = PB_PF + 2,          // [head]
   PB_COUNT = PB_OD + 2
@@ -95,12 +105,38 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                : "memory");
 }
+__device__ __forceinline__ void cp_async16_full(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// tcgen05 issue from a converged warp: one elected lane issues, every lane
+// computes the same (uniform) descriptors
+__device__ __forceinline__ void mma_ss_e(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_ts_e(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void commit_e(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+      : "memory");
 }
 
 __global__ void __launch_bounds__(kThreadsPair, 1)
@@ -129,9 +165,13 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
 
   if (tid == 0) {
     mbar_init(bar(PB_Q), 1);
-    for (int s = 0; s < NST; ++s) {
-      mbar_init(bar(PB_KVF + s), kProdThreads);
-      mbar_init(bar(PB_KVE + s), 1);
+    for (int s = 0; s < NSK; ++s) {
+      mbar_init(bar(PB_KF + s), kProdThreads);
+      mbar_init(bar(PB_KE + s), 1);
+    }
+    for (int s = 0; s < NSV; ++s) {
+      mbar_init(bar(PB_VF + s), kProdThreads);
+      mbar_init(bar(PB_VE + s), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(PB_SF + i), 1);
@@ -157,8 +197,6 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
     const int pt = tid - kSoftThreads;          // 0..63
     const int rsub = pt >> 4, cc = pt & 15;     // row within a group of 4, 16-byte chunk
     const int half = cc >> 3, ch = cc & 7;
-    const __nv_bfloat16* kc = static_cast<const __nv_bfloat16*>(a.k_cache);
-    const __nv_bfloat16* vc = static_cast<const __nv_bfloat16*>(a.v_cache);
     const int nblk_seq = (p.total_len + kBlockSize - 1) / kBlockSize;
     // block ids of the sequence, 32 per window (one per lane), next window prefetched
     auto load_ids = [&](int win) {
@@ -176,74 +214,104 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
     constexpr int kBlkPerTile = BN / kBlockSize;   // 8
     constexpr int kTilesPerWin = 32 / kBlkPerTile;  // 4
     int cur_ids = load_ids(0), next_ids = load_ids(1);
+    // one 128-key tile of one pool: 8 blocks of 16 rows, each thread 4 rows x one 16-byte chunk
+    // per block; rows past the sequence end (last tile only) are zero-filled
+    const uint32_t thr_dst = half * KHALF + rsub * 128;
+    auto issue_tile = [&](const __nv_bfloat16* src_pool, uint32_t dst, int j) {
+      const bool full = (j + 1) * BN <= p.total_len;
+#pragma unroll 2
+      for (int bi = 0; bi < kBlkPerTile; ++bi) {
+        const int blk = __shfl_sync(0xffffffffu, cur_ids, ((j % kTilesPerWin) * kBlkPerTile + bi) & 31);
+        const __nv_bfloat16* bsrc =
+            src_pool + ((int64_t)blk * a.num_kv_heads + g) * (kBlockSize * HD) + rsub * HD + cc * 8;
+        const uint32_t bdst = dst + thr_dst + bi * kBlockSize * 128;
+        if (full) {
+#pragma unroll
+          for (int rq = 0; rq < kBlockSize / 4; ++rq)
+            cp_async16_full(bdst + rq * 512 + ((ch ^ ((rq & 1) * 4 + rsub)) << 4), bsrc + rq * 4 * HD);
+        } else {
+#pragma unroll
+          for (int rq = 0; rq < kBlockSize / 4; ++rq) {
+            const int tok = j * BN + bi * kBlockSize + rq * 4 + rsub;
+            cp_async16(bdst + rq * 512 + ((ch ^ ((rq & 1) * 4 + rsub)) << 4), bsrc + rq * 4 * HD,
+                       tok < p.total_len ? 16u : 0u);
+          }
+        }
+      }
+      cp_async_commit();
+    };
+    const __nv_bfloat16* kc = static_cast<const __nv_bfloat16*>(a.k_cache);
+    const __nv_bfloat16* vc = static_cast<const __nv_bfloat16*>(a.v_cache);
+    // Copy groups go out as K(0), V(0), K(1), V(1), ...  K(j) is signalled
+    // once V(j) has been issued behind it and V(j-1) once K(j) has, so each
+    // signal waits only for the older group.  Neither wait can close a
+    // cycle: the stage K(j) reuses is released by Q_B K(j-2)^T and the one
+    // V(j) reuses by P_B V(j-2), both issued before the products that need
+    // V(j-1) and K(j).
     for (int j = 0; j < n_tiles; ++j) {
       if (j > 0 && j % kTilesPerWin == 0) {
         cur_ids = next_ids;
         next_ids = load_ids(j / kTilesPerWin + 1);
       }
-      const int st = j % NST;
       bool go = true;
-      if (j >= NST) go = wait_or_abort(bar(PB_KVE + st), ((j / NST) - 1) & 1, abort_flag, a.err);
-      if (!__all_sync(0xffffffffu, go && !*abort_flag)) break;  // leave the loop as a warp
-      const uint32_t kdst = sbase + OFF_KV + st * STAGE, vdst = kdst + KV_TILE;
-#pragma unroll 2
-      for (int bi = 0; bi < kBlkPerTile; ++bi) {
-        const int blk = __shfl_sync(0xffffffffu, cur_ids, ((j % kTilesPerWin) * kBlkPerTile + bi) & 31);
-        const int64_t tile = ((int64_t)blk * a.num_kv_heads + g) * (kBlockSize * HD);
-#pragma unroll
-        for (int rq = 0; rq < kBlockSize / 4; ++rq) {
-          const int rr = rq * 4 + rsub;               // row within the block
-          const int row = bi * kBlockSize + rr;       // row within the 128-key tile
-          const int tok = j * BN + row;
-          const uint32_t nbytes = tok < p.total_len ? 16u : 0u;   // zero-fill past the end
-          const int64_t src = tile + rr * HD + cc * 8;
-          const uint32_t doff = half * KHALF + row * 128 + ((ch ^ (row & 7)) << 4);
-          cp_async16(kdst + doff, kc + src, nbytes);
-          cp_async16(vdst + doff, vc + src, nbytes);
-        }
+      if (j >= NSK) go = wait_or_abort(bar(PB_KE + j % NSK), ((j / NSK) - 1) & 1, abort_flag, a.err);
+      if (!__all_sync(0xffffffffu, go && !*abort_flag)) break;
+      issue_tile(kc, sbase + OFF_K + (j % NSK) * KV_TILE, j);
+      if (j > 0) {
+        cp_async_wait<1>();
+        fence_proxy_async_smem();
+        mbar_arrive(bar(PB_VF + (j - 1) % NSV));
       }
-      cp_async_commit();
-      // signal tile j as soon as this thread's copies of it landed (no lag:
-      // the MMA side may wait for tile j before releasing tile j-1's stage)
-      cp_async_wait<0>();
-      fence_proxy_async_smem();             // make them visible to the tensor core
-      mbar_arrive(bar(PB_KVF + st));
+      if (j >= NSV) go = wait_or_abort(bar(PB_VE + j % NSV), ((j / NSV) - 1) & 1, abort_flag, a.err);
+      if (!__all_sync(0xffffffffu, go && !*abort_flag)) break;
+      issue_tile(vc, sbase + OFF_V + (j % NSV) * KV_TILE, j);
+      cp_async_wait<1>();
+      fence_proxy_async_smem();
+      mbar_arrive(bar(PB_KF + j % NSK));
+      if (j == n_tiles - 1) {
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        mbar_arrive(bar(PB_VF + j % NSV));
+      }
     }
     cp_async_wait<0>();
   } else if (warp == W_MMA) {
     // ------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
-      mbar_arrive_expect_tx(bar(PB_Q), 2 * Q_BYTES);
-      for (int hh = 0; hh < 2; ++hh) {
-        tma_load_3d(sbase + OFF_Q + hh * Q_BYTES, &tm_q, bar(PB_Q), 0, h0 + hh, q0);
-        tma_load_3d(sbase + OFF_Q + hh * Q_BYTES + QHALF, &tm_q, bar(PB_Q), 64, h0 + hh, q0);
+    {
+      if (lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
+        mbar_arrive_expect_tx(bar(PB_Q), 2 * Q_BYTES);
+        for (int hh = 0; hh < 2; ++hh) {
+          tma_load_3d(sbase + OFF_Q + hh * Q_BYTES, &tm_q, bar(PB_Q), 0, h0 + hh, q0);
+          tma_load_3d(sbase + OFF_Q + hh * Q_BYTES + QHALF, &tm_q, bar(PB_Q), 64, h0 + hh, q0);
+        }
       }
+      __syncwarp();
       constexpr uint32_t idesc_qk = make_idesc(false, BM, BN);
       constexpr uint32_t idesc_pv = make_idesc(true, BM, HD);
-      bool ok = wait_or_abort(bar(PB_Q), 0, abort_flag, a.err);
+      bool ok = __all_sync(0xffffffffu, wait_or_abort(bar(PB_Q), 0, abort_flag, a.err));
       // S_h = Q_h K_j^T into the TMEM columns of S_h
       auto issue_qk = [&](int hh, int j) {
-        const uint32_t kb = sbase + OFF_KV + (j % NST) * STAGE;
+        const uint32_t kb = sbase + OFF_K + (j % NSK) * KV_TILE;
         const uint32_t qa = sbase + OFF_Q + hh * Q_BYTES;
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
           const uint64_t ad = make_sw128_desc(qa + (k >> 2) * QHALF + (k & 3) * 32, 16, 1024);
           const uint64_t bd = make_sw128_desc(kb + (k >> 2) * KHALF + (k & 3) * 32, 16, 1024);
-          mma_bf16(tmem + COL_S + hh * BN, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+          mma_ss_e(tmem + COL_S + hh * BN, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
         }
-        mma_commit(bar(PB_SF + hh));
+        commit_e(bar(PB_SF + hh));
       };
       // O_h += P_h V_j, P_h from TMEM (16 keys = 8 columns per step)
       auto issue_pv = [&](int hh, int j) {
-        const uint32_t vb = sbase + OFF_KV + (j % NST) * STAGE + KV_TILE;
+        const uint32_t vb = sbase + OFF_V + (j % NSV) * KV_TILE;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
           const uint64_t bd = make_sw128_desc(vb + k * 16 * 128, KHALF, 1024);
-          mma_bf16_tmem_a(tmem + COL_O + hh * HD, tmem + COL_S + hh * BN + k * 8, bd, idesc_pv,
-                          (j > 0 || k > 0) ? 1u : 0u);
+          mma_ts_e(tmem + COL_O + hh * HD, tmem + COL_S + hh * BN + k * 8, bd, idesc_pv,
+                   (j > 0 || k > 0) ? 1u : 0u);
         }
-        mma_commit(bar(PB_OD + hh));
+        commit_e(bar(PB_OD + hh));
       };
       // The two heads alternate on the tensor core: while head A's softmax
       // turns S_A into P_A, the products of head B run, and the other way
@@ -251,24 +319,28 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
       // P_h V_j: tcgen05.mma operations issued by one thread execute in issue
       // order, so the earlier product has read P_h before the later one
       // writes there, and no wait for its completion is needed.
-      if (ok) ok = wait_or_abort(bar(PB_KVF + 0), 0, abort_flag, a.err);
+      if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(bar(PB_KF + 0), 0, abort_flag, a.err));
       if (ok) {
         tc_fence_after();
         issue_qk(0, 0);
         issue_qk(1, 0);
+        commit_e(bar(PB_KE + 0));               // K(0) no longer needed
       }
       for (int j = 0; j < n_tiles && ok; ++j) {
         const bool more = j + 1 < n_tiles;
         for (int hh = 0; hh < 2 && ok; ++hh) {
-          ok = wait_or_abort(bar(PB_PF + hh), j & 1, abort_flag, a.err);
+          ok = __all_sync(0xffffffffu, wait_or_abort(bar(PB_PF + hh), j & 1, abort_flag, a.err));
           if (!ok) break;
           tc_fence_after();
+          if (hh == 0) ok = __all_sync(0xffffffffu, wait_or_abort(bar(PB_VF + j % NSV), (j / NSV) & 1, abort_flag, a.err));
+          if (!ok) break;
           issue_pv(hh, j);
-          if (hh == 1) mma_commit(bar(PB_KVE + j % NST));   // tile j no longer needed
+          if (hh == 1) commit_e(bar(PB_VE + j % NSV));   // V(j) no longer needed
           if (more) {
-            if (hh == 0) ok = wait_or_abort(bar(PB_KVF + (j + 1) % NST), ((j + 1) / NST) & 1, abort_flag, a.err);
+            if (hh == 0) ok = __all_sync(0xffffffffu, wait_or_abort(bar(PB_KF + (j + 1) % NSK), ((j + 1) / NSK) & 1, abort_flag, a.err));
             if (!ok) break;
             issue_qk(hh, j + 1);
+            if (hh == 1) commit_e(bar(PB_KE + (j + 1) % NSK));   // K(j+1) no longer needed
           }
         }
       }
