@@ -25,7 +25,7 @@
 //    (128 columns) for the two heads = all 512 columns; one CTA per SM.  The
 //    two heads take turns on the tensor core: while one head's softmax runs,
 //    the other head's products execute.
-// Roles (352 threads):
+// Roles (384 threads):
 //   warps 0-3 / 4-7   softmax of head A / B: thread r owns query row r (TMEM
 //                     lane r).  It loads its whole S row into registers (four
 //                     TMEM loads in flight), takes the row max (causal mask on
@@ -39,6 +39,8 @@
 //                     separate two-stage rings: a K stage is released once
 //                     both heads' Q K^T have read it, a tile before its V
 //                     stage, so the next K tile is in flight earlier.
+//   warp 11           idle: completes warpgroup 2, which gives registers to
+//                     the softmax warpgroups (setmaxnreg).
 //   warp 10           TMEM allocator and MMA issuer:
 //                     S_h = Q_h K_j^T    (A, B from shared memory)
 //                     O_h += P_h V_j     (A from TMEM, V as an MN-major B)
@@ -73,7 +75,13 @@ constexpr int SMEM_BYTES = OFF_BAR + 256;
 constexpr int kSoftThreads = 256;
 constexpr int kProdThreads = 64;
 constexpr int W_PROD = 8, W_MMA = 10;
-constexpr int kThreadsPair = kSoftThreads + kProdThreads + 32;
+constexpr int kThreadsPair = kSoftThreads + kProdThreads + 64;   // + an idle warp completing warpgroup 2
+// registers per thread after the split (setmaxnreg), against the launch budget
+constexpr int kRegsSoft = 200, kRegsRest = 96;
+constexpr int kRegsLaunch = (65536 / kThreadsPair) & ~7;   // 168
+static_assert(kRegsSoft * kSoftThreads + kRegsRest * (kThreadsPair - kSoftThreads) <=
+                  kRegsLaunch * kThreadsPair,
+              "the register split must fit in what the CTA was launched with");
 constexpr uint32_t kTmemColsPair = 512;
 constexpr uint32_t COL_S = 0;                 // S_h at 128*h (P_h in its first 64 columns)
 constexpr uint32_t COL_O = 2 * BN;            // O_h at 256 + 128*h
@@ -139,6 +147,13 @@ __device__ __forceinline__ void commit_e(uint32_t bar) {
       : "memory");
 }
 
+// three-input maximum (one instruction on sm_100 and later)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 __global__ void __launch_bounds__(kThreadsPair, 1)
 prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant__ CUtensorMap tm_q) {
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -192,161 +207,169 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp >= W_PROD && warp < W_MMA) {
-    // ------------------------------------------------------------- K/V producers
-    const int pt = tid - kSoftThreads;          // 0..63
-    const int rsub = pt >> 4, cc = pt & 15;     // row within a group of 4, 16-byte chunk
-    const int half = cc >> 3, ch = cc & 7;
-    const int nblk_seq = (p.total_len + kBlockSize - 1) / kBlockSize;
-    // block ids of the sequence, 32 per window (one per lane), next window prefetched
-    auto load_ids = [&](int win) {
-      const int idx = win * 32 + lane;
-      int blk = 0;
-      if (idx < nblk_seq) {
-        blk = __ldg(a.block_table_row + idx);
-        if (blk < 0 || (int64_t)blk >= a.num_blocks) {
-          record_error(a.err, DEVERR_BLOCK_RANGE);
-          blk = 0;
-        }
-      }
-      return blk;
-    };
-    constexpr int kBlkPerTile = BN / kBlockSize;   // 8
-    constexpr int kTilesPerWin = 32 / kBlkPerTile;  // 4
-    int cur_ids = load_ids(0), next_ids = load_ids(1);
-    // one 128-key tile of one pool: 8 blocks of 16 rows, each thread 4 rows x one 16-byte chunk
-    // per block; rows past the sequence end (last tile only) are zero-filled
-    const uint32_t thr_dst = half * KHALF + rsub * 128;
-    auto issue_tile = [&](const __nv_bfloat16* src_pool, uint32_t dst, int j) {
-      const bool full = (j + 1) * BN <= p.total_len;
-#pragma unroll 2
-      for (int bi = 0; bi < kBlkPerTile; ++bi) {
-        const int blk = __shfl_sync(0xffffffffu, cur_ids, ((j % kTilesPerWin) * kBlkPerTile + bi) & 31);
-        const __nv_bfloat16* bsrc =
-            src_pool + ((int64_t)blk * a.num_kv_heads + g) * (kBlockSize * HD) + rsub * HD + cc * 8;
-        const uint32_t bdst = dst + thr_dst + bi * kBlockSize * 128;
-        if (full) {
-#pragma unroll
-          for (int rq = 0; rq < kBlockSize / 4; ++rq)
-            cp_async16_full(bdst + rq * 512 + ((ch ^ ((rq & 1) * 4 + rsub)) << 4), bsrc + rq * 4 * HD);
-        } else {
-#pragma unroll
-          for (int rq = 0; rq < kBlockSize / 4; ++rq) {
-            const int tok = j * BN + bi * kBlockSize + rq * 4 + rsub;
-            cp_async16(bdst + rq * 512 + ((ch ^ ((rq & 1) * 4 + rsub)) << 4), bsrc + rq * 4 * HD,
-                       tok < p.total_len ? 16u : 0u);
+  if (warp >= 8) {
+    // Warpgroup 2 (producers, MMA issuer and an idle warp) hands registers to
+    // the two softmax warpgroups (kRegsRest / kRegsSoft).  With the 168 of
+    // the launch the softmax spilled; with 200 its whole S row, the running
+    // sums and the packed P fit.
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsRest));
+    if (warp >= W_PROD && warp < W_MMA) {
+      // ------------------------------------------------------------- K/V producers
+      const int pt = tid - kSoftThreads;          // 0..63
+      const int rsub = pt >> 4, cc = pt & 15;     // row within a group of 4, 16-byte chunk
+      const int half = cc >> 3, ch = cc & 7;
+      const int nblk_seq = (p.total_len + kBlockSize - 1) / kBlockSize;
+      // block ids of the sequence, 32 per window (one per lane), next window prefetched
+      auto load_ids = [&](int win) {
+        const int idx = win * 32 + lane;
+        int blk = 0;
+        if (idx < nblk_seq) {
+          blk = __ldg(a.block_table_row + idx);
+          if (blk < 0 || (int64_t)blk >= a.num_blocks) {
+            record_error(a.err, DEVERR_BLOCK_RANGE);
+            blk = 0;
           }
         }
-      }
-      cp_async_commit();
-    };
-    const __nv_bfloat16* kc = static_cast<const __nv_bfloat16*>(a.k_cache);
-    const __nv_bfloat16* vc = static_cast<const __nv_bfloat16*>(a.v_cache);
-    // Copy groups go out as K(0), V(0), K(1), V(1), ...  K(j) is signalled
-    // once V(j) has been issued behind it and V(j-1) once K(j) has, so each
-    // signal waits only for the older group.  Neither wait can close a
-    // cycle: the stage K(j) reuses is released by Q_B K(j-2)^T and the one
-    // V(j) reuses by P_B V(j-2), both issued before the products that need
-    // V(j-1) and K(j).
-    for (int j = 0; j < n_tiles; ++j) {
-      if (j > 0 && j % kTilesPerWin == 0) {
-        cur_ids = next_ids;
-        next_ids = load_ids(j / kTilesPerWin + 1);
-      }
-      bool go = true;
-      if (j >= NSK) go = wait_or_abort(bar(PB_KE + j % NSK), ((j / NSK) - 1) & 1, abort_flag, a.err);
-      if (!__all_sync(0xffffffffu, go && !*abort_flag)) break;
-      issue_tile(kc, sbase + OFF_K + (j % NSK) * KV_TILE, j);
-      if (j > 0) {
+        return blk;
+      };
+      constexpr int kBlkPerTile = BN / kBlockSize;   // 8
+      constexpr int kTilesPerWin = 32 / kBlkPerTile;  // 4
+      int cur_ids = load_ids(0), next_ids = load_ids(1);
+      // one 128-key tile of one pool: 8 blocks of 16 rows, each thread 4 rows x one 16-byte chunk
+      // per block; rows past the sequence end (last tile only) are zero-filled
+      const uint32_t thr_dst = half * KHALF + rsub * 128;
+      auto issue_tile = [&](const __nv_bfloat16* src_pool, uint32_t dst, int j) {
+        const bool full = (j + 1) * BN <= p.total_len;
+  #pragma unroll 2
+        for (int bi = 0; bi < kBlkPerTile; ++bi) {
+          const int blk = __shfl_sync(0xffffffffu, cur_ids, ((j % kTilesPerWin) * kBlkPerTile + bi) & 31);
+          const __nv_bfloat16* bsrc =
+              src_pool + ((int64_t)blk * a.num_kv_heads + g) * (kBlockSize * HD) + rsub * HD + cc * 8;
+          const uint32_t bdst = dst + thr_dst + bi * kBlockSize * 128;
+          if (full) {
+  #pragma unroll
+            for (int rq = 0; rq < kBlockSize / 4; ++rq)
+              cp_async16_full(bdst + rq * 512 + ((ch ^ ((rq & 1) * 4 + rsub)) << 4), bsrc + rq * 4 * HD);
+          } else {
+  #pragma unroll
+            for (int rq = 0; rq < kBlockSize / 4; ++rq) {
+              const int tok = j * BN + bi * kBlockSize + rq * 4 + rsub;
+              cp_async16(bdst + rq * 512 + ((ch ^ ((rq & 1) * 4 + rsub)) << 4), bsrc + rq * 4 * HD,
+                         tok < p.total_len ? 16u : 0u);
+            }
+          }
+        }
+        cp_async_commit();
+      };
+      const __nv_bfloat16* kc = static_cast<const __nv_bfloat16*>(a.k_cache);
+      const __nv_bfloat16* vc = static_cast<const __nv_bfloat16*>(a.v_cache);
+      // Copy groups go out as K(0), V(0), K(1), V(1), ...  K(j) is signalled
+      // once V(j) has been issued behind it and V(j-1) once K(j) has, so each
+      // signal waits only for the older group.  Neither wait can close a
+      // cycle: the stage K(j) reuses is released by Q_B K(j-2)^T and the one
+      // V(j) reuses by P_B V(j-2), both issued before the products that need
+      // V(j-1) and K(j).
+      for (int j = 0; j < n_tiles; ++j) {
+        if (j > 0 && j % kTilesPerWin == 0) {
+          cur_ids = next_ids;
+          next_ids = load_ids(j / kTilesPerWin + 1);
+        }
+        bool go = true;
+        if (j >= NSK) go = wait_or_abort(bar(PB_KE + j % NSK), ((j / NSK) - 1) & 1, abort_flag, a.err);
+        if (!__all_sync(0xffffffffu, go && !*abort_flag)) break;
+        issue_tile(kc, sbase + OFF_K + (j % NSK) * KV_TILE, j);
+        if (j > 0) {
+          cp_async_wait<1>();
+          fence_proxy_async_smem();
+          mbar_arrive(bar(PB_VF + (j - 1) % NSV));
+        }
+        if (j >= NSV) go = wait_or_abort(bar(PB_VE + j % NSV), ((j / NSV) - 1) & 1, abort_flag, a.err);
+        if (!__all_sync(0xffffffffu, go && !*abort_flag)) break;
+        issue_tile(vc, sbase + OFF_V + (j % NSV) * KV_TILE, j);
         cp_async_wait<1>();
         fence_proxy_async_smem();
-        mbar_arrive(bar(PB_VF + (j - 1) % NSV));
-      }
-      if (j >= NSV) go = wait_or_abort(bar(PB_VE + j % NSV), ((j / NSV) - 1) & 1, abort_flag, a.err);
-      if (!__all_sync(0xffffffffu, go && !*abort_flag)) break;
-      issue_tile(vc, sbase + OFF_V + (j % NSV) * KV_TILE, j);
-      cp_async_wait<1>();
-      fence_proxy_async_smem();
-      mbar_arrive(bar(PB_KF + j % NSK));
-      if (j == n_tiles - 1) {
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
-        mbar_arrive(bar(PB_VF + j % NSV));
-      }
-    }
-    cp_async_wait<0>();
-  } else if (warp == W_MMA) {
-    // ------------------------------------------------------------- MMA issuer
-    {
-      if (lane == 0) {
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
-        mbar_arrive_expect_tx(bar(PB_Q), 2 * Q_BYTES);
-        for (int hh = 0; hh < 2; ++hh) {
-          tma_load_3d(sbase + OFF_Q + hh * Q_BYTES, &tm_q, bar(PB_Q), 0, h0 + hh, q0);
-          tma_load_3d(sbase + OFF_Q + hh * Q_BYTES + QHALF, &tm_q, bar(PB_Q), 64, h0 + hh, q0);
+        mbar_arrive(bar(PB_KF + j % NSK));
+        if (j == n_tiles - 1) {
+          cp_async_wait<0>();
+          fence_proxy_async_smem();
+          mbar_arrive(bar(PB_VF + j % NSV));
         }
       }
-      __syncwarp();
-      constexpr uint32_t idesc_qk = make_idesc(false, BM, BN);
-      constexpr uint32_t idesc_pv = make_idesc(true, BM, HD);
-      bool ok = __all_sync(0xffffffffu, wait_or_abort(bar(PB_Q), 0, abort_flag, a.err));
-      // S_h = Q_h K_j^T into the TMEM columns of S_h
-      auto issue_qk = [&](int hh, int j) {
-        const uint32_t kb = sbase + OFF_K + (j % NSK) * KV_TILE;
-        const uint32_t qa = sbase + OFF_Q + hh * Q_BYTES;
-#pragma unroll
-        for (int k = 0; k < HD / 16; ++k) {
-          const uint64_t ad = make_sw128_desc(qa + (k >> 2) * QHALF + (k & 3) * 32, 16, 1024);
-          const uint64_t bd = make_sw128_desc(kb + (k >> 2) * KHALF + (k & 3) * 32, 16, 1024);
-          mma_ss_e(tmem + COL_S + hh * BN, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
-        }
-        commit_e(bar(PB_SF + hh));
-      };
-      // O_h += P_h V_j, P_h from TMEM (16 keys = 8 columns per step)
-      auto issue_pv = [&](int hh, int j) {
-        const uint32_t vb = sbase + OFF_V + (j % NSV) * KV_TILE;
-#pragma unroll
-        for (int k = 0; k < BN / 16; ++k) {
-          const uint64_t bd = make_sw128_desc(vb + k * 16 * 128, KHALF, 1024);
-          mma_ts_e(tmem + COL_O + hh * HD, tmem + COL_S + hh * BN + k * 8, bd, idesc_pv,
-                   (j > 0 || k > 0) ? 1u : 0u);
-        }
-        commit_e(bar(PB_OD + hh));
-      };
-      // The two heads alternate on the tensor core: while head A's softmax
-      // turns S_A into P_A, the products of head B run, and the other way
-      // round.  Q_h K_{j+1}^T rewrites S_h, which holds P_h, right behind
-      // P_h V_j: tcgen05.mma operations issued by one thread execute in issue
-      // order, so the earlier product has read P_h before the later one
-      // writes there, and no wait for its completion is needed.
-      if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(bar(PB_KF + 0), 0, abort_flag, a.err));
-      if (ok) {
-        tc_fence_after();
-        issue_qk(0, 0);
-        issue_qk(1, 0);
-        commit_e(bar(PB_KE + 0));               // K(0) no longer needed
-      }
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const bool more = j + 1 < n_tiles;
-        for (int hh = 0; hh < 2 && ok; ++hh) {
-          ok = __all_sync(0xffffffffu, wait_or_abort(bar(PB_PF + hh), j & 1, abort_flag, a.err));
-          if (!ok) break;
-          tc_fence_after();
-          if (hh == 0) ok = __all_sync(0xffffffffu, wait_or_abort(bar(PB_VF + j % NSV), (j / NSV) & 1, abort_flag, a.err));
-          if (!ok) break;
-          issue_pv(hh, j);
-          if (hh == 1) commit_e(bar(PB_VE + j % NSV));   // V(j) no longer needed
-          if (more) {
-            if (hh == 0) ok = __all_sync(0xffffffffu, wait_or_abort(bar(PB_KF + (j + 1) % NSK), ((j + 1) / NSK) & 1, abort_flag, a.err));
-            if (!ok) break;
-            issue_qk(hh, j + 1);
-            if (hh == 1) commit_e(bar(PB_KE + (j + 1) % NSK));   // K(j+1) no longer needed
+      cp_async_wait<0>();
+    } else if (warp == W_MMA) {
+      // ------------------------------------------------------------- MMA issuer
+      {
+        if (lane == 0) {
+          asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
+          mbar_arrive_expect_tx(bar(PB_Q), 2 * Q_BYTES);
+          for (int hh = 0; hh < 2; ++hh) {
+            tma_load_3d(sbase + OFF_Q + hh * Q_BYTES, &tm_q, bar(PB_Q), 0, h0 + hh, q0);
+            tma_load_3d(sbase + OFF_Q + hh * Q_BYTES + QHALF, &tm_q, bar(PB_Q), 64, h0 + hh, q0);
           }
         }
+        __syncwarp();
+        constexpr uint32_t idesc_qk = make_idesc(false, BM, BN);
+        constexpr uint32_t idesc_pv = make_idesc(true, BM, HD);
+        bool ok = __all_sync(0xffffffffu, wait_or_abort(bar(PB_Q), 0, abort_flag, a.err));
+        // S_h = Q_h K_j^T into the TMEM columns of S_h
+        auto issue_qk = [&](int hh, int j) {
+          const uint32_t kb = sbase + OFF_K + (j % NSK) * KV_TILE;
+          const uint32_t qa = sbase + OFF_Q + hh * Q_BYTES;
+  #pragma unroll
+          for (int k = 0; k < HD / 16; ++k) {
+            const uint64_t ad = make_sw128_desc(qa + (k >> 2) * QHALF + (k & 3) * 32, 16, 1024);
+            const uint64_t bd = make_sw128_desc(kb + (k >> 2) * KHALF + (k & 3) * 32, 16, 1024);
+            mma_ss_e(tmem + COL_S + hh * BN, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+          }
+          commit_e(bar(PB_SF + hh));
+        };
+        // O_h += P_h V_j, P_h from TMEM (16 keys = 8 columns per step)
+        auto issue_pv = [&](int hh, int j) {
+          const uint32_t vb = sbase + OFF_V + (j % NSV) * KV_TILE;
+  #pragma unroll
+          for (int k = 0; k < BN / 16; ++k) {
+            const uint64_t bd = make_sw128_desc(vb + k * 16 * 128, KHALF, 1024);
+            mma_ts_e(tmem + COL_O + hh * HD, tmem + COL_S + hh * BN + k * 8, bd, idesc_pv,
+                     (j > 0 || k > 0) ? 1u : 0u);
+          }
+          commit_e(bar(PB_OD + hh));
+        };
+        // The two heads alternate on the tensor core: while head A's softmax
+        // turns S_A into P_A, the products of head B run, and the other way
+        // round.  Q_h K_{j+1}^T rewrites S_h, which holds P_h, right behind
+        // P_h V_j: tcgen05.mma operations issued by one thread execute in issue
+        // order, so the earlier product has read P_h before the later one
+        // writes there, and no wait for its completion is needed.
+        if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(bar(PB_KF + 0), 0, abort_flag, a.err));
+        if (ok) {
+          tc_fence_after();
+          issue_qk(0, 0);
+          issue_qk(1, 0);
+          commit_e(bar(PB_KE + 0));               // K(0) no longer needed
+        }
+        for (int j = 0; j < n_tiles && ok; ++j) {
+          const bool more = j + 1 < n_tiles;
+          for (int hh = 0; hh < 2 && ok; ++hh) {
+            ok = __all_sync(0xffffffffu, wait_or_abort(bar(PB_PF + hh), j & 1, abort_flag, a.err));
+            if (!ok) break;
+            tc_fence_after();
+            if (hh == 0) ok = __all_sync(0xffffffffu, wait_or_abort(bar(PB_VF + j % NSV), (j / NSV) & 1, abort_flag, a.err));
+            if (!ok) break;
+            issue_pv(hh, j);
+            if (hh == 1) commit_e(bar(PB_VE + j % NSV));   // V(j) no longer needed
+            if (more) {
+              if (hh == 0) ok = __all_sync(0xffffffffu, wait_or_abort(bar(PB_KF + (j + 1) % NSK), ((j + 1) / NSK) & 1, abort_flag, a.err));
+              if (!ok) break;
+              issue_qk(hh, j + 1);
+              if (hh == 1) commit_e(bar(PB_KE + (j + 1) % NSK));   // K(j+1) no longer needed
+            }
+          }
+        }
+        if (*abort_flag) mbar_wait(bar(PB_Q), 0, nullptr);  // let the Q loads land
       }
-      if (*abort_flag) mbar_wait(bar(PB_Q), 0, nullptr);  // let the Q loads land
     }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoft));
     // ------------------------------------------------------------- softmax (head hh)
     const int hh = warp >> 2;               // 0: warps 0-3, 1: warps 4-7
     const int r = tid & 127;                // query row in the tile, TMEM lane
@@ -379,11 +402,11 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c)
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          mx4[0] = fmaxf(mx4[0], t[c][i]);
-          mx4[1] = fmaxf(mx4[1], t[c][i + 1]);
-          mx4[2] = fmaxf(mx4[2], t[c][i + 2]);
-          mx4[3] = fmaxf(mx4[3], t[c][i + 3]);
+        for (int i = 0; i < 32; i += 8) {
+          mx4[0] = fmax3(mx4[0], t[c][i], t[c][i + 4]);
+          mx4[1] = fmax3(mx4[1], t[c][i + 1], t[c][i + 5]);
+          mx4[2] = fmax3(mx4[2], t[c][i + 2], t[c][i + 6]);
+          mx4[3] = fmax3(mx4[3], t[c][i + 3], t[c][i + 7]);
         }
       const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
       float m_new = m_run;
@@ -409,7 +432,8 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
       }
       // p = 2^(s*scale*log2e - m), written as bf16 pairs over the first 64
       // columns of S
-      float2 sum2 = make_float2(0.f, 0.f);
+      float2 sum2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                        make_float2(0.f, 0.f)};
       const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-m_new, -m_new);
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) {
@@ -418,12 +442,13 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
         for (int i = 0; i < 32; i += 2) {
           const float2 x = ffma2(make_float2(t[c][i], t[c][i + 1]), sl2x2, negm);
           const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-          sum2 = fadd2(sum2, pp);
+          sum2[(i >> 1) & 3] = fadd2(sum2[(i >> 1) & 3], pp);
           pk[i / 2] = pack_bf16(pp.x, pp.y);
         }
         tmem_st16(lane_base + col_s + c * 16, pk);
       }
-      const float sum0 = sum2.x, sum1 = sum2.y;
+      const float2 s01 = fadd2(sum2[0], sum2[1]), s23 = fadd2(sum2[2], sum2[3]);
+      const float sum0 = s01.x + s23.x, sum1 = s01.y + s23.y;
       tmem_wait_st();
       l_run = l_run * alpha + (sum0 + sum1);
       m_run = m_new;
