@@ -32,15 +32,17 @@
 //                     the diagonal tiles); the max is raised lazily, only when
 //                     it grows by more than 2^8, and then O is rescaled in
 //                     TMEM.  It forms p = 2^(s*scale*log2e - m) with one FMA and
-//                     ex2 per score, sums it and stores it as bf16 into TMEM.
+//                     ex2 per score, sums it and stores it as bf16 into TMEM;
+//                     one arrival per warp hands P to the MMA issuer.  Once a
+//                     tile's S_B is complete, the head-B warps release its K
+//                     stage (the S_B commit follows both heads' Q K^T).
 //                     Epilogue O / l.
-//   warps 8-9         K/V producers (cp.async; once their copies of a tile
-//                     landed: proxy fence, mbarrier arrive).  K and V sit in
-//                     separate two-stage rings: a K stage is released once
-//                     both heads' Q K^T have read it, a tile before its V
-//                     stage, so the next K tile is in flight earlier.
-//   warp 11           idle: completes warpgroup 2, which gives registers to
-//                     the softmax warpgroups (setmaxnreg).
+//   warps 8-9 / 11    K producers / V producer (cp.async; once their copies of
+//                     a tile landed: proxy fence, mbarrier arrive).  K and V
+//                     sit in separate two-stage rings with their own
+//                     producers: a K stage is released once both heads' Q K^T
+//                     have read it, a tile before its V stage, so the next K
+//                     tile is in flight earlier.
 //   warp 10           TMEM allocator and MMA issuer:
 //                     S_h = Q_h K_j^T    (A, B from shared memory)
 //                     O_h += P_h V_j     (A from TMEM, V as an MN-major B)
@@ -52,6 +54,8 @@
 // Every mbarrier wait is bounded; on time-out the kernel records an error,
 // stops issuing work, lets its copies land, frees its TMEM and returns.
 #include <cuda.h>
+
+#include <type_traits>
 
 #include "common.cuh"
 #include "launch.h"
@@ -74,8 +78,8 @@ constexpr int OFF_BAR = OFF_V + NSV * KV_TILE;
 constexpr int SMEM_BYTES = OFF_BAR + 256;
 constexpr int kSoftThreads = 256;
 constexpr int kProdThreads = 64;
-constexpr int W_PROD = 8, W_MMA = 10;
-constexpr int kThreadsPair = kSoftThreads + kProdThreads + 64;   // + an idle warp completing warpgroup 2
+constexpr int W_MMA = 10, W_VPROD = 11;     // K producers: warps 8-9
+constexpr int kThreadsPair = kSoftThreads + kProdThreads + 64;   // + MMA issuer + V producer
 // registers per thread after the split (setmaxnreg), against the launch budget
 constexpr int kRegsSoft = 200, kRegsRest = 96;
 constexpr int kRegsLaunch = (65536 / kThreadsPair) & ~7;   // 168
@@ -154,6 +158,13 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
+// wait with a fast path: a phase that is already complete costs one
+// try_wait; otherwise the bounded, abort-aware wait
+__device__ __forceinline__ bool wait_fast(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_or_abort(bar, parity, abort_flag, err);
+}
+
 __global__ void __launch_bounds__(kThreadsPair, 1)
 prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant__ CUtensorMap tm_q) {
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -182,15 +193,15 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
     mbar_init(bar(PB_Q), 1);
     for (int s = 0; s < NSK; ++s) {
       mbar_init(bar(PB_KF + s), kProdThreads);
-      mbar_init(bar(PB_KE + s), 1);
+      mbar_init(bar(PB_KE + s), 4);              // one arrival per head-B softmax warp
     }
     for (int s = 0; s < NSV; ++s) {
-      mbar_init(bar(PB_VF + s), kProdThreads);
+      mbar_init(bar(PB_VF + s), 32);
       mbar_init(bar(PB_VE + s), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(PB_SF + i), 1);
-      mbar_init(bar(PB_PF + i), 128);
+      mbar_init(bar(PB_PF + i), 4);              // one arrival per softmax warp
       mbar_init(bar(PB_OD + i), 1);
     }
     *abort_i = 0;
@@ -208,16 +219,15 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
   const uint32_t tmem = *tmem_slot;
 
   if (warp >= 8) {
-    // Warpgroup 2 (producers, MMA issuer and an idle warp) hands registers to
+    // Warpgroup 2 (producers and MMA issuer) hands registers to
     // the two softmax warpgroups (kRegsRest / kRegsSoft).  With the 168 of
     // the launch the softmax spilled; with 200 its whole S row, the running
     // sums and the packed P fit.
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsRest));
-    if (warp >= W_PROD && warp < W_MMA) {
+    if (warp != W_MMA) {
       // ------------------------------------------------------------- K/V producers
-      const int pt = tid - kSoftThreads;          // 0..63
-      const int rsub = pt >> 4, cc = pt & 15;     // row within a group of 4, 16-byte chunk
-      const int half = cc >> 3, ch = cc & 7;
+      // warps 8-9 gather K, warp 11 gathers V, each pool on its own ring
+      const bool is_v = warp == W_VPROD;
       const int nblk_seq = (p.total_len + kBlockSize - 1) / kBlockSize;
       // block ids of the sequence, 32 per window (one per lane), next window prefetched
       auto load_ids = [&](int win) {
@@ -234,68 +244,60 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
       };
       constexpr int kBlkPerTile = BN / kBlockSize;   // 8
       constexpr int kTilesPerWin = 32 / kBlkPerTile;  // 4
-      int cur_ids = load_ids(0), next_ids = load_ids(1);
-      // one 128-key tile of one pool: 8 blocks of 16 rows, each thread 4 rows x one 16-byte chunk
-      // per block; rows past the sequence end (last tile only) are zero-filled
-      const uint32_t thr_dst = half * KHALF + rsub * 128;
-      auto issue_tile = [&](const __nv_bfloat16* src_pool, uint32_t dst, int j) {
-        const bool full = (j + 1) * BN <= p.total_len;
-  #pragma unroll 2
-        for (int bi = 0; bi < kBlkPerTile; ++bi) {
-          const int blk = __shfl_sync(0xffffffffu, cur_ids, ((j % kTilesPerWin) * kBlkPerTile + bi) & 31);
-          const __nv_bfloat16* bsrc =
-              src_pool + ((int64_t)blk * a.num_kv_heads + g) * (kBlockSize * HD) + rsub * HD + cc * 8;
-          const uint32_t bdst = dst + thr_dst + bi * kBlockSize * 128;
-          if (full) {
-  #pragma unroll
-            for (int rq = 0; rq < kBlockSize / 4; ++rq)
-              cp_async16_full(bdst + rq * 512 + ((ch ^ ((rq & 1) * 4 + rsub)) << 4), bsrc + rq * 4 * HD);
-          } else {
-  #pragma unroll
-            for (int rq = 0; rq < kBlockSize / 4; ++rq) {
-              const int tok = j * BN + bi * kBlockSize + rq * 4 + rsub;
-              cp_async16(bdst + rq * 512 + ((ch ^ ((rq & 1) * 4 + rsub)) << 4), bsrc + rq * 4 * HD,
-                         tok < p.total_len ? 16u : 0u);
+      // NT threads copy a 128-key tile: 8 blocks of 16 rows; per block each
+      // thread takes NT/16-row steps of one 16-byte chunk.  Rows past the
+      // sequence end (last tile only) are zero-filled.
+      auto produce = [&](auto nt_tag, const __nv_bfloat16* pool, uint32_t ring, int nst, int full_bar,
+                         int empty_bar, int pt) {
+        constexpr int NT = decltype(nt_tag)::value;
+        constexpr int RS = NT / 16;                  // rows per step
+        const int rsub = pt >> 4, cc = pt & 15;
+        const int half = cc >> 3, ch = cc & 7;
+        const uint32_t thr_dst = half * KHALF + rsub * 128;
+        int cur_ids = load_ids(0), next_ids = load_ids(1);
+        for (int j = 0; j < n_tiles; ++j) {
+          if (j > 0 && j % kTilesPerWin == 0) {
+            cur_ids = next_ids;
+            next_ids = load_ids(j / kTilesPerWin + 1);
+          }
+          bool go = true;
+          if (j >= nst) go = wait_or_abort(bar(empty_bar + j % nst), ((j / nst) - 1) & 1, abort_flag, a.err);
+          if (!__all_sync(0xffffffffu, go && !*abort_flag)) break;  // leave the loop as a warp
+          const uint32_t dst = ring + (j % nst) * KV_TILE;
+          const bool full = (j + 1) * BN <= p.total_len;
+#pragma unroll 2
+          for (int bi = 0; bi < kBlkPerTile; ++bi) {
+            const int blk = __shfl_sync(0xffffffffu, cur_ids, ((j % kTilesPerWin) * kBlkPerTile + bi) & 31);
+            const __nv_bfloat16* bsrc =
+                pool + ((int64_t)blk * a.num_kv_heads + g) * (kBlockSize * HD) + rsub * HD + cc * 8;
+            const uint32_t bdst = dst + thr_dst + bi * kBlockSize * 128;
+            if (full) {
+#pragma unroll
+              for (int rq = 0; rq < kBlockSize / RS; ++rq)
+                cp_async16_full(bdst + rq * RS * 128 + ((ch ^ ((rq * RS + rsub) & 7)) << 4),
+                                bsrc + rq * RS * HD);
+            } else {
+#pragma unroll
+              for (int rq = 0; rq < kBlockSize / RS; ++rq) {
+                const int tok = j * BN + bi * kBlockSize + rq * RS + rsub;
+                cp_async16(bdst + rq * RS * 128 + ((ch ^ ((rq * RS + rsub) & 7)) << 4), bsrc + rq * RS * HD,
+                           tok < p.total_len ? 16u : 0u);
+              }
             }
           }
-        }
-        cp_async_commit();
-      };
-      const __nv_bfloat16* kc = static_cast<const __nv_bfloat16*>(a.k_cache);
-      const __nv_bfloat16* vc = static_cast<const __nv_bfloat16*>(a.v_cache);
-      // Copy groups go out as K(0), V(0), K(1), V(1), ...  K(j) is signalled
-      // once V(j) has been issued behind it and V(j-1) once K(j) has, so each
-      // signal waits only for the older group.  Neither wait can close a
-      // cycle: the stage K(j) reuses is released by Q_B K(j-2)^T and the one
-      // V(j) reuses by P_B V(j-2), both issued before the products that need
-      // V(j-1) and K(j).
-      for (int j = 0; j < n_tiles; ++j) {
-        if (j > 0 && j % kTilesPerWin == 0) {
-          cur_ids = next_ids;
-          next_ids = load_ids(j / kTilesPerWin + 1);
-        }
-        bool go = true;
-        if (j >= NSK) go = wait_or_abort(bar(PB_KE + j % NSK), ((j / NSK) - 1) & 1, abort_flag, a.err);
-        if (!__all_sync(0xffffffffu, go && !*abort_flag)) break;
-        issue_tile(kc, sbase + OFF_K + (j % NSK) * KV_TILE, j);
-        if (j > 0) {
-          cp_async_wait<1>();
-          fence_proxy_async_smem();
-          mbar_arrive(bar(PB_VF + (j - 1) % NSV));
-        }
-        if (j >= NSV) go = wait_or_abort(bar(PB_VE + j % NSV), ((j / NSV) - 1) & 1, abort_flag, a.err);
-        if (!__all_sync(0xffffffffu, go && !*abort_flag)) break;
-        issue_tile(vc, sbase + OFF_V + (j % NSV) * KV_TILE, j);
-        cp_async_wait<1>();
-        fence_proxy_async_smem();
-        mbar_arrive(bar(PB_KF + j % NSK));
-        if (j == n_tiles - 1) {
+          cp_async_commit();
           cp_async_wait<0>();
-          fence_proxy_async_smem();
-          mbar_arrive(bar(PB_VF + j % NSV));
+          fence_proxy_async_smem();             // make them visible to the tensor core
+          mbar_arrive(bar(full_bar + j % nst));
         }
-      }
-      cp_async_wait<0>();
+        cp_async_wait<0>();
+      };
+      if (is_v)
+        produce(std::integral_constant<int, 32>{}, static_cast<const __nv_bfloat16*>(a.v_cache),
+                sbase + OFF_V, NSV, PB_VF, PB_VE, lane);
+      else
+        produce(std::integral_constant<int, 64>{}, static_cast<const __nv_bfloat16*>(a.k_cache),
+                sbase + OFF_K, NSK, PB_KF, PB_KE, tid - kSoftThreads);
     } else if (warp == W_MMA) {
       // ------------------------------------------------------------- MMA issuer
       {
@@ -315,7 +317,7 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
         auto issue_qk = [&](int hh, int j) {
           const uint32_t kb = sbase + OFF_K + (j % NSK) * KV_TILE;
           const uint32_t qa = sbase + OFF_Q + hh * Q_BYTES;
-  #pragma unroll
+#pragma unroll
           for (int k = 0; k < HD / 16; ++k) {
             const uint64_t ad = make_sw128_desc(qa + (k >> 2) * QHALF + (k & 3) * 32, 16, 1024);
             const uint64_t bd = make_sw128_desc(kb + (k >> 2) * KHALF + (k & 3) * 32, 16, 1024);
@@ -324,15 +326,15 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
           commit_e(bar(PB_SF + hh));
         };
         // O_h += P_h V_j, P_h from TMEM (16 keys = 8 columns per step)
-        auto issue_pv = [&](int hh, int j) {
+        auto issue_pv = [&](int hh, int j) {   // commits O_done after the last tile only
           const uint32_t vb = sbase + OFF_V + (j % NSV) * KV_TILE;
-  #pragma unroll
+#pragma unroll
           for (int k = 0; k < BN / 16; ++k) {
             const uint64_t bd = make_sw128_desc(vb + k * 16 * 128, KHALF, 1024);
             mma_ts_e(tmem + COL_O + hh * HD, tmem + COL_S + hh * BN + k * 8, bd, idesc_pv,
                      (j > 0 || k > 0) ? 1u : 0u);
           }
-          commit_e(bar(PB_OD + hh));
+          if (j == n_tiles - 1) commit_e(bar(PB_OD + hh));
         };
         // The two heads alternate on the tensor core: while head A's softmax
         // turns S_A into P_A, the products of head B run, and the other way
@@ -340,28 +342,31 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
         // P_h V_j: tcgen05.mma operations issued by one thread execute in issue
         // order, so the earlier product has read P_h before the later one
         // writes there, and no wait for its completion is needed.
+        // The tensor core queues only a few products ahead of the issuer, so
+        // whatever the issuer does between products (waits, commits, fences)
+        // can leave it idle.  The loop therefore commits only what a waiter
+        // needs (S_h and V(j) per tile, O_h after the last tile; the softmax
+        // warps release the K stages) and its waits take a fast path.
         if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(bar(PB_KF + 0), 0, abort_flag, a.err));
         if (ok) {
           tc_fence_after();
           issue_qk(0, 0);
           issue_qk(1, 0);
-          commit_e(bar(PB_KE + 0));               // K(0) no longer needed
         }
         for (int j = 0; j < n_tiles && ok; ++j) {
           const bool more = j + 1 < n_tiles;
           for (int hh = 0; hh < 2 && ok; ++hh) {
-            ok = __all_sync(0xffffffffu, wait_or_abort(bar(PB_PF + hh), j & 1, abort_flag, a.err));
+            ok = __all_sync(0xffffffffu, wait_fast(bar(PB_PF + hh), j & 1, abort_flag, a.err));
             if (!ok) break;
             tc_fence_after();
-            if (hh == 0) ok = __all_sync(0xffffffffu, wait_or_abort(bar(PB_VF + j % NSV), (j / NSV) & 1, abort_flag, a.err));
+            if (hh == 0) ok = __all_sync(0xffffffffu, wait_fast(bar(PB_VF + j % NSV), (j / NSV) & 1, abort_flag, a.err));
             if (!ok) break;
             issue_pv(hh, j);
             if (hh == 1) commit_e(bar(PB_VE + j % NSV));   // V(j) no longer needed
             if (more) {
-              if (hh == 0) ok = __all_sync(0xffffffffu, wait_or_abort(bar(PB_KF + (j + 1) % NSK), ((j + 1) / NSK) & 1, abort_flag, a.err));
+              if (hh == 0) ok = __all_sync(0xffffffffu, wait_fast(bar(PB_KF + (j + 1) % NSK), ((j + 1) / NSK) & 1, abort_flag, a.err));
               if (!ok) break;
               issue_qk(hh, j + 1);
-              if (hh == 1) commit_e(bar(PB_KE + (j + 1) % NSK));   // K(j+1) no longer needed
             }
           }
         }
@@ -379,9 +384,11 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
     const float sl2 = a.scale * 1.4426950408889634f;
     float m_run = -INFINITY, l_run = 0.f;   // running max in scaled log2 units
     for (int j = 0; j < n_tiles; ++j) {
-      wait_or_abort(bar(PB_SF + hh), j & 1, abort_flag, a.err);
+      wait_fast(bar(PB_SF + hh), j & 1, abort_flag, a.err);
       __syncwarp();
       tc_fence_after();
+      // the S_B commit follows both heads' Q K_j^T: K(j) can be refilled
+      if (hh == 1 && lane == 0) mbar_arrive(bar(PB_KE + j % NSK));
       const int k0 = j * BN;
       const bool diag = k0 + BN - 1 > a.prior_len + q0;   // causal mask needed
       // the whole S row into registers: four loads in flight, one wait
@@ -413,11 +420,10 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
       if (mx > m_run + kLazyP || m_run == -INFINITY) m_new = mx;
       const float alpha = (m_new == m_run) ? 1.f : fast_exp2(m_run - m_new);
       if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        // O holds P V of the tiles before; its last product is done (S_h of
-        // this tile was only computed after it), so rescale it in place
-        wait_or_abort(bar(PB_OD + hh), (j - 1) & 1, abort_flag, a.err);
+        // O holds P V of the tiles before; the S_h commit of this tile was
+        // issued behind their last product, so that product is complete and
+        // O can be rescaled in place
         __syncwarp();
-        tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < HD / 32; ++c) {
           float o[32];
@@ -453,9 +459,10 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
       l_run = l_run * alpha + (sum0 + sum1);
       m_run = m_new;
       tc_fence_before();
-      mbar_arrive(bar(PB_PF + hh));
+      __syncwarp();                         // the warp's P stores precede its one arrival
+      if (lane == 0) mbar_arrive(bar(PB_PF + hh));
     }
-    wait_or_abort(bar(PB_OD + hh), (n_tiles - 1) & 1, abort_flag, a.err);
+    wait_or_abort(bar(PB_OD + hh), 0, abort_flag, a.err);
     __syncwarp();
     tc_fence_after();
     const float inv = 1.f / l_run;
