@@ -32,8 +32,10 @@
 //                     the diagonal tiles); the max is raised lazily, only when
 //                     it grows by more than 2^8, and then O is rescaled in
 //                     TMEM.  It forms p = 2^(s*scale*log2e - m) with one FMA and
-//                     ex2 per score, sums it and stores it as bf16 into TMEM;
-//                     one arrival per warp hands P to the MMA issuer.  Once a
+//                     ex2 per score, sums it and stores it as bf16 into TMEM.
+//                     P goes to the MMA issuer in two halves (one arrival per
+//                     warp each): P V of the first 64 keys runs while the
+//                     exponentials of the second 64 are formed.  Once a
 //                     tile's S_B is complete, the head-B warps release its K
 //                     stage (the S_B commit follows both heads' Q K^T).
 //                     Epilogue O / l.
@@ -100,8 +102,8 @@ enum {
   PB_VF = PB_KE + NSK,        // [NSV]
   PB_VE = PB_VF + NSV,        // [NSV]
   PB_SF = PB_VE + NSV,        // [head]
-  PB_PF = PB_SF + 2,          // [head]
-  PB_OD = PB_PF + 2,          // [head]
+  PB_PF = PB_SF + 2,          // [head][half]
+  PB_OD = PB_PF + 4,          // [head]
   PB_COUNT = PB_OD + 2
 };
 static_assert(PB_COUNT * 8 + 8 <= 256, "barrier area");
@@ -201,7 +203,8 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(PB_SF + i), 1);
-      mbar_init(bar(PB_PF + i), 4);              // one arrival per softmax warp
+      mbar_init(bar(PB_PF + 2 * i), 4);          // one arrival per softmax warp
+      mbar_init(bar(PB_PF + 2 * i + 1), 4);
       mbar_init(bar(PB_OD + i), 1);
     }
     *abort_i = 0;
@@ -326,15 +329,17 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
           commit_e(bar(PB_SF + hh));
         };
         // O_h += P_h V_j, P_h from TMEM (16 keys = 8 columns per step)
-        auto issue_pv = [&](int hh, int j) {   // commits O_done after the last tile only
+        // (half 0: keys 0-63, half 1: keys 64-127; O_done is committed after
+        // the last tile only)
+        auto issue_pv = [&](int hh, int j, int half) {
           const uint32_t vb = sbase + OFF_V + (j % NSV) * KV_TILE;
 #pragma unroll
-          for (int k = 0; k < BN / 16; ++k) {
+          for (int k = half * 4; k < half * 4 + 4; ++k) {
             const uint64_t bd = make_sw128_desc(vb + k * 16 * 128, KHALF, 1024);
             mma_ts_e(tmem + COL_O + hh * HD, tmem + COL_S + hh * BN + k * 8, bd, idesc_pv,
                      (j > 0 || k > 0) ? 1u : 0u);
           }
-          if (j == n_tiles - 1) commit_e(bar(PB_OD + hh));
+          if (half == 1 && j == n_tiles - 1) commit_e(bar(PB_OD + hh));
         };
         // The two heads alternate on the tensor core: while head A's softmax
         // turns S_A into P_A, the products of head B run, and the other way
@@ -356,12 +361,16 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
         for (int j = 0; j < n_tiles && ok; ++j) {
           const bool more = j + 1 < n_tiles;
           for (int hh = 0; hh < 2 && ok; ++hh) {
-            ok = __all_sync(0xffffffffu, wait_fast(bar(PB_PF + hh), j & 1, abort_flag, a.err));
+            ok = __all_sync(0xffffffffu, wait_fast(bar(PB_PF + 2 * hh), j & 1, abort_flag, a.err));
             if (!ok) break;
             tc_fence_after();
             if (hh == 0) ok = __all_sync(0xffffffffu, wait_fast(bar(PB_VF + j % NSV), (j / NSV) & 1, abort_flag, a.err));
             if (!ok) break;
-            issue_pv(hh, j);
+            issue_pv(hh, j, 0);
+            ok = __all_sync(0xffffffffu, wait_fast(bar(PB_PF + 2 * hh + 1), j & 1, abort_flag, a.err));
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(hh, j, 1);
             if (hh == 1) commit_e(bar(PB_VE + j % NSV));   // V(j) no longer needed
             if (more) {
               if (hh == 0) ok = __all_sync(0xffffffffu, wait_fast(bar(PB_KF + (j + 1) % NSK), ((j + 1) / NSK) & 1, abort_flag, a.err));
@@ -452,15 +461,17 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
           pk[i / 2] = pack_bf16(pp.x, pp.y);
         }
         tmem_st16(lane_base + col_s + c * 16, pk);
+        if (c & 1) {                        // a half of P is in TMEM
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(PB_PF + 2 * hh + (c >> 1)));
+        }
       }
       const float2 s01 = fadd2(sum2[0], sum2[1]), s23 = fadd2(sum2[2], sum2[3]);
       const float sum0 = s01.x + s23.x, sum1 = s01.y + s23.y;
-      tmem_wait_st();
       l_run = l_run * alpha + (sum0 + sum1);
       m_run = m_new;
-      tc_fence_before();
-      __syncwarp();                         // the warp's P stores precede its one arrival
-      if (lane == 0) mbar_arrive(bar(PB_PF + hh));
     }
     wait_or_abort(bar(PB_OD + hh), 0, abort_flag, a.err);
     __syncwarp();
