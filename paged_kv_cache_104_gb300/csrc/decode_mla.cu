@@ -20,7 +20,10 @@
 //  * a block is loaded once (16 rows x 256 B) and serves as both the K and the
 //    V operand;
 //  * eight consumer warps: warp w takes block w % 4 of each stage for the
-//    query heads 16 * (w / 4) .. + 15, so each staged block feeds two warps.
+//    query heads 16 * (w / 4) .. + 15, so each staged block feeds two warps;
+//  * a register split (setmaxnreg): the producer warp and three idle warps
+//    completing its warpgroup drop to 40 registers so the consumers can take
+//    232; at the 168 of the launch the consumers spilled.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -37,7 +40,10 @@ constexpr int kNTL = kHalfHeads / 8;             // head tiles of 8 per warp
 constexpr int kBPSL = 4;                         // blocks per stage
 constexpr int kCWL = 2 * kBPSL;                  // consumer warps
 constexpr int kConsumersL = kCWL * 32;
-constexpr int kThreadsL = kConsumersL + 32;
+constexpr int kThreadsL = kConsumersL + 128;     // producer warp + three idle warps (warpgroup 2)
+constexpr int kRegsConsL = 232, kRegsRestL = 40;
+static_assert(kRegsConsL * kConsumersL + kRegsRestL * 128 <= ((65536 / kThreadsL) & ~7) * kThreadsL,
+              "register split within the launch budget");
 constexpr int kStageTokL = kBPSL * kBlockSize;   // 64 tokens
 constexpr int kHalfL = kBlockSize * 128;         // 16 rows x 128 B: one 64-column half
 constexpr int kTileL = 2 * kHalfL;               // one latent block, 4 KiB
@@ -127,6 +133,8 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c) 
   const int total = cu[a.num_seqs];
   volatile int* vabort = abort_flag;
 
+  if (warp >= kCWL) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsRestL));
+  if (warp > kCWL) return;   // idle warps of warpgroup 2
   if (warp == kCWL) {
     // ------------------------------------------------------------ producer
     if (lane == 0)
@@ -188,6 +196,7 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c) 
   }
 
   // -------------------------------------------------------------- consumers
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsConsL));
   const int g = lane >> 2, t = lane & 3;
   const int bw = warp & (kBPSL - 1);              // block of the stage this warp takes
   const int hbase = (warp / kBPSL) * kHalfHeads;   // its 16 query heads
