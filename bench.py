@@ -521,16 +521,34 @@ def run_ours(args, w, lay, acct):
     k_new_pre = [inputs[li].k_new[nd:] for li in range(L)]
     v_new_pre = [inputs[li].v_new[nd:] for li in range(L)]
     slot_pre = slot[nd:]
+    # decode and prefill of a layer side by side on disjoint SMs (the prefill
+    # as persistent CTAs on prefill_sms SMs, the decode on the rest)
+    side = bool(args.side_by_side and fused and w.prefill_chunk and hq // hkv % 2 == 0)
+    split = {"prefill_sms": int(args.prefill_sms)}
 
-    def step(ev=None, s=None):
+    def step(ev=None, s=None, serial=False):
         for li in range(L):
-            layer(li, ev, s)
+            layer(li, ev, s, serial)
 
-    def layer(li, ev=None, s=None):
+    def layer(li, ev=None, s=None, serial=False):
         s = stream if s is None else s
         if True:
             x = inputs[li]
             kc, vc = pools[li % n_pools]
+            if side and not serial:
+                # the chunk's tokens by kv_append; then the decode (appending
+                # its tokens) and the prefill side by side
+                B.kv_append(k_new_pre[li], v_new_pre[li], kc, vc, slot_pre, stream=s)
+                if ev is not None:
+                    ev[li][0].record(s)
+                B.decode_prefill_attention(out_dec[li], x.q_decode, k_new_dec[li], v_new_dec[li],
+                                           kc, vc, bt_dec, seq_lens, max_seq, out_pre[li],
+                                           x.q_prefill, bt_pre, w.prefill_prior, w.scale, wsp,
+                                           prefill_sms=split["prefill_sms"], stream=s)
+                if ev is not None:
+                    ev[li][1].record(s)
+                    ev[li][2].record(s)
+                return
             if fused:
                 # decode tokens are appended inside the decode launch; the
                 # prefill chunk's tokens by kv_append
@@ -555,6 +573,23 @@ def run_ours(args, w, lay, acct):
                 if ev is not None:
                     ev[li][2].record(s)
 
+    if side and split["prefill_sms"] <= 0:
+        # pick the split: a short eager run of the whole step per candidate
+        # (outside the timed region); the decode needs far fewer SMs than the
+        # GPU has to stream the cache, the prefill's time falls with its SMs
+        nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+        trials = {}
+        for cand in sorted({max(4, nsm * f // 64) for f in (8, 10, 12, 14, 16, 18, 20, 24)}):
+            split["prefill_sms"] = cand
+            step()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            trials[cand] = e0.elapsed_time(e1)
+        split["prefill_sms"] = min(trials, key=trials.get)
+        split["trials_ms"] = {str(k): round(v, 3) for k, v in sorted(trials.items())}
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -611,6 +646,19 @@ def run_ours(args, w, lay, acct):
     dec_ms = [evs[k][li][0].elapsed_time(evs[k][li][1]) for k in range(nsteps_ev) for li in range(L)]
     pre_ms = ([evs[k][li][1].elapsed_time(evs[k][li][2]) for k in range(nsteps_ev)
                for li in range(L)] if w.prefill_chunk else [])
+    ser_dec_ms = None
+    if side:
+        # in the timed steps the decode and the prefill of a layer overlap:
+        # the events bracket the pair, which the decode spans, so the decode's
+        # rate over the timed region is its bytes over the pair's time.  The
+        # prefill's own time (and the decode's alone) comes from one serial
+        # step (decode, then prefill, each on the whole GPU) right after.
+        ev_ser = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(L)]
+        step(ev_ser, serial=True)
+        torch.cuda.synchronize(dev)
+        assert B.get_device_error() == 0, "device error word set during the serial step"
+        ser_dec_ms = [ev_ser[li][0].elapsed_time(ev_ser[li][1]) for li in range(L)]
+        pre_ms = [ev_ser[li][1].elapsed_time(ev_ser[li][2]) for li in range(L)]
     ms_step = total_ms / args.steps
     n = ws
     value = n * acct["bytes_step"] / (ms_step / 1e3) / 1e9
@@ -658,8 +706,29 @@ def run_ours(args, w, lay, acct):
         "clocks": clk.summary(),
         "gpu_launches": args.steps * L * ((0 if fused and not w.prefill_chunk else 1) + split_launch
                                           + (1 if w.prefill_chunk else 0)),
-        "mode": {"fused_append": bool(fused), "cuda_graph": graph is not None},
+        "mode": {"fused_append": bool(fused), "cuda_graph": graph is not None,
+                 "side_by_side": side},
     }
+    if side:
+        nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+        ser_dec = sum(ser_dec_ms) / len(ser_dec_ms)
+        line["side_by_side"] = {
+            "what": "per layer, the decode (fused append, main + reduce) and the chunk's prefill run "
+                    "at the same time on disjoint SMs: the prefill as persistent CTAs on prefill_sms "
+                    "SMs, the decode as their programmatic dependent on the rest",
+            "prefill_sms": split["prefill_sms"], "decode_sms": nsm - split["prefill_sms"],
+            "split_trials_ms_per_step": split.get("trials_ms"),
+            "pair_ms_per_layer": dec_avg,
+            "decode_ms_per_layer_alone": ser_dec,
+            "decode_gbs_alone": acct["decode_bytes_layer"] / (ser_dec / 1e3) / 1e9,
+            "prefill_ms_per_layer_alone": line["prefill_ms_per_layer"],
+        }
+        line["roofline"]["note"] = ("timed steps: the decode runs side by side with the prefill and "
+                                    "spans the pair, so achieved = its bytes / the pair's event time "
+                                    "(a lower bound on its own rate)")
+        if line["prefill_roofline"]:
+            line["prefill_roofline"]["note"] = ("prefill measured alone, on all SMs, in one serial "
+                                                "step right after the timed region")
 
     # ---- end to end through the C ABI with host buffers (pinned), same step
     if args.e2e_steps > 0:
@@ -773,6 +842,10 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--fused-append", type=int, default=1,
                     help="1: decode tokens are appended inside the decode launch")
+    ap.add_argument("--side-by-side", type=int, default=1,
+                    help="1: each layer's decode and prefill run at the same time on disjoint SMs")
+    ap.add_argument("--prefill-sms", type=int, default=0,
+                    help="SMs for the prefill when side by side (0: pick by a short trial)")
     ap.add_argument("--graph", type=int, default=1,
                     help="1: replay the whole step as one captured CUDA graph")
     ap.add_argument("--fp8-decode", type=int, default=1,

@@ -205,6 +205,66 @@ pkv_status pkv_chunked_prefill_attention(void *out, const void *q, const void *k
                                          int head_dim, int block_size, float scale,
                                          pkv_dtype dtype, pkv_stream_t stream);
 
+/*
+ * decode_prefill_attention -- one layer of a continuous-batching step: the
+ * batch's decode (as pkv_paged_decode_attention_append: each sequence's new
+ * key/value appended, then one query per sequence over its cache) and one
+ * prompt chunk's prefill (as pkv_chunked_prefill_attention), run side by side
+ * on disjoint SMs of the GPU.  "The KV cache is not your bottleneck", section
+ * "The fix that mattered", admits prompts in capped chunks that share each
+ * step with the running decodes; this call gives them the tensor cores of
+ * some SMs while the memory-bound decode streams the cache on the rest.
+ *   All fields of pkv_decode_prefill_args mean what the same arguments of the
+ *   two calls mean (decode_out/decode_q/k_new/v_new/block_table/seq_lens/
+ *   num_seqs/max_blocks_per_seq/max_seq_len/workspace for the decode,
+ *   prefill_out/prefill_q/prefill_block_table/prefill_max_blocks/prior_len/
+ *   chunk_len for the prefill; pools, head counts, sizes, scale and dtype are
+ *   shared).  The chunk's own keys and values must already be in the pools,
+ *   and the chunk's sequence must not be one of the decoded sequences.
+ *   prefill_sms  SMs given to the prefill (0: a quarter of the GPU).  The
+ *                best split makes both halves end together; it depends on
+ *                the batch (the decode's cache bytes) and the chunk.
+ * Results are those of the two calls made one after the other (bit for bit).
+ * Both halves are checked before either is launched.  When the prefill
+ * cannot run as persistent tensor-core CTAs (not bf16 with head_dim 128, an
+ * odd GQA group, more than 512 work items -- 128-row query tiles times half
+ * the query heads -- or prefill_sms not below the SM count), the two run one
+ * after the other instead.  bf16 with head_dim 128 only for the decode
+ * (PKV_EUNSUPPORTED otherwise).
+ */
+typedef struct pkv_decode_prefill_args {
+  void *decode_out;
+  const void *decode_q;
+  const void *k_new;
+  const void *v_new;
+  const int32_t *block_table;
+  const int32_t *seq_lens;
+  int num_seqs;
+  int max_blocks_per_seq;
+  int max_seq_len;
+  void *workspace;
+  size_t workspace_bytes;
+  void *prefill_out;
+  const void *prefill_q;
+  const int32_t *prefill_block_table;
+  int prefill_max_blocks;
+  int prior_len;
+  int chunk_len;
+  void *k_cache;
+  void *v_cache;
+  int64_t num_blocks;
+  int num_q_heads;
+  int num_kv_heads;
+  int head_dim;
+  int block_size;
+  float scale;
+  pkv_dtype dtype;
+  int prefill_sms;
+} pkv_decode_prefill_args;
+
+pkv_status pkv_decode_prefill_attention(const pkv_decode_prefill_args *args,
+                                        pkv_stream_t stream);
+
 /* ---------------------------------------------------------------------------
  * fp8 KV cache (E4M3 codes with a float scale per KV head).  "The KV cache is
  * not your bottleneck", section "What the profile said", names cache

@@ -25,6 +25,7 @@ DEVERR = {0: "none", 1: "slot out of range", 2: "block id out of range",
           5: "shared-memory layout check failed"}
 EXPORTS = ("pkv_kv_append", "pkv_decode_workspace_bytes", "pkv_paged_decode_attention",
            "pkv_paged_decode_attention_append", "pkv_paged_decode_attention_noalloc", "pkv_chunked_prefill_attention",
+           "pkv_decode_prefill_attention",
            "pkv_get_device_error", "pkv_status_str", "pkv_abi_version",
            "pkv_kv_append_fp8", "pkv_paged_decode_attention_fp8",
            "pkv_latent_append", "pkv_mla_workspace_bytes", "pkv_mla_decode_attention",
@@ -32,6 +33,23 @@ EXPORTS = ("pkv_kv_append", "pkv_decode_workspace_bytes", "pkv_paged_decode_atte
            "pkv_prefix_cache_destroy", "pkv_prefix_cache_size", "pkv_prefix_cache_insert",
            "pkv_prefix_cache_evict", "pkv_prefix_cache_match", "pkv_prefix_plan")
 NOALLOC_SCRATCH_BYTES = 32 << 20  # PKV_NOALLOC_SCRATCH_BYTES
+
+
+class DecodePrefillArgs(ctypes.Structure):
+    """pkv_decode_prefill_args (field order and types as in pagedkv.h)."""
+    _fields_ = [("decode_out", ctypes.c_void_p), ("decode_q", ctypes.c_void_p),
+                ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
+                ("block_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
+                ("num_seqs", ctypes.c_int), ("max_blocks_per_seq", ctypes.c_int),
+                ("max_seq_len", ctypes.c_int), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t), ("prefill_out", ctypes.c_void_p),
+                ("prefill_q", ctypes.c_void_p), ("prefill_block_table", ctypes.c_void_p),
+                ("prefill_max_blocks", ctypes.c_int), ("prior_len", ctypes.c_int),
+                ("chunk_len", ctypes.c_int), ("k_cache", ctypes.c_void_p),
+                ("v_cache", ctypes.c_void_p), ("num_blocks", ctypes.c_int64),
+                ("num_q_heads", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("block_size", ctypes.c_int),
+                ("scale", ctypes.c_float), ("dtype", ctypes.c_int), ("prefill_sms", ctypes.c_int)]
 
 
 class PagedKVError(RuntimeError):
@@ -62,6 +80,7 @@ def load():
                                                            i, i, f, i, p]
         lib.pkv_paged_decode_attention_append.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i64, i,
                                                           i, i, i, f, p, sz, i, p]
+        lib.pkv_decode_prefill_attention.argtypes = [ctypes.POINTER(DecodePrefillArgs), p]
         lib.pkv_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int), i]
         lib.pkv_status_str.argtypes = [i]
         lib.pkv_status_str.restype = ctypes.c_char_p
@@ -99,7 +118,8 @@ def load():
         lib.pkv_prefix_plan.restype = i64
         for name in ("pkv_kv_append", "pkv_paged_decode_attention",
                      "pkv_paged_decode_attention_noalloc", "pkv_paged_decode_attention_append",
-                     "pkv_chunked_prefill_attention", "pkv_get_device_error", "pkv_abi_version"):
+                     "pkv_chunked_prefill_attention", "pkv_decode_prefill_attention",
+                     "pkv_get_device_error", "pkv_abi_version"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -262,6 +282,33 @@ def chunked_prefill_attention(out, q, k_cache, v_cache, block_table_row, prior_l
         int(block_table_row.shape[0]), int(prior_len), c, nb, hq, hkv, d, bs, float(scale),
         _dtype_code(q), _stream(stream))
     _check("pkv_chunked_prefill_attention", st)
+
+
+def decode_prefill_attention(dec_out, dec_q, k_new, v_new, k_cache, v_cache, block_table, seq_lens,
+                             max_seq_len: int, pre_out, pre_q, pre_block_table_row, prior_len: int,
+                             scale: float, workspace=None, prefill_sms: int = 0,
+                             stream=None) -> None:
+    """One layer's decode (as paged_decode_attention_append) and one chunk's
+    prefill (as chunked_prefill_attention) side by side on disjoint SMs:
+    prefill_sms SMs for the prefill (0: a quarter of the GPU)."""
+    b, hq, d = dec_q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    a = DecodePrefillArgs()
+    a.decode_out, a.decode_q = _ptr(dec_out), _ptr(dec_q)
+    a.k_new, a.v_new = _ptr(k_new), _ptr(v_new)
+    a.block_table, a.seq_lens = _ptr(block_table), _ptr(seq_lens)
+    a.num_seqs, a.max_blocks_per_seq, a.max_seq_len = b, int(block_table.shape[1]), int(max_seq_len)
+    a.workspace = _ptr(workspace)
+    a.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    a.prefill_out, a.prefill_q = _ptr(pre_out), _ptr(pre_q)
+    a.prefill_block_table = _ptr(pre_block_table_row)
+    a.prefill_max_blocks = int(pre_block_table_row.shape[0])
+    a.prior_len, a.chunk_len = int(prior_len), int(pre_q.shape[0])
+    a.k_cache, a.v_cache, a.num_blocks = _ptr(k_cache), _ptr(v_cache), nb
+    a.num_q_heads, a.num_kv_heads, a.head_dim, a.block_size = hq, hkv, d, bs
+    a.scale, a.dtype, a.prefill_sms = float(scale), _dtype_code(dec_q), int(prefill_sms)
+    st = load().pkv_decode_prefill_attention(ctypes.byref(a), _stream(stream))
+    _check("pkv_decode_prefill_attention", st)
 
 
 def get_device_error(clear: bool = True) -> int:

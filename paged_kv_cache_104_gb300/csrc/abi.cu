@@ -132,12 +132,14 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, i
 namespace {
 
 // Shared by paged_decode_attention and its fused-append form (k_new != null).
-pkv_status decode_impl(void* out, const void* q, const void* k_new, const void* v_new,
-                       const void* k_cache, const void* v_cache, const int32_t* block_table,
-                       const int32_t* seq_lens, int num_seqs, int max_blocks_per_seq,
-                       int max_seq_len, int64_t num_blocks, int num_q_heads, int num_kv_heads,
-                       int head_dim, int block_size, float scale, void* workspace,
-                       size_t workspace_bytes, pkv_dtype dtype, pkv_stream_t stream) {
+// Validates a decode call and fills its launch arguments; launches nothing.
+pkv_status decode_prepare(pkv::DecodeArgs* out_args, int* out_sms, void* out, const void* q,
+                          const void* k_new, const void* v_new, const void* k_cache,
+                          const void* v_cache, const int32_t* block_table,
+                          const int32_t* seq_lens, int num_seqs, int max_blocks_per_seq,
+                          int max_seq_len, int64_t num_blocks, int num_q_heads, int num_kv_heads,
+                          int head_dim, int block_size, float scale, void* workspace,
+                          size_t workspace_bytes, pkv_dtype dtype) {
   pkv_status st = check_heads(num_q_heads, num_kv_heads, head_dim, block_size, dtype);
   if (st != PKV_OK) return st;
   if (num_seqs < 0 || max_blocks_per_seq < 1 || max_seq_len < 1 || num_blocks < 1)
@@ -188,11 +190,104 @@ pkv_status decode_impl(void* out, const void* q, const void* k_new, const void* 
   a.is_bf16 = dtype == PKV_BF16;
   a.k_new = k_new;
   a.v_new = v_new;
-  cudaStream_t s_ = reinterpret_cast<cudaStream_t>(stream);
-  const cudaError_t e = pkv::decode_mma_supported(a.is_bf16, head_dim, num_q_heads / num_kv_heads)
-                            ? pkv::launch_paged_decode_mma(a, sms, s_)
-                            : pkv::launch_paged_decode(a, sms, s_);
+  *out_args = a;
+  *out_sms = sms;
+  return PKV_OK;
+}
+
+// Launches a prepared decode; sm_budget bounds its persistent grid, and
+// dependent launches it as the programmatic dependent of the stream's
+// previous kernel (tensor-core path only).
+pkv_status decode_launch(const pkv::DecodeArgs& a, int sm_budget, bool dependent,
+                         cudaStream_t s_) {
+  if (a.num_seqs == 0) return PKV_OK;   // nothing was prepared: an empty batch
+  const cudaError_t e =
+      pkv::decode_mma_supported(a.is_bf16, a.head_dim, a.num_q_heads / a.num_kv_heads)
+          ? pkv::launch_paged_decode_mma(a, sm_budget, s_, dependent)
+          : pkv::launch_paged_decode(a, sm_budget, s_);
   return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+pkv_status decode_impl(void* out, const void* q, const void* k_new, const void* v_new,
+                       const void* k_cache, const void* v_cache, const int32_t* block_table,
+                       const int32_t* seq_lens, int num_seqs, int max_blocks_per_seq,
+                       int max_seq_len, int64_t num_blocks, int num_q_heads, int num_kv_heads,
+                       int head_dim, int block_size, float scale, void* workspace,
+                       size_t workspace_bytes, pkv_dtype dtype, pkv_stream_t stream) {
+  pkv::DecodeArgs a{};
+  int sms = 0;
+  const pkv_status st = decode_prepare(&a, &sms, out, q, k_new, v_new, k_cache, v_cache,
+                                       block_table, seq_lens, num_seqs, max_blocks_per_seq,
+                                       max_seq_len, num_blocks, num_q_heads, num_kv_heads,
+                                       head_dim, block_size, scale, workspace, workspace_bytes,
+                                       dtype);
+  if (st != PKV_OK) return st;
+  return decode_launch(a, sms, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// Validates a chunked-prefill call; launches nothing.
+pkv_status prefill_check(const void* out, const void* q, const void* k_cache, const void* v_cache,
+                         const int32_t* block_table_row, int max_blocks, int prior_len,
+                         int chunk_len, int64_t num_blocks, int num_q_heads, int num_kv_heads,
+                         int head_dim, int block_size, float scale, pkv_dtype dtype) {
+  pkv_status st = check_heads(num_q_heads, num_kv_heads, head_dim, block_size, dtype);
+  if (st != PKV_OK) return st;
+  if (max_blocks < 1 || prior_len < 0 || chunk_len < 0 || num_blocks < 1) return PKV_EINVAL;
+  if (chunk_len == 0) return PKV_OK;
+  if ((int64_t)prior_len + chunk_len > (int64_t)max_blocks * block_size) return PKV_EINVAL;
+  if (!isfinite(scale)) return PKV_EINVAL;
+  if (!out || !q || !k_cache || !v_cache || !block_table_row) return PKV_EINVAL;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(block_table_row) & 3u))
+    return PKV_EINVAL;
+  if (!(dtype == PKV_BF16 && head_dim == 128) && chunk_len > PKV_MAX_SEQS) return PKV_ERANGE;
+  return PKV_OK;
+}
+
+// Launches a checked chunked prefill (chunk_len > 0).  persistent_ctas > 0
+// asks the two-head tensor-core kernel for that many persistent CTAs.
+pkv_status prefill_launch(void* out, const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_table_row, int max_blocks, int prior_len,
+                          int chunk_len, int64_t num_blocks, int num_q_heads, int num_kv_heads,
+                          int head_dim, float scale, pkv_dtype dtype, int persistent_ctas,
+                          cudaStream_t s) {
+  int* err = nullptr;
+  int sms = 0;
+  pkv_status st = device_state(&err, &sms);
+  if (st != PKV_OK) return st;
+  if (dtype == PKV_BF16 && head_dim == 128) {
+    pkv::PrefillArgs a{out, q, k_cache, v_cache, block_table_row, max_blocks, prior_len, chunk_len,
+                       num_blocks, num_q_heads, num_kv_heads, scale, err};
+    const cudaError_t e = pkv::prefill_pair_supported(num_q_heads, num_kv_heads)
+                              ? pkv::launch_prefill_pair(a, s, persistent_ctas)
+                              : pkv::launch_prefill_tc(a, sms, s);
+    return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
+  }
+  // CUDA-core path: every chunk row is one query over its causal prefix, run
+  // as a single split so no workspace is needed.
+  const int total = prior_len + chunk_len;
+  pkv::DecodeArgs a{};
+  a.out = const_cast<void*>(out);
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_table = block_table_row;
+  a.seq_lens = nullptr;
+  a.err = err;
+  a.num_seqs = chunk_len;
+  a.bt_stride = 0;
+  a.max_blocks_per_seq = max_blocks;
+  a.max_seq_len = total;
+  a.max_splits = 1;
+  a.split_tokens = ((total + pkv::kSplitTokens - 1) / pkv::kSplitTokens) * pkv::kSplitTokens;
+  a.num_blocks = num_blocks;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.scale = scale;
+  a.chunk_prior = prior_len;
+  a.is_bf16 = dtype == PKV_BF16;
+  return pkv::launch_paged_decode(a, sms, s) == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
 }  // namespace
@@ -427,55 +522,66 @@ pkv_status pkv_chunked_prefill_attention(void* out, const void* q, const void* k
                                          int64_t num_blocks, int num_q_heads, int num_kv_heads,
                                          int head_dim, int block_size, float scale,
                                          pkv_dtype dtype, pkv_stream_t stream) {
-  pkv_status st = check_heads(num_q_heads, num_kv_heads, head_dim, block_size, dtype);
-  if (st != PKV_OK) return st;
-  if (max_blocks < 1 || prior_len < 0 || chunk_len < 0 || num_blocks < 1) return PKV_EINVAL;
-  if (chunk_len == 0) return PKV_OK;
-  if ((int64_t)prior_len + chunk_len > (int64_t)max_blocks * block_size) return PKV_EINVAL;
-  if (!isfinite(scale)) return PKV_EINVAL;
-  if (!out || !q || !k_cache || !v_cache || !block_table_row) return PKV_EINVAL;
-  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
-      (reinterpret_cast<uintptr_t>(block_table_row) & 3u))
+  pkv_status st = prefill_check(out, q, k_cache, v_cache, block_table_row, max_blocks, prior_len,
+                                chunk_len, num_blocks, num_q_heads, num_kv_heads, head_dim,
+                                block_size, scale, dtype);
+  if (st != PKV_OK || chunk_len == 0) return st;
+  return prefill_launch(out, q, k_cache, v_cache, block_table_row, max_blocks, prior_len, chunk_len,
+                        num_blocks, num_q_heads, num_kv_heads, head_dim, scale, dtype, 0,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status pkv_decode_prefill_attention(const pkv_decode_prefill_args* x, pkv_stream_t stream) {
+  if (!x) return PKV_EINVAL;
+  // validate both halves before anything is launched
+  if (!dtype_ok(x->dtype)) return PKV_EDTYPE;
+  if (x->num_q_heads < 1 || x->num_kv_heads < 1 || x->num_q_heads % x->num_kv_heads != 0)
     return PKV_EINVAL;
-  int* err = nullptr;
+  if (!pkv::decode_mma_supported(x->dtype == PKV_BF16, x->head_dim,
+                                 x->num_q_heads / x->num_kv_heads))
+    return PKV_EUNSUPPORTED;
+  if (x->num_seqs > 0 && (!x->k_new || !x->v_new || !aligned16(x->k_new) || !aligned16(x->v_new)))
+    return PKV_EINVAL;
+  pkv::DecodeArgs d{};
   int sms = 0;
+  pkv_status st = decode_prepare(&d, &sms, x->decode_out, x->decode_q, x->k_new, x->v_new,
+                                 x->k_cache, x->v_cache, x->block_table, x->seq_lens, x->num_seqs,
+                                 x->max_blocks_per_seq, x->max_seq_len, x->num_blocks,
+                                 x->num_q_heads, x->num_kv_heads, x->head_dim, x->block_size,
+                                 x->scale, x->workspace, x->workspace_bytes, x->dtype);
+  if (st != PKV_OK) return st;
+  st = prefill_check(x->prefill_out, x->prefill_q, x->k_cache, x->v_cache, x->prefill_block_table,
+                     x->prefill_max_blocks, x->prior_len, x->chunk_len, x->num_blocks,
+                     x->num_q_heads, x->num_kv_heads, x->head_dim, x->block_size, x->scale,
+                     x->dtype);
+  if (st != PKV_OK) return st;
+  if (x->prefill_sms < 0) return PKV_EINVAL;
+  int* err = nullptr;
   st = device_state(&err, &sms);
   if (st != PKV_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (dtype == PKV_BF16 && head_dim == 128) {
-    pkv::PrefillArgs a{out, q, k_cache, v_cache, block_table_row, max_blocks, prior_len, chunk_len,
-                       num_blocks, num_q_heads, num_kv_heads, scale, err};
-    const cudaError_t e = pkv::prefill_pair_supported(num_q_heads, num_kv_heads)
-                              ? pkv::launch_prefill_pair(a, s)
-                              : pkv::launch_prefill_tc(a, sms, s);
-    return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
+  const int p_sms = x->prefill_sms > 0 ? x->prefill_sms : sms / 4;
+  pkv::PrefillArgs pa{x->prefill_out, x->prefill_q, x->k_cache, x->v_cache, x->prefill_block_table,
+                      x->prefill_max_blocks, x->prior_len, x->chunk_len, x->num_blocks,
+                      x->num_q_heads, x->num_kv_heads, x->scale, err};
+  const bool side_by_side = x->chunk_len > 0 && d.num_seqs > 0 && x->head_dim == 128 &&
+                            x->dtype == PKV_BF16 &&
+                            pkv::prefill_pair_supported(x->num_q_heads, x->num_kv_heads) &&
+                            p_sms < sms && pkv::prefill_pair_persistent_ok(pa, p_sms);
+  if (!side_by_side) {   // one after the other, each on the whole GPU
+    if (x->chunk_len > 0) {
+      st = prefill_launch(x->prefill_out, x->prefill_q, x->k_cache, x->v_cache,
+                          x->prefill_block_table, x->prefill_max_blocks, x->prior_len,
+                          x->chunk_len, x->num_blocks, x->num_q_heads, x->num_kv_heads,
+                          x->head_dim, x->scale, x->dtype, 0, s);
+      if (st != PKV_OK) return st;
+    }
+    return decode_launch(d, sms, false, s);
   }
-  // CUDA-core path: every chunk row is one query over its causal prefix, run
-  // as a single split so no workspace is needed.
-  if (chunk_len > PKV_MAX_SEQS) return PKV_ERANGE;
-  const int total = prior_len + chunk_len;
-  pkv::DecodeArgs a{};
-  a.out = out;
-  a.q = q;
-  a.k_cache = k_cache;
-  a.v_cache = v_cache;
-  a.block_table = block_table_row;
-  a.seq_lens = nullptr;
-  a.err = err;
-  a.num_seqs = chunk_len;
-  a.bt_stride = 0;
-  a.max_blocks_per_seq = max_blocks;
-  a.max_seq_len = total;
-  a.max_splits = 1;
-  a.split_tokens = ((total + pkv::kSplitTokens - 1) / pkv::kSplitTokens) * pkv::kSplitTokens;
-  a.num_blocks = num_blocks;
-  a.num_q_heads = num_q_heads;
-  a.num_kv_heads = num_kv_heads;
-  a.head_dim = head_dim;
-  a.scale = scale;
-  a.chunk_prior = prior_len;
-  a.is_bf16 = dtype == PKV_BF16;
-  return pkv::launch_paged_decode(a, sms, s) == cudaSuccess ? PKV_OK : PKV_ECUDA;
+  // the prefill's persistent CTAs take p_sms SMs; the decode, launched as its
+  // programmatic dependent, runs on the others and finishes after it
+  if (pkv::launch_prefill_pair(pa, s, p_sms) != cudaSuccess) return PKV_ECUDA;
+  return decode_launch(d, sms - p_sms, true, s);
 }
 
 }  // extern "C"

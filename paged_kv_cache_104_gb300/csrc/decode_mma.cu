@@ -500,10 +500,14 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
     }
     named_bar_sync(1, kConsumersM);
   }
+  // Launched as the programmatic dependent of a persistent prefill on the
+  // other SMs, this grid finishes only after that one, so the launches that
+  // follow in the stream see both.  Without such a launch it returns at once.
+  if (tid == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <int G, bool FUSE>
-cudaError_t launch_g(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
+cudaError_t launch_g(const DecodeArgs& a, int num_sms, cudaStream_t stream, bool dependent) {
   using C = MCfg<G>;
   CUtensorMap tm_k, tm_v;
   const int64_t rows = a.num_blocks * a.num_kv_heads * kBlockSize;
@@ -518,7 +522,24 @@ cudaError_t launch_g(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
   const int per_sm = by_smem < 1 ? 1 : (by_smem > (G <= 8 ? 3 : 2) ? (G <= 8 ? 3 : 2) : by_smem);
   const int64_t upper = (int64_t)a.num_seqs * a.num_kv_heads * a.max_splits;
   const int grid = (int)(upper < (int64_t)num_sms * per_sm ? upper : (int64_t)num_sms * per_sm);
-  decode_mma_kernel<G, FUSE><<<grid, kThreadsM, smem, stream>>>(a, tm_k, tm_v);
+  if (dependent) {
+    // programmatic dependent launch: may start while the previous kernel in
+    // the stream (a persistent prefill holding its own SMs) still runs
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreadsM);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, decode_mma_kernel<G, FUSE>, a, tm_k, tm_v);
+    if (e != cudaSuccess) return e;
+  } else {
+    decode_mma_kernel<G, FUSE><<<grid, kThreadsM, smem, stream>>>(a, tm_k, tm_v);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess || a.max_splits <= 1) return e;
   return launch_decode_reduce_bf16_128(a, stream);
@@ -531,15 +552,17 @@ bool decode_mma_supported(int is_bf16, int head_dim, int group) {
          (group == 1 || group == 2 || group == 4 || group == 8 || group == 16);
 }
 
-cudaError_t launch_paged_decode_mma(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
+cudaError_t launch_paged_decode_mma(const DecodeArgs& a, int num_sms, cudaStream_t stream,
+                                    bool dependent) {
   if (a.chunk_prior >= 0 || a.split_tokens % kStageTok != 0) return cudaErrorInvalidValue;
   const bool fuse = a.k_new != nullptr;
+  const int d = dependent;
   switch (a.num_q_heads / a.num_kv_heads) {
-    case 1: return fuse ? launch_g<1, true>(a, num_sms, stream) : launch_g<1, false>(a, num_sms, stream);
-    case 2: return fuse ? launch_g<2, true>(a, num_sms, stream) : launch_g<2, false>(a, num_sms, stream);
-    case 4: return fuse ? launch_g<4, true>(a, num_sms, stream) : launch_g<4, false>(a, num_sms, stream);
-    case 8: return fuse ? launch_g<8, true>(a, num_sms, stream) : launch_g<8, false>(a, num_sms, stream);
-    case 16: return fuse ? launch_g<16, true>(a, num_sms, stream) : launch_g<16, false>(a, num_sms, stream);
+    case 1: return fuse ? launch_g<1, true>(a, num_sms, stream, d) : launch_g<1, false>(a, num_sms, stream, d);
+    case 2: return fuse ? launch_g<2, true>(a, num_sms, stream, d) : launch_g<2, false>(a, num_sms, stream, d);
+    case 4: return fuse ? launch_g<4, true>(a, num_sms, stream, d) : launch_g<4, false>(a, num_sms, stream, d);
+    case 8: return fuse ? launch_g<8, true>(a, num_sms, stream, d) : launch_g<8, false>(a, num_sms, stream, d);
+    case 16: return fuse ? launch_g<16, true>(a, num_sms, stream, d) : launch_g<16, false>(a, num_sms, stream, d);
     default: return cudaErrorInvalidValue;
   }
 }

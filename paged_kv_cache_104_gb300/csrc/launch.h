@@ -79,7 +79,11 @@ cudaError_t launch_paged_decode(const DecodeArgs& a, int num_sms, cudaStream_t s
 // Tensor-core (mma.sync) decode for bf16, head_dim 128, group in {1,2,4,8,16};
 // decode mode only (chunk_prior < 0).  Launches the split reduce when needed.
 bool decode_mma_supported(int is_bf16, int head_dim, int group);
-cudaError_t launch_paged_decode_mma(const DecodeArgs& a, int num_sms, cudaStream_t stream);
+// dependent: launch as the programmatic dependent of the previous kernel in
+// the stream (see launch_prefill_pair); the grid then also waits, at its end,
+// for that kernel to complete.  num_sms bounds the persistent grid.
+cudaError_t launch_paged_decode_mma(const DecodeArgs& a, int num_sms, cudaStream_t stream,
+                                    bool dependent = false);
 // fp8 (E4M3) cache, bf16 q/out, head_dim 128, group in {1,2,4,8,16}; uses
 // DecodeArgs with k_scale / v_scale set.
 cudaError_t launch_paged_decode_fp8(const DecodeArgs& a, int num_sms, cudaStream_t stream);
@@ -111,7 +115,12 @@ struct PrefillArgs {
 // tcgen05 path, one query head per CTA: bf16, head_dim 128, block_size 16.
 cudaError_t launch_prefill_tc(const PrefillArgs& a, int num_sms, cudaStream_t stream);
 // tcgen05 path, two query heads of one GQA group per CTA (group size even).
+// persistent_ctas > 0: that many persistent CTAs run the work items (query
+// tile x head pair), assigned longest first, and each signals at its start
+// that a programmatically dependent launch may begin (so a kernel launched
+// next with that attribute runs on the remaining SMs); 0: one CTA per item.
 bool prefill_pair_supported(int num_q_heads, int num_kv_heads);
-cudaError_t launch_prefill_pair(const PrefillArgs& a, cudaStream_t stream);
+bool prefill_pair_persistent_ok(const PrefillArgs& a, int ctas);
+cudaError_t launch_prefill_pair(const PrefillArgs& a, cudaStream_t stream, int persistent_ctas = 0);
 
 }  // namespace pkv

@@ -57,6 +57,10 @@
 // stops issuing work, lets its copies land, frees its TMEM and returns.
 #include <cuda.h>
 
+#include <algorithm>
+#include <queue>
+#include <vector>
+
 #include <type_traits>
 
 #include "common.cuh"
@@ -108,11 +112,20 @@ enum {
 };
 static_assert(PB_COUNT * 8 + 8 <= 256, "barrier area");
 
+constexpr int kMaxItems = 512;      // persistent mode: work items in the parameter list
+constexpr int kMaxCtas = 160;
 struct PairParams {
   PrefillArgs a;
   int total_len;
   int kv_rows;
   int q_tiles;
+  // Persistent mode (n_list > 0): CTA c runs the work items
+  // list[start[c]] .. list[start[c + 1] - 1] one after the other, item =
+  // query tile * (heads / 2) + head pair, assigned by the host.  Otherwise
+  // each CTA runs one item, head pair blockIdx.x, query tile from blockIdx.y.
+  int n_list;
+  uint16_t start[kMaxCtas + 1];
+  uint16_t list[kMaxItems];
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
@@ -184,12 +197,31 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int group = a.num_q_heads / a.num_kv_heads;
-  const int h0 = 2 * blockIdx.x;                          // heads h0, h0 + 1
-  const int g = h0 / group;                               // their KV head
-  const int qt = p.q_tiles - 1 - (int)blockIdx.y;         // heaviest tiles first
-  const int q0 = qt * BM;
-  const int last_row_pos = a.prior_len + min(a.chunk_len, q0 + BM) - 1;
-  const int n_tiles = last_row_pos / BN + 1;
+  const int n_pairs = a.num_q_heads / 2;
+  const int it_begin = p.n_list > 0 ? p.start[blockIdx.x] : 0;
+  const int it_end = p.n_list > 0 ? p.start[blockIdx.x + 1] : 1;
+  // work item it: heads h0, h0 + 1 (KV head g), query rows q0 .. q0 + 127,
+  // key tiles 0 .. n_tiles - 1
+  struct Item {
+    int h0, g, q0, n_tiles;
+  };
+  auto item_at = [&](int it) {
+    int pair, qt;
+    if (p.n_list > 0) {
+      const int item = p.list[it];
+      pair = item % n_pairs;
+      qt = item / n_pairs;
+    } else {
+      pair = blockIdx.x;
+      qt = p.q_tiles - 1 - (int)blockIdx.y;               // heaviest tiles first
+    }
+    Item w;
+    w.h0 = 2 * pair;
+    w.g = w.h0 / group;
+    w.q0 = qt * BM;
+    w.n_tiles = (a.prior_len + min(a.chunk_len, w.q0 + BM) - 1) / BN + 1;
+    return w;
+  };
 
   if (tid == 0) {
     mbar_init(bar(PB_Q), 1);
@@ -220,6 +252,9 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // persistent mode: this CTA holds its SM for the whole launch, so a kernel
+  // launched next as a programmatic dependent may start on the other SMs
+  if (p.n_list > 0 && tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp >= 8) {
     // Warpgroup 2 (producers and MMA issuer) hands registers to
@@ -257,22 +292,46 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
         const int rsub = pt >> 4, cc = pt & 15;
         const int half = cc >> 3, ch = cc & 7;
         const uint32_t thr_dst = half * KHALF + rsub * 128;
+        int jg = 0;                            // ring position over all items
+        bool go = true, q_pending = false;
+        uint32_t q_phase = 0;
+        if (is_v && lane == 0)
+          asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
+        for (int it = it_begin; it < it_end && go; ++it) {
+        const Item w = item_at(it);
+        if (is_v) {
+          // the item's Q, once the previous item's last Q_B K^T has read the buffer
+          const int ii = it - it_begin;
+          if (ii > 0) go = wait_or_abort(bar(PB_SF + 1), (jg - 1) & 1, abort_flag, a.err);
+          go = __all_sync(0xffffffffu, go && !*abort_flag);
+          if (!go) break;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar(PB_Q), 2 * Q_BYTES);
+            for (int hh = 0; hh < 2; ++hh) {
+              tma_load_3d(sbase + OFF_Q + hh * Q_BYTES, &tm_q, bar(PB_Q), 0, w.h0 + hh, w.q0);
+              tma_load_3d(sbase + OFF_Q + hh * Q_BYTES + QHALF, &tm_q, bar(PB_Q), 64, w.h0 + hh, w.q0);
+            }
+          }
+          __syncwarp();
+          q_pending = true;
+          q_phase = ii & 1;
+        }
         int cur_ids = load_ids(0), next_ids = load_ids(1);
-        for (int j = 0; j < n_tiles; ++j) {
+        for (int j = 0; j < w.n_tiles; ++j, ++jg) {
           if (j > 0 && j % kTilesPerWin == 0) {
             cur_ids = next_ids;
             next_ids = load_ids(j / kTilesPerWin + 1);
           }
-          bool go = true;
-          if (j >= nst) go = wait_or_abort(bar(empty_bar + j % nst), ((j / nst) - 1) & 1, abort_flag, a.err);
-          if (!__all_sync(0xffffffffu, go && !*abort_flag)) break;  // leave the loop as a warp
-          const uint32_t dst = ring + (j % nst) * KV_TILE;
+          if (jg >= nst) go = wait_or_abort(bar(empty_bar + jg % nst), ((jg / nst) - 1) & 1, abort_flag, a.err);
+          go = __all_sync(0xffffffffu, go && !*abort_flag);
+          if (!go) break;                      // leave the loop as a warp
+          const uint32_t dst = ring + (jg % nst) * KV_TILE;
           const bool full = (j + 1) * BN <= p.total_len;
 #pragma unroll 2
           for (int bi = 0; bi < kBlkPerTile; ++bi) {
             const int blk = __shfl_sync(0xffffffffu, cur_ids, ((j % kTilesPerWin) * kBlkPerTile + bi) & 31);
             const __nv_bfloat16* bsrc =
-                pool + ((int64_t)blk * a.num_kv_heads + g) * (kBlockSize * HD) + rsub * HD + cc * 8;
+                pool + ((int64_t)blk * a.num_kv_heads + w.g) * (kBlockSize * HD) + rsub * HD + cc * 8;
             const uint32_t bdst = dst + thr_dst + bi * kBlockSize * 128;
             if (full) {
 #pragma unroll
@@ -291,8 +350,12 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
           cp_async_commit();
           cp_async_wait<0>();
           fence_proxy_async_smem();             // make them visible to the tensor core
-          mbar_arrive(bar(full_bar + j % nst));
+          mbar_arrive(bar(full_bar + jg % nst));
         }
+        if (is_v && go) q_pending = false;   // its consumer waits for it before the item's products
+        }
+        // after an abort, let a Q load still in flight land
+        if (is_v && q_pending) mbar_wait(bar(PB_Q), q_phase, nullptr);
         cp_async_wait<0>();
       };
       if (is_v)
@@ -304,21 +367,11 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
     } else if (warp == W_MMA) {
       // ------------------------------------------------------------- MMA issuer
       {
-        if (lane == 0) {
-          asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
-          mbar_arrive_expect_tx(bar(PB_Q), 2 * Q_BYTES);
-          for (int hh = 0; hh < 2; ++hh) {
-            tma_load_3d(sbase + OFF_Q + hh * Q_BYTES, &tm_q, bar(PB_Q), 0, h0 + hh, q0);
-            tma_load_3d(sbase + OFF_Q + hh * Q_BYTES + QHALF, &tm_q, bar(PB_Q), 64, h0 + hh, q0);
-          }
-        }
-        __syncwarp();
         constexpr uint32_t idesc_qk = make_idesc(false, BM, BN);
         constexpr uint32_t idesc_pv = make_idesc(true, BM, HD);
-        bool ok = __all_sync(0xffffffffu, wait_or_abort(bar(PB_Q), 0, abort_flag, a.err));
-        // S_h = Q_h K_j^T into the TMEM columns of S_h
-        auto issue_qk = [&](int hh, int j) {
-          const uint32_t kb = sbase + OFF_K + (j % NSK) * KV_TILE;
+        // S_h = Q_h K^T of ring position jg into the TMEM columns of S_h
+        auto issue_qk = [&](int hh, int jg) {
+          const uint32_t kb = sbase + OFF_K + (jg % NSK) * KV_TILE;
           const uint32_t qa = sbase + OFF_Q + hh * Q_BYTES;
 #pragma unroll
           for (int k = 0; k < HD / 16; ++k) {
@@ -328,11 +381,11 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
           }
           commit_e(bar(PB_SF + hh));
         };
-        // O_h += P_h V_j, P_h from TMEM (16 keys = 8 columns per step)
-        // (half 0: keys 0-63, half 1: keys 64-127; O_done is committed after
-        // the last tile only)
-        auto issue_pv = [&](int hh, int j, int half) {
-          const uint32_t vb = sbase + OFF_V + (j % NSV) * KV_TILE;
+        // O_h += P_h V, P_h from TMEM (16 keys = 8 columns per step), for key
+        // tile j of the item at ring position jg (half 0: keys 0-63, half 1:
+        // keys 64-127; O_done is committed after the item's last tile only)
+        auto issue_pv = [&](int hh, int jg, int j, int n_tiles, int half) {
+          const uint32_t vb = sbase + OFF_V + (jg % NSV) * KV_TILE;
 #pragma unroll
           for (int k = half * 4; k < half * 4 + 4; ++k) {
             const uint64_t bd = make_sw128_desc(vb + k * 16 * 128, KHALF, 1024);
@@ -346,40 +399,49 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
         // round.  Q_h K_{j+1}^T rewrites S_h, which holds P_h, right behind
         // P_h V_j: tcgen05.mma operations issued by one thread execute in issue
         // order, so the earlier product has read P_h before the later one
-        // writes there, and no wait for its completion is needed.
+        // writes there, and no wait for its completion is needed.  The same
+        // holds across items, for the next item's first Q K^T and for its first
+        // P V, which overwrites O_h after the softmax warps have read it out.
         // The tensor core queues only a few products ahead of the issuer, so
         // whatever the issuer does between products (waits, commits, fences)
         // can leave it idle.  The loop therefore commits only what a waiter
-        // needs (S_h and V(j) per tile, O_h after the last tile; the softmax
-        // warps release the K stages) and its waits take a fast path.
-        if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(bar(PB_KF + 0), 0, abort_flag, a.err));
-        if (ok) {
+        // needs (S_h and V(j) per tile, O_h after an item's last tile; the
+        // softmax warps release the K stages) and its waits take a fast path.
+        int jg = 0;                        // ring position over all items
+        bool ok = true;
+        for (int it = it_begin; it < it_end && ok; ++it) {
+          const Item w = item_at(it);
+          const int ii = it - it_begin;
+          // this item's Q (loaded by the V producer warp)
+          ok = __all_sync(0xffffffffu, wait_or_abort(bar(PB_Q), ii & 1, abort_flag, a.err));
+          if (!ok) break;
+          ok = __all_sync(0xffffffffu, wait_fast(bar(PB_KF + jg % NSK), (jg / NSK) & 1, abort_flag, a.err));
+          if (!ok) break;
           tc_fence_after();
-          issue_qk(0, 0);
-          issue_qk(1, 0);
-        }
-        for (int j = 0; j < n_tiles && ok; ++j) {
-          const bool more = j + 1 < n_tiles;
-          for (int hh = 0; hh < 2 && ok; ++hh) {
-            ok = __all_sync(0xffffffffu, wait_fast(bar(PB_PF + 2 * hh), j & 1, abort_flag, a.err));
-            if (!ok) break;
-            tc_fence_after();
-            if (hh == 0) ok = __all_sync(0xffffffffu, wait_fast(bar(PB_VF + j % NSV), (j / NSV) & 1, abort_flag, a.err));
-            if (!ok) break;
-            issue_pv(hh, j, 0);
-            ok = __all_sync(0xffffffffu, wait_fast(bar(PB_PF + 2 * hh + 1), j & 1, abort_flag, a.err));
-            if (!ok) break;
-            tc_fence_after();
-            issue_pv(hh, j, 1);
-            if (hh == 1) commit_e(bar(PB_VE + j % NSV));   // V(j) no longer needed
-            if (more) {
-              if (hh == 0) ok = __all_sync(0xffffffffu, wait_fast(bar(PB_KF + (j + 1) % NSK), ((j + 1) / NSK) & 1, abort_flag, a.err));
+          issue_qk(0, jg);
+          issue_qk(1, jg);
+          for (int j = 0; j < w.n_tiles && ok; ++j, ++jg) {
+            const bool more = j + 1 < w.n_tiles;
+            for (int hh = 0; hh < 2 && ok; ++hh) {
+              ok = __all_sync(0xffffffffu, wait_fast(bar(PB_PF + 2 * hh), jg & 1, abort_flag, a.err));
               if (!ok) break;
-              issue_qk(hh, j + 1);
+              tc_fence_after();
+              if (hh == 0) ok = __all_sync(0xffffffffu, wait_fast(bar(PB_VF + jg % NSV), (jg / NSV) & 1, abort_flag, a.err));
+              if (!ok) break;
+              issue_pv(hh, jg, j, w.n_tiles, 0);
+              ok = __all_sync(0xffffffffu, wait_fast(bar(PB_PF + 2 * hh + 1), jg & 1, abort_flag, a.err));
+              if (!ok) break;
+              tc_fence_after();
+              issue_pv(hh, jg, j, w.n_tiles, 1);
+              if (hh == 1) commit_e(bar(PB_VE + jg % NSV));   // V no longer needed
+              if (more) {
+                if (hh == 0) ok = __all_sync(0xffffffffu, wait_fast(bar(PB_KF + (jg + 1) % NSK), ((jg + 1) / NSK) & 1, abort_flag, a.err));
+                if (!ok) break;
+                issue_qk(hh, jg + 1);
+              }
             }
           }
         }
-        if (*abort_flag) mbar_wait(bar(PB_Q), 0, nullptr);  // let the Q loads land
       }
     }
   } else {
@@ -387,17 +449,21 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
     // ------------------------------------------------------------- softmax (head hh)
     const int hh = warp >> 2;               // 0: warps 0-3, 1: warps 4-7
     const int r = tid & 127;                // query row in the tile, TMEM lane
-    const int row_pos = a.prior_len + q0 + r;
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t col_s = COL_S + hh * BN, col_o = COL_O + hh * HD;
     const float sl2 = a.scale * 1.4426950408889634f;
+    int jg = 0;                             // tile position over all items
+    for (int it = it_begin; it < it_end; ++it) {
+    const Item w = item_at(it);
+    const int q0 = w.q0, h0 = w.h0;
+    const int row_pos = a.prior_len + q0 + r;
     float m_run = -INFINITY, l_run = 0.f;   // running max in scaled log2 units
-    for (int j = 0; j < n_tiles; ++j) {
-      wait_fast(bar(PB_SF + hh), j & 1, abort_flag, a.err);
+    for (int j = 0; j < w.n_tiles; ++j, ++jg) {
+      wait_fast(bar(PB_SF + hh), jg & 1, abort_flag, a.err);
       __syncwarp();
       tc_fence_after();
-      // the S_B commit follows both heads' Q K_j^T: K(j) can be refilled
-      if (hh == 1 && lane == 0) mbar_arrive(bar(PB_KE + j % NSK));
+      // the S_B commit follows both heads' Q K^T: this K stage can be refilled
+      if (hh == 1 && lane == 0) mbar_arrive(bar(PB_KE + jg % NSK));
       const int k0 = j * BN;
       const bool diag = k0 + BN - 1 > a.prior_len + q0;   // causal mask needed
       // the whole S row into registers: four loads in flight, one wait
@@ -473,7 +539,7 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
       l_run = l_run * alpha + (sum0 + sum1);
       m_run = m_new;
     }
-    wait_or_abort(bar(PB_OD + hh), 0, abort_flag, a.err);
+    wait_or_abort(bar(PB_OD + hh), (it - it_begin) & 1, abort_flag, a.err);
     __syncwarp();
     tc_fence_after();
     const float inv = 1.f / l_run;
@@ -497,6 +563,7 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
         }
       }
     }
+    }                                       // items
     tc_fence_before();
   }
   __syncthreads();
@@ -513,7 +580,12 @@ bool prefill_pair_supported(int num_q_heads, int num_kv_heads) {
   return (num_q_heads / num_kv_heads) % 2 == 0;
 }
 
-cudaError_t launch_prefill_pair(const PrefillArgs& a, cudaStream_t stream) {
+bool prefill_pair_persistent_ok(const PrefillArgs& a, int ctas) {
+  const int n_items = a.num_q_heads / 2 * ((a.chunk_len + BM - 1) / BM);
+  return n_items <= kMaxItems && ctas >= 1 && ctas <= kMaxCtas;
+}
+
+cudaError_t launch_prefill_pair(const PrefillArgs& a, cudaStream_t stream, int persistent_ctas) {
   PairParams p;
   p.a = a;
   p.total_len = a.prior_len + a.chunk_len;
@@ -527,6 +599,34 @@ cudaError_t launch_prefill_pair(const PrefillArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  const int n_pairs = a.num_q_heads / 2;
+  const int n_items = n_pairs * p.q_tiles;
+  const int P = persistent_ctas < n_items ? persistent_ctas : n_items;
+  p.n_list = 0;
+  if (persistent_ctas > 0 && n_items <= kMaxItems && P <= kMaxCtas) {
+    // greedy longest-first assignment of the items to P persistent CTAs
+    std::vector<std::vector<int>> per(P);
+    std::priority_queue<std::pair<long, int>, std::vector<std::pair<long, int>>, std::greater<>> heap;
+    for (int c = 0; c < P; ++c) heap.push({0, c});
+    for (int qt = p.q_tiles - 1; qt >= 0; --qt) {
+      const int n_tiles = (a.prior_len + std::min(a.chunk_len, qt * BM + BM) - 1) / BN + 1;
+      for (int pr = 0; pr < n_pairs; ++pr) {
+        auto top = heap.top();
+        heap.pop();
+        per[top.second].push_back(qt * n_pairs + pr);
+        heap.push({top.first + n_tiles, top.second});
+      }
+    }
+    int k = 0;
+    for (int c = 0; c < P; ++c) {
+      p.start[c] = (uint16_t)k;
+      for (int item : per[c]) p.list[k++] = (uint16_t)item;
+    }
+    p.start[P] = (uint16_t)k;
+    p.n_list = n_items;
+    prefill_pair_kernel<<<P, kThreadsPair, SMEM_BYTES, stream>>>(p, tm_q);
+    return cudaGetLastError();
+  }
   dim3 grid(a.num_q_heads / 2, p.q_tiles);
   prefill_pair_kernel<<<grid, kThreadsPair, SMEM_BYTES, stream>>>(p, tm_q);
   return cudaGetLastError();

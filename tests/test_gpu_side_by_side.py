@@ -1,0 +1,132 @@
+"""One layer's decode and a prompt chunk's prefill run side by side on
+disjoint SMs (pkv_decode_prefill_attention): the prefill as persistent CTAs on
+prefill_sms SMs, the decode (with its fused append) on the rest.  The results
+must equal, bit for bit, those of the two calls made one after the other
+(kv_append of the chunk, paged_decode_attention_append, chunked_prefill), and
+stay within the bf16 tolerance of the oracle."""
+import pytest
+import torch
+
+import gpu_cases as G
+import oracle
+from paged_kv_cache_104_gb300 import binding as B
+from paged_kv_cache_104_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _bits(t):
+    return t.detach().cpu().view(torch.int16)
+
+
+def _run_both(w, lay, x, prior, prefill_sms, dev="cuda"):
+    """Serial calls, then the side-by-side call on a second copy of the pools;
+    returns (serial decode, serial prefill, side decode, side prefill, pools)."""
+    nd = lay.num_decode_tokens
+    bt = lay.decode_block_table.to(dev).contiguous()
+    sl = lay.seq_lens.to(dev)
+    msl = int(lay.seq_lens.max())
+    bt_pre = lay.block_table[lay.prefill_row].to(dev).contiguous()
+    q_dec, q_pre = x.q_decode.to(dev), x.q_prefill.to(dev)
+    k_dec, v_dec = x.k_new[:nd].to(dev), x.v_new[:nd].to(dev)
+    k_pre, v_pre = x.k_new[nd:].to(dev), x.v_new[nd:].to(dev)
+    slot_pre = lay.slot_mapping[nd:].to(dev)
+    ws = B.decode_workspace(nd, w.num_q_heads, w.head_dim, msl, device=dev)
+    outs = []
+    pools = []
+    for side in (False, True):
+        kc, vc = x.k_cache.to(dev), x.v_cache.to(dev)
+        B.kv_append(k_pre, v_pre, kc, vc, slot_pre)
+        od, op = torch.empty_like(q_dec), torch.empty_like(q_pre)
+        if side:
+            B.decode_prefill_attention(od, q_dec, k_dec, v_dec, kc, vc, bt, sl, msl, op, q_pre, bt_pre,
+                                       prior, w.scale, ws, prefill_sms=prefill_sms)
+        else:
+            B.paged_decode_attention_append(od, q_dec, k_dec, v_dec, kc, vc, bt, sl, msl, w.scale, ws)
+            B.chunked_prefill_attention(op, q_pre, kc, vc, bt_pre, prior, w.scale)
+        torch.cuda.synchronize()
+        assert B.get_device_error() == 0
+        outs += [od, op]
+        pools.append((kc, vc))
+    return outs, pools
+
+
+@pytest.mark.parametrize("prefill_sms", [8, 40, 100])
+def test_side_by_side_equals_serial_and_oracle(prefill_sms):
+    w = G.custom_workload(torch.bfloat16, 32, 8, 128, seed=91)
+    lens = [1, 17, 300, 512, 513, 1500, 2600, 4097]
+    lay = W.make_layout(w, seq_lens_after=lens, prefill=(700, 600))
+    x = W.draw_layer(w, lay, 0)
+    (sd, sp, bd, bp), pools = _run_both(w, lay, x, 700, prefill_sms)
+    assert torch.equal(_bits(sd), _bits(bd)), "decode differs from the serial calls"
+    assert torch.equal(_bits(sp), _bits(bp)), "prefill differs from the serial calls"
+    (k1, v1), (k2, v2) = pools
+    assert torch.equal(_bits(k1), _bits(k2)) and torch.equal(_bits(v1), _bits(v2))
+    rk, rv = G.oracle_append(lay, x)
+    ref_d = oracle.paged_decode(x.q_decode, rk, rv, lay.decode_block_table, lay.seq_lens, w.scale)
+    ref_p = oracle.chunked_prefill(x.q_prefill, rk, rv, lay.block_table[lay.prefill_row], 700,
+                                   w.scale)
+    assert G.max_err(bd, ref_d) <= 2e-2
+    assert G.max_err(bp, ref_p) <= 2e-2
+
+
+def test_side_by_side_full_size_layer():
+    """The ragged 128-sequence batch with its 2,048-token chunk over 4,096
+    cached tokens, 40 SMs for the prefill: equal to the serial calls."""
+    w = W.WORKLOADS["ragged_prefill"]
+    lay = W.make_layout(w)
+    x = W.draw_layer(w, lay, 0)
+    (sd, sp, bd, bp), _ = _run_both(w, lay, x, w.prefill_prior, 40)
+    assert torch.equal(_bits(sd), _bits(bd))
+    assert torch.equal(_bits(sp), _bits(bp))
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (4, 4)])
+def test_side_by_side_falls_back_to_serial(hq, hkv):
+    """A GQA group of 1 has no two-head prefill: the call runs the two halves
+    one after the other, with the same results."""
+    w = G.custom_workload(torch.bfloat16, hq, hkv, 128, seed=92)
+    lay = W.make_layout(w, seq_lens_after=[5, 700, 1300], prefill=(130, 250))
+    x = W.draw_layer(w, lay, 0)
+    (sd, sp, bd, bp), _ = _run_both(w, lay, x, 130, 16)
+    assert torch.equal(_bits(sd), _bits(bd)) and torch.equal(_bits(sp), _bits(bp))
+
+
+def test_side_by_side_too_many_work_items_runs_serial():
+    """514 work items (257 query tiles x 2 head pairs) exceed the persistent
+    list: serial, same results."""
+    w = G.custom_workload(torch.bfloat16, 4, 2, 128, seed=94)
+    lay = W.make_layout(w, seq_lens_after=[9, 2000], prefill=(0, 257 * 128))
+    x = W.draw_layer(w, lay, 0)
+    (sd, sp, bd, bp), _ = _run_both(w, lay, x, 0, 20)
+    assert torch.equal(_bits(sd), _bits(bd)) and torch.equal(_bits(sp), _bits(bp))
+
+
+def test_side_by_side_prefill_sms_at_or_above_the_gpu():
+    """prefill_sms at the SM count leaves nothing for the decode: serial."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    w = G.custom_workload(torch.bfloat16, 8, 2, 128, seed=93)
+    lay = W.make_layout(w, seq_lens_after=[40, 900], prefill=(0, 300))
+    x = W.draw_layer(w, lay, 0)
+    (sd, sp, bd, bp), _ = _run_both(w, lay, x, 0, sms)
+    assert torch.equal(_bits(sd), _bits(bd)) and torch.equal(_bits(sp), _bits(bp))
+
+
+def test_side_by_side_rejects_fp32_and_bad_split():
+    w = G.custom_workload(torch.float32, 4, 2, 128)
+    lay = W.make_layout(w, seq_lens_after=[3], prefill=(0, 20))
+    x = W.draw_layer(w, lay, 0)
+    kc, vc = x.k_cache.cuda(), x.v_cache.cuda()
+    bt = lay.decode_block_table.cuda().contiguous()
+    ws = B.decode_workspace(1, 4, 128, 3)
+    with pytest.raises(B.PagedKVError):
+        B.decode_prefill_attention(torch.empty_like(x.q_decode).cuda(), x.q_decode.cuda(),
+                                   x.k_new[:1].cuda(), x.v_new[:1].cuda(), kc, vc, bt,
+                                   lay.seq_lens.cuda(), 3, torch.empty_like(x.q_prefill).cuda(),
+                                   x.q_prefill.cuda(), lay.block_table[lay.prefill_row].cuda(), 0,
+                                   w.scale, ws, prefill_sms=8)
+    w = G.custom_workload(torch.bfloat16, 4, 2, 128)
+    lay = W.make_layout(w, seq_lens_after=[3], prefill=(0, 20))
+    x = W.draw_layer(w, lay, 0)
+    with pytest.raises(B.PagedKVError):
+        _run_both(w, lay, x, 0, -1)
