@@ -53,6 +53,17 @@
 //                     tcgen05 instruction.  Issuing from a lone lane inside a
 //                     divergent branch starved the tensor core: the same
 //                     instruction stream ran about 25% slower.
+// Work items.  One item is 128 query rows x the two heads; by default each
+// CTA runs one item (heaviest first).  In persistent mode a chosen number of
+// CTAs each run a host-assigned list of items (longest first, greedy), so the
+// prefill holds exactly that many SMs: the decode of the same layer is then
+// launched as a programmatic dependent and runs on the other SMs at the same
+// time.  Rings, barrier phases and TMEM carry over from item to item: the
+// next item's first Q K^T and P V follow the previous item's last products in
+// issue order, and the softmax warps read the previous O out before they
+// hand over the next item's first P.  Each item's Q is loaded once the
+// previous item's Q K^T are done (the first by the MMA warp at once, the
+// rest by the V producer).
 // Every mbarrier wait is bounded; on time-out the kernel records an error,
 // stops issuing work, lets its copies land, frees its TMEM and returns.
 #include <cuda.h>
@@ -295,17 +306,16 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
         int jg = 0;                            // ring position over all items
         bool go = true, q_pending = false;
         uint32_t q_phase = 0;
-        if (is_v && lane == 0)
-          asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
         for (int it = it_begin; it < it_end && go; ++it) {
         const Item w = item_at(it);
         if (is_v) {
-          // the item's Q, once the previous item's last Q_B K^T has read the buffer
+          // the item's Q (after the first), once the previous item's last
+          // Q_B K^T has read the buffer
           const int ii = it - it_begin;
           if (ii > 0) go = wait_or_abort(bar(PB_SF + 1), (jg - 1) & 1, abort_flag, a.err);
           go = __all_sync(0xffffffffu, go && !*abort_flag);
           if (!go) break;
-          if (lane == 0) {
+          if (lane == 0 && ii > 0) {
             mbar_arrive_expect_tx(bar(PB_Q), 2 * Q_BYTES);
             for (int hh = 0; hh < 2; ++hh) {
               tma_load_3d(sbase + OFF_Q + hh * Q_BYTES, &tm_q, bar(PB_Q), 0, w.h0 + hh, w.q0);
@@ -313,8 +323,10 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
             }
           }
           __syncwarp();
-          q_pending = true;
-          q_phase = ii & 1;
+          if (ii > 0) {
+            q_pending = true;
+            q_phase = ii & 1;
+          }
         }
         int cur_ids = load_ids(0), next_ids = load_ids(1);
         for (int j = 0; j < w.n_tiles; ++j, ++jg) {
@@ -367,6 +379,19 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
     } else if (warp == W_MMA) {
       // ------------------------------------------------------------- MMA issuer
       {
+        // the first item's Q, at once (the V producer loads the later ones
+        // as their buffer frees up); issuing it here, first thing, measured
+        // 3% faster than from the V producer warp
+        if (lane == 0) {
+          asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
+          const Item w0 = item_at(it_begin);
+          mbar_arrive_expect_tx(bar(PB_Q), 2 * Q_BYTES);
+          for (int hh = 0; hh < 2; ++hh) {
+            tma_load_3d(sbase + OFF_Q + hh * Q_BYTES, &tm_q, bar(PB_Q), 0, w0.h0 + hh, w0.q0);
+            tma_load_3d(sbase + OFF_Q + hh * Q_BYTES + QHALF, &tm_q, bar(PB_Q), 64, w0.h0 + hh, w0.q0);
+          }
+        }
+        __syncwarp();
         constexpr uint32_t idesc_qk = make_idesc(false, BM, BN);
         constexpr uint32_t idesc_pv = make_idesc(true, BM, HD);
         // S_h = Q_h K^T of ring position jg into the TMEM columns of S_h
@@ -408,13 +433,14 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
         // needs (S_h and V(j) per tile, O_h after an item's last tile; the
         // softmax warps release the K stages) and its waits take a fast path.
         int jg = 0;                        // ring position over all items
-        bool ok = true;
+        bool ok = true, q0_landed = false;
         for (int it = it_begin; it < it_end && ok; ++it) {
           const Item w = item_at(it);
           const int ii = it - it_begin;
-          // this item's Q (loaded by the V producer warp)
+          // this item's Q
           ok = __all_sync(0xffffffffu, wait_or_abort(bar(PB_Q), ii & 1, abort_flag, a.err));
           if (!ok) break;
+          q0_landed = true;
           ok = __all_sync(0xffffffffu, wait_fast(bar(PB_KF + jg % NSK), (jg / NSK) & 1, abort_flag, a.err));
           if (!ok) break;
           tc_fence_after();
@@ -442,6 +468,8 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
             }
           }
         }
+        // after an abort, let the first item's Q load (issued above) land
+        if (!q0_landed) mbar_wait(bar(PB_Q), 0, nullptr);
       }
     }
   } else {
