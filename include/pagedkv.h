@@ -226,11 +226,11 @@ pkv_status pkv_chunked_prefill_attention(void *out, const void *q, const void *k
  *                the batch (the decode's cache bytes) and the chunk.
  * Results are those of the two calls made one after the other (bit for bit).
  * Both halves are checked before either is launched.  When the prefill
- * cannot run as persistent tensor-core CTAs (not bf16 with head_dim 128, an
- * odd GQA group, more than 512 work items -- 128-row query tiles times half
- * the query heads -- or prefill_sms not below the SM count), the two run one
- * after the other instead.  bf16 with head_dim 128 only for the decode
- * (PKV_EUNSUPPORTED otherwise).
+ * cannot run as persistent tensor-core CTAs (not bf16 with head_dim 128, more
+ * than 512 work items -- a work item is 128 query rows of two heads of one KV
+ * head, or 256 rows of one head when the GQA group is odd -- or prefill_sms
+ * not below the SM count), the two run one after the other instead.  bf16
+ * with head_dim 128 only for the decode (PKV_EUNSUPPORTED otherwise).
  */
 typedef struct pkv_decode_prefill_args {
   void *decode_out;

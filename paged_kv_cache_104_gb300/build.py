@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpagedkv.so")
 SOURCES = ["abi.cu", "append.cu", "decode.cu", "decode_fp8.cu", "decode_mla.cu", "decode_mma.cu", "gemm_heads.cu", "decode_noalloc.cu",
-           "prefill_pair.cu", "prefill_tc.cu", "prefix_cache.cpp", "tmap.cu"]
+           "prefill_pair.cu", "prefix_cache.cpp", "tmap.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

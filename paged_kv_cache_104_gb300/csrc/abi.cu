@@ -258,10 +258,7 @@ pkv_status prefill_launch(void* out, const void* q, const void* k_cache, const v
   if (dtype == PKV_BF16 && head_dim == 128) {
     pkv::PrefillArgs a{out, q, k_cache, v_cache, block_table_row, max_blocks, prior_len, chunk_len,
                        num_blocks, num_q_heads, num_kv_heads, scale, err};
-    const cudaError_t e = pkv::prefill_pair_supported(num_q_heads, num_kv_heads)
-                              ? pkv::launch_prefill_pair(a, s, persistent_ctas)
-                              : pkv::launch_prefill_tc(a, sms, s);
-    return e == cudaSuccess ? PKV_OK : PKV_ECUDA;
+    return pkv::launch_prefill_pair(a, s, persistent_ctas) == cudaSuccess ? PKV_OK : PKV_ECUDA;
   }
   // CUDA-core path: every chunk row is one query over its causal prefix, run
   // as a single split so no workspace is needed.
@@ -565,9 +562,8 @@ pkv_status pkv_decode_prefill_attention(const pkv_decode_prefill_args* x, pkv_st
                       x->prefill_max_blocks, x->prior_len, x->chunk_len, x->num_blocks,
                       x->num_q_heads, x->num_kv_heads, x->scale, err};
   const bool side_by_side = x->chunk_len > 0 && d.num_seqs > 0 && x->head_dim == 128 &&
-                            x->dtype == PKV_BF16 &&
-                            pkv::prefill_pair_supported(x->num_q_heads, x->num_kv_heads) &&
-                            p_sms < sms && pkv::prefill_pair_persistent_ok(pa, p_sms);
+                            x->dtype == PKV_BF16 && p_sms < sms &&
+                            pkv::prefill_pair_persistent_ok(pa, p_sms);
   if (!side_by_side) {   // one after the other, each on the whole GPU
     if (x->chunk_len > 0) {
       st = prefill_launch(x->prefill_out, x->prefill_q, x->k_cache, x->v_cache,

@@ -112,14 +112,13 @@ struct PrefillArgs {
   float scale;
   int* err;
 };
-// tcgen05 path, one query head per CTA: bf16, head_dim 128, block_size 16.
-cudaError_t launch_prefill_tc(const PrefillArgs& a, int num_sms, cudaStream_t stream);
-// tcgen05 path, two query heads of one GQA group per CTA (group size even).
+// tcgen05 path (bf16, head_dim 128, block_size 16): two streams of 128 query
+// rows per CTA sharing each K/V tile -- two query heads of one KV head when
+// the GQA group is even, else two consecutive query tiles of one head.
 // persistent_ctas > 0: that many persistent CTAs run the work items (query
 // tile x head pair), assigned longest first, and each signals at its start
 // that a programmatically dependent launch may begin (so a kernel launched
 // next with that attribute runs on the remaining SMs); 0: one CTA per item.
-bool prefill_pair_supported(int num_q_heads, int num_kv_heads);
 bool prefill_pair_persistent_ok(const PrefillArgs& a, int ctas);
 cudaError_t launch_prefill_pair(const PrefillArgs& a, cudaStream_t stream, int persistent_ctas = 0);
 

@@ -130,6 +130,11 @@ struct PairParams {
   int total_len;
   int kv_rows;
   int q_tiles;
+  // The CTA's two streams ("heads" A and B below): two query heads of one KV
+  // head over the same 128 query rows (rows_mode 0, the GQA group even), or
+  // one head over two consecutive 128-row query tiles (rows_mode 1, any
+  // group).  Either way every K/V tile feeds both.
+  int rows_mode;
   // Persistent mode (n_list > 0): CTA c runs the work items
   // list[start[c]] .. list[start[c + 1] - 1] one after the other, item =
   // query tile * (heads / 2) + head pair, assigned by the host.  Otherwise
@@ -154,42 +159,6 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// tcgen05 issue from a converged warp: one elected lane issues, every lane
-// computes the same (uniform) descriptors
-__device__ __forceinline__ void mma_ss_e(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
-}
-__device__ __forceinline__ void mma_ts_e(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
-}
-__device__ __forceinline__ void commit_e(uint32_t bar) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
-      : "memory");
-}
-
-// three-input maximum (one instruction on sm_100 and later)
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-
-// wait with a fast path: a phase that is already complete costs one
-// try_wait; otherwise the bounded, abort-aware wait
-__device__ __forceinline__ bool wait_fast(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err) {
-  if (mbar_try_wait(bar, parity)) return true;
-  return wait_or_abort(bar, parity, abort_flag, err);
-}
 
 __global__ void __launch_bounds__(kThreadsPair, 1)
 prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant__ CUtensorMap tm_q) {
@@ -208,29 +177,39 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int group = a.num_q_heads / a.num_kv_heads;
-  const int n_pairs = a.num_q_heads / 2;
+  // items: x * ... + t with x the head pair (rows_mode 0) or the head
+  // (rows_mode 1) and t the query tile or tile pair
+  const int n_x = p.rows_mode ? a.num_q_heads : a.num_q_heads / 2;
+  const int n_t = p.rows_mode ? (p.q_tiles + 1) / 2 : p.q_tiles;
   const int it_begin = p.n_list > 0 ? p.start[blockIdx.x] : 0;
   const int it_end = p.n_list > 0 ? p.start[blockIdx.x + 1] : 1;
-  // work item it: heads h0, h0 + 1 (KV head g), query rows q0 .. q0 + 127,
-  // key tiles 0 .. n_tiles - 1
+  // work item it: stream hh covers head[hh], query rows qrow[hh] ..
+  // qrow[hh] + 127; both read KV head g, key tiles 0 .. n_tiles - 1
   struct Item {
-    int h0, g, q0, n_tiles;
+    int head[2], qrow[2], g, n_tiles;
   };
   auto item_at = [&](int it) {
-    int pair, qt;
+    int x, tq;
     if (p.n_list > 0) {
       const int item = p.list[it];
-      pair = item % n_pairs;
-      qt = item / n_pairs;
+      x = item % n_x;
+      tq = item / n_x;
     } else {
-      pair = blockIdx.x;
-      qt = p.q_tiles - 1 - (int)blockIdx.y;               // heaviest tiles first
+      x = blockIdx.x;
+      tq = n_t - 1 - (int)blockIdx.y;                     // heaviest tiles first
     }
     Item w;
-    w.h0 = 2 * pair;
-    w.g = w.h0 / group;
-    w.q0 = qt * BM;
-    w.n_tiles = (a.prior_len + min(a.chunk_len, w.q0 + BM) - 1) / BN + 1;
+    if (p.rows_mode) {
+      w.head[0] = w.head[1] = x;
+      w.qrow[0] = 2 * tq * BM;
+      w.qrow[1] = w.qrow[0] + BM;
+    } else {
+      w.head[0] = 2 * x;
+      w.head[1] = 2 * x + 1;
+      w.qrow[0] = w.qrow[1] = tq * BM;
+    }
+    w.g = w.head[0] / group;
+    w.n_tiles = (a.prior_len + min(a.chunk_len, w.qrow[1] + BM) - 1) / BN + 1;
     return w;
   };
 
@@ -318,8 +297,8 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
           if (lane == 0 && ii > 0) {
             mbar_arrive_expect_tx(bar(PB_Q), 2 * Q_BYTES);
             for (int hh = 0; hh < 2; ++hh) {
-              tma_load_3d(sbase + OFF_Q + hh * Q_BYTES, &tm_q, bar(PB_Q), 0, w.h0 + hh, w.q0);
-              tma_load_3d(sbase + OFF_Q + hh * Q_BYTES + QHALF, &tm_q, bar(PB_Q), 64, w.h0 + hh, w.q0);
+              tma_load_3d(sbase + OFF_Q + hh * Q_BYTES, &tm_q, bar(PB_Q), 0, w.head[hh], w.qrow[hh]);
+              tma_load_3d(sbase + OFF_Q + hh * Q_BYTES + QHALF, &tm_q, bar(PB_Q), 64, w.head[hh], w.qrow[hh]);
             }
           }
           __syncwarp();
@@ -387,8 +366,8 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
           const Item w0 = item_at(it_begin);
           mbar_arrive_expect_tx(bar(PB_Q), 2 * Q_BYTES);
           for (int hh = 0; hh < 2; ++hh) {
-            tma_load_3d(sbase + OFF_Q + hh * Q_BYTES, &tm_q, bar(PB_Q), 0, w0.h0 + hh, w0.q0);
-            tma_load_3d(sbase + OFF_Q + hh * Q_BYTES + QHALF, &tm_q, bar(PB_Q), 64, w0.h0 + hh, w0.q0);
+            tma_load_3d(sbase + OFF_Q + hh * Q_BYTES, &tm_q, bar(PB_Q), 0, w0.head[hh], w0.qrow[hh]);
+            tma_load_3d(sbase + OFF_Q + hh * Q_BYTES + QHALF, &tm_q, bar(PB_Q), 64, w0.head[hh], w0.qrow[hh]);
           }
         }
         __syncwarp();
@@ -483,7 +462,7 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
     int jg = 0;                             // tile position over all items
     for (int it = it_begin; it < it_end; ++it) {
     const Item w = item_at(it);
-    const int q0 = w.q0, h0 = w.h0;
+    const int q0 = w.qrow[hh], head = w.head[hh];
     const int row_pos = a.prior_len + q0 + r;
     float m_run = -INFINITY, l_run = 0.f;   // running max in scaled log2 units
     for (int j = 0; j < w.n_tiles; ++j, ++jg) {
@@ -573,7 +552,7 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
     const float inv = 1.f / l_run;
     const bool row_ok = (q0 + r) < a.chunk_len;
     __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
-                          ((int64_t)(q0 + r) * a.num_q_heads + h0 + hh) * HD;
+                          ((int64_t)(q0 + r) * a.num_q_heads + head) * HD;
 #pragma unroll 1
     for (int c = 0; c < HD / 32; ++c) {
       float o[32];
@@ -604,13 +583,17 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
 
 }  // namespace
 
-bool prefill_pair_supported(int num_q_heads, int num_kv_heads) {
-  return (num_q_heads / num_kv_heads) % 2 == 0;
+namespace {
+// rows mode (two query tiles of one head per CTA) unless the group is even
+bool rows_mode_for(const PrefillArgs& a) { return (a.num_q_heads / a.num_kv_heads) % 2 != 0; }
+int items_for(const PrefillArgs& a) {
+  const int q_tiles = (a.chunk_len + BM - 1) / BM;
+  return rows_mode_for(a) ? a.num_q_heads * ((q_tiles + 1) / 2) : a.num_q_heads / 2 * q_tiles;
 }
+}  // namespace
 
 bool prefill_pair_persistent_ok(const PrefillArgs& a, int ctas) {
-  const int n_items = a.num_q_heads / 2 * ((a.chunk_len + BM - 1) / BM);
-  return n_items <= kMaxItems && ctas >= 1 && ctas <= kMaxCtas;
+  return items_for(a) <= kMaxItems && ctas >= 1 && ctas <= kMaxCtas;
 }
 
 cudaError_t launch_prefill_pair(const PrefillArgs& a, cudaStream_t stream, int persistent_ctas) {
@@ -627,8 +610,10 @@ cudaError_t launch_prefill_pair(const PrefillArgs& a, cudaStream_t stream, int p
   cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const int n_pairs = a.num_q_heads / 2;
-  const int n_items = n_pairs * p.q_tiles;
+  p.rows_mode = rows_mode_for(a) ? 1 : 0;
+  const int n_x = p.rows_mode ? a.num_q_heads : a.num_q_heads / 2;
+  const int n_t = p.rows_mode ? (p.q_tiles + 1) / 2 : p.q_tiles;
+  const int n_items = items_for(a);
   const int P = persistent_ctas < n_items ? persistent_ctas : n_items;
   p.n_list = 0;
   if (persistent_ctas > 0 && n_items <= kMaxItems && P <= kMaxCtas) {
@@ -636,12 +621,13 @@ cudaError_t launch_prefill_pair(const PrefillArgs& a, cudaStream_t stream, int p
     std::vector<std::vector<int>> per(P);
     std::priority_queue<std::pair<long, int>, std::vector<std::pair<long, int>>, std::greater<>> heap;
     for (int c = 0; c < P; ++c) heap.push({0, c});
-    for (int qt = p.q_tiles - 1; qt >= 0; --qt) {
-      const int n_tiles = (a.prior_len + std::min(a.chunk_len, qt * BM + BM) - 1) / BN + 1;
-      for (int pr = 0; pr < n_pairs; ++pr) {
+    for (int tq = n_t - 1; tq >= 0; --tq) {
+      const int last_row = p.rows_mode ? (2 * tq + 2) * BM : (tq + 1) * BM;
+      const int n_tiles = (a.prior_len + std::min(a.chunk_len, last_row) - 1) / BN + 1;
+      for (int x = 0; x < n_x; ++x) {
         auto top = heap.top();
         heap.pop();
-        per[top.second].push_back(qt * n_pairs + pr);
+        per[top.second].push_back(tq * n_x + x);
         heap.push({top.first + n_tiles, top.second});
       }
     }
@@ -655,7 +641,7 @@ cudaError_t launch_prefill_pair(const PrefillArgs& a, cudaStream_t stream, int p
     prefill_pair_kernel<<<P, kThreadsPair, SMEM_BYTES, stream>>>(p, tm_q);
     return cudaGetLastError();
   }
-  dim3 grid(a.num_q_heads / 2, p.q_tiles);
+  dim3 grid(n_x, n_t);
   prefill_pair_kernel<<<grid, kThreadsPair, SMEM_BYTES, stream>>>(p, tm_q);
   return cudaGetLastError();
 }

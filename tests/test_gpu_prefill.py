@@ -41,9 +41,11 @@ def test_prefill_tcgen05_small_heads(prior, chunk):
     assert G.max_err(got, ref) <= 2e-2
 
 
-@pytest.mark.parametrize("prior,chunk", [(0, 200), (100, 300), (37, 513)])
-def test_prefill_tcgen05_one_head_per_cta(prior, chunk):
-    """Group size 1 (no pair of heads shares a KV head): one query head per CTA."""
+@pytest.mark.parametrize("prior,chunk", [(0, 200), (100, 300), (37, 513), (0, 128)])
+def test_prefill_tcgen05_query_tile_pairs(prior, chunk):
+    """Group size 1 (no pair of heads shares a KV head): each CTA takes two
+    consecutive query tiles of one head; an odd tile count leaves the last
+    CTA's second tile past the chunk (chunk 200, 513 and 128)."""
     got, ref = _prefill_case(torch.bfloat16, 4, 4, 128, prior, chunk)
     assert torch.isfinite(got).all()
     assert G.max_err(got, ref) <= 2e-2

@@ -82,9 +82,9 @@ def test_side_by_side_full_size_layer():
 
 
 @pytest.mark.parametrize("hq,hkv", [(8, 8), (4, 4)])
-def test_side_by_side_falls_back_to_serial(hq, hkv):
-    """A GQA group of 1 has no two-head prefill: the call runs the two halves
-    one after the other, with the same results."""
+def test_side_by_side_group_of_one(hq, hkv):
+    """A GQA group of 1: the prefill pairs query tiles of one head instead of
+    heads; still equal to the serial calls."""
     w = G.custom_workload(torch.bfloat16, hq, hkv, 128, seed=92)
     lay = W.make_layout(w, seq_lens_after=[5, 700, 1300], prefill=(130, 250))
     x = W.draw_layer(w, lay, 0)
