@@ -579,7 +579,10 @@ def run_ours(args, w, lay, acct):
         # GPU has to stream the cache, the prefill's time falls with its SMs
         nsm = torch.cuda.get_device_properties(dev).multi_processor_count
         trials = {}
-        for cand in sorted({max(4, nsm * f // 64) for f in (8, 10, 12, 14, 16, 18, 20, 24)}):
+
+        def trial(cand):
+            if cand in trials or not 1 <= cand < nsm:
+                return
             split["prefill_sms"] = cand
             step()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -588,6 +591,13 @@ def run_ours(args, w, lay, acct):
             e1.record(stream)
             torch.cuda.synchronize(dev)
             trials[cand] = e0.elapsed_time(e1)
+
+        # a coarse sweep, then every count within 3 of the best one
+        for cand in sorted({max(4, nsm * f // 64) for f in (8, 10, 12, 14, 16, 18, 20, 24)}):
+            trial(cand)
+        best = min(trials, key=trials.get)
+        for cand in range(best - 3, best + 4):
+            trial(cand)
         split["prefill_sms"] = min(trials, key=trials.get)
         split["trials_ms"] = {str(k): round(v, 3) for k, v in sorted(trials.items())}
     for _ in range(args.warmup):
