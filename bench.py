@@ -523,7 +523,7 @@ def run_ours(args, w, lay, acct):
     slot_pre = slot[nd:]
     # decode and prefill of a layer side by side on disjoint SMs (the prefill
     # as persistent CTAs on prefill_sms SMs, the decode on the rest)
-    side = bool(args.side_by_side and fused and w.prefill_chunk and hq // hkv % 2 == 0)
+    side = bool(args.side_by_side and fused and w.prefill_chunk)
     split = {"prefill_sms": int(args.prefill_sms)}
 
     def step(ev=None, s=None, serial=False):

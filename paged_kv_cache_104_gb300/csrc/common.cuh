@@ -117,6 +117,31 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// fp32 store carrying an L2 eviction-priority hint.
+__device__ __forceinline__ void st_global_hint(float* dst, float v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(dst), "f"(v), "l"(policy)
+               : "memory");
+}
+
+// Drop one 128-byte L2 line without writing it back: its contents become
+// undefined.  For scratch that is dead once read; line must be 128-byte
+// aligned and hold nothing else that is still live.
+__device__ __forceinline__ void discard_l2_line(const void* line) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(__cvta_generic_to_global(line)) : "memory");
+}
+
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

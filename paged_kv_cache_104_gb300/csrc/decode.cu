@@ -342,10 +342,16 @@ decode_split_kernel(const DecodeArgs a) {
   }
 }
 
-// Merge split partials: one warp per (sequence, query head).
+// Merge split partials: one warp per (sequence, query head).  Launched as the
+// programmatic dependent of the main kernel (its launch overlaps that
+// kernel's tail; its first instruction waits for that grid to complete).
+// The partial rows are dead once merged: when the main kernel kept them in
+// L2 (keep_partials) and they sit on whole 128-byte lines, each line is
+// dropped from L2 after its last read, so they are never written back.
 template <typename T, int D>
 __global__ void __launch_bounds__(256)
 decode_reduce_kernel(const DecodeArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp_global >= a.num_seqs * a.num_q_heads) return;
@@ -374,6 +380,9 @@ decode_reduce_kernel(const DecodeArgs a) {
     // splits at a time) and broadcast, and 8 partial rows are loaded before
     // their FMAs so the L2 latency of the walk over splits overlaps
     const float4* acc4 = reinterpret_cast<const float4*>(a.ws_acc) + base * (D / 4) + lane;
+    // lane 8i reads the first 16 bytes of line i of every 512-byte row
+    const bool drop = a.keep_partials && (reinterpret_cast<uintptr_t>(a.ws_acc) & 127u) == 0 &&
+                      (lane & 7) == 0;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s0 = 0; s0 < ns; s0 += 32) {
       float wl = 0.f;
@@ -395,6 +404,12 @@ decode_reduce_kernel(const DecodeArgs a) {
           o.z = fmaf(wgt, v[i].z, o.z);
           o.w = fmaf(wgt, v[i].w, o.w);
         }
+        // every lane's read of these rows has returned (the FMAs used them)
+        __syncwarp();
+        if (drop) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) discard_l2_line(acc4 + (int64_t)(s0 + k + i) * (D / 4));
+        }
       }
       for (; k < cnt; ++k) {
         const float wgt = __shfl_sync(kFull, wl, k);
@@ -403,6 +418,8 @@ decode_reduce_kernel(const DecodeArgs a) {
         o.y = fmaf(wgt, v.y, o.y);
         o.z = fmaf(wgt, v.z, o.z);
         o.w = fmaf(wgt, v.w, o.w);
+        __syncwarp();
+        if (drop) discard_l2_line(acc4 + (int64_t)(s0 + k) * (D / 4));
       }
     }
     Elem<T>::store(outp + lane * 4 + 0, o.x * inv);
@@ -432,7 +449,19 @@ decode_reduce_kernel(const DecodeArgs a) {
 template <typename T, int D>
 cudaError_t launch_reduce_typed(const DecodeArgs& a, cudaStream_t stream) {
   const int warps = a.num_seqs * a.num_q_heads;
-  decode_reduce_kernel<T, D><<<(warps + 7) / 8, 256, 0, stream>>>(a);
+  if (warps == 0) return cudaSuccess;
+  // programmatic dependent of the main kernel before it in the stream
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((warps + 7) / 8);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_reduce_kernel<T, D>, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -468,6 +468,9 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
     // warp w merges heads w, w + 4, ...: the combine weights once per head,
     // then 4 dims per lane
     const bool direct = (u.ns == 1);
+    // keep_partials: partials stay in L2 (evict-last) until the merge reads
+    // and drops them
+    const uint64_t keep = a.keep_partials ? policy_evict_last() : policy_evict_normal();
     for (int h = warp; h < G; h += kCW) {
       float M = -INFINITY;
 #pragma unroll
@@ -491,7 +494,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
         if (direct)
           outp[row * kHD + d] = __float2bfloat16_rn(O * rl);
         else
-          a.ws_acc[pidx * kHD + d] = O;
+          st_global_hint(a.ws_acc + pidx * kHD + d, O, keep);
       }
       if (!direct && lane == 0) {
         a.ws_ml[pidx * 2 + 0] = M;
@@ -507,8 +510,10 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
 }
 
 template <int G, bool FUSE>
-cudaError_t launch_g(const DecodeArgs& a, int num_sms, cudaStream_t stream, bool dependent) {
+cudaError_t launch_g(const DecodeArgs& args, int num_sms, cudaStream_t stream, bool dependent) {
   using C = MCfg<G>;
+  DecodeArgs a = args;
+  a.keep_partials = dependent ? 0 : 1;
   CUtensorMap tm_k, tm_v;
   const int64_t rows = a.num_blocks * a.num_kv_heads * kBlockSize;
   if (!encode_pool_map_bf16(&tm_k, a.k_cache, rows) || !encode_pool_map_bf16(&tm_v, a.v_cache, rows))

@@ -72,6 +72,12 @@ struct DecodeArgs {
   // fp8 cache only: per-KV-head dequantisation scales [Hkv]
   const float* k_scale;
   const float* v_scale;
+  // 1: the main kernel stores split partials with an L2 evict-last hint and
+  // the merge drops each partial line from L2 once read (no write-back);
+  // 0: plain stores.  Set by the bf16 decode launcher when the decode runs
+  // alone; beside a prefill, whose re-read K/V lives in L2, plain stores
+  // measured faster.
+  int keep_partials;
 };
 // True if (dtype, head_dim, group) has a compiled decode kernel.
 bool decode_supported(int is_bf16, int head_dim, int group);
