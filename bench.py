@@ -373,6 +373,100 @@ def run_fp8_decode(args, w, lay, inputs, dev, stream, dist, n):
     }
 
 
+def run_decode_config(args, name, dev, stream, dist, n):
+    """Time the bf16 decode step of another configuration (no prefill chunk):
+    per layer the fused append + paged decode (main + reduce), every layer
+    with its own pools (as many as fit), one CUDA graph per step, inputs far
+    larger than L2."""
+    from paged_kv_cache_104_gb300 import binding as B
+
+    w = W.WORKLOADS[name]
+    lay = W.make_layout(w)
+    acct = step_accounting(w, lay)
+    L, hq, hkv, d = w.layers, w.num_q_heads, w.num_kv_heads, w.head_dim
+    nd = lay.num_decode_tokens
+    pool_bytes = 2 * lay.num_blocks * hkv * w.block_size * d * w.elem_bytes
+    free, _ = torch.cuda.mem_get_info(dev)
+    n_pools = min(L, max(2, int((free - 8 * 2 ** 30) // max(pool_bytes, 1))))
+    if args.layer_pools > 0:
+        n_pools = min(n_pools, args.layer_pools)
+    xs = [W.draw_layer(w, lay, li + 1000 * dist_env()[1], device=dev, with_pool=li < n_pools)
+          for li in range(L)]
+    pools = [(xs[li].k_cache, xs[li].v_cache) for li in range(n_pools)]
+    bt = lay.decode_block_table.to(dev).contiguous()
+    sl = lay.seq_lens.to(dev)
+    msl = int(lay.seq_lens.max())
+    wsp = B.decode_workspace(nd, hq, d, msl, device=dev)
+    outs = [torch.empty_like(xs[li].q_decode) for li in range(L)]
+
+    def step(ev=None, s=None):
+        s = stream if s is None else s
+        for li in range(L):
+            x = xs[li]
+            kc, vc = pools[li % n_pools]
+            if ev is not None:
+                ev[li][0].record(s)
+            B.paged_decode_attention_append(outs[li], x.q_decode, x.k_new, x.v_new, kc, vc, bt, sl,
+                                            msl, w.scale, wsp, stream=s)
+            if ev is not None:
+                ev[li][1].record(s)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    assert B.get_device_error() == 0, f"device error word set during the {name} warm-up"
+    try:
+        gev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+               for _ in range(L)]
+    except TypeError:
+        gev = None
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            step(gev, s=cap)
+    stream.wait_stream(cap)
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    t0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(dist)
+    ms_step = max_over_ranks(dist, t0.elapsed_time(t1)) / args.steps
+    assert B.get_device_error() == 0, f"device error word set during the {name} steps"
+    if gev is None:
+        gev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(L)]
+        step(gev)
+        torch.cuda.synchronize(dev)
+    dec_ms = sum(gev[li][0].elapsed_time(gev[li][1]) for li in range(L)) / L
+    hbm_peak, _, peak_src = measured_peaks()
+    dec_gbs = acct["decode_bytes_layer"] / (dec_ms / 1e3) / 1e9
+    return {
+        "what": w.description + "; per layer the fused append + paged decode (main + reduce), "
+                "all layers, one CUDA graph",
+        "ms_per_step": ms_step,
+        "value": n * acct["bytes_step"] / (ms_step / 1e3) / 1e9, "unit": "GB/s",
+        "decode_tokens_per_s": n * nd / (ms_step / 1e3),
+        "decode_ms_per_layer": dec_ms,
+        "cached_tokens": int(lay.seq_lens.sum()),
+        "distinct_layer_pools": n_pools, "pool_gb_per_layer": pool_bytes / 1e9,
+        "gpu_launches": args.steps * L * (2 if msl > 512 else 1),
+        "roofline": {
+            "kernel": "paged_decode_attention (split-K main + reduce)", "bound": "hbm",
+            "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": dec_gbs / hbm_peak,
+            "algorithmic_bytes_per_launch": acct["decode_bytes_layer"],
+            "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+            else "fallback 6.8 TB/s",
+        },
+    }
+
+
 def run_mla_decode(args, w, lay, dev, stream, dist, n):
     """Time decode over a latent (MLA-style) cache on the decode batch of the
     workload: per layer latent_append of the decode tokens' latents, then the
@@ -819,6 +913,14 @@ def run_ours(args, w, lay, acct):
         torch.cuda.empty_cache()
         line["mla_decode"] = run_mla_decode(args, w, lay, dev, stream, dist, n)
 
+    # ---- the decode step of the other multi-layer configurations
+    if args.other_configs and w.name == "ragged_prefill":
+        torch.cuda.empty_cache()
+        line["decode_configs"] = {}
+        for name in ("llama8b_decode", "long_context"):
+            line["decode_configs"][name] = run_decode_config(args, name, dev, stream, dist, n)
+            torch.cuda.empty_cache()
+
     # ---- the oracle on this host's cores, bounded sample, rank 0 at N=1 only
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         pools = None
@@ -864,6 +966,9 @@ def main():
     ap.add_argument("--mla-decode", type=int, default=1,
                     help="1: also time decode over a latent (MLA-style) cache (reported under "
                          "mla_decode)")
+    ap.add_argument("--other-configs", type=int, default=1,
+                    help="also time the decode step of the 2,301-token and 32,001-token "
+                         "batches (decode_configs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-decode-seqs", type=int, default=128,
                     help="decode sequences in the oracle sample of cpu_baseline")
