@@ -47,7 +47,32 @@ int max_splits_for(int max_seq_len) {
   return (max_seq_len + pkv::kSplitTokens - 1) / pkv::kSplitTokens;
 }
 
+// Partial slots per (sequence, query head) row: a sequence of n tokens gives
+// at most ceil(n / kSplitTokens) partials in 512-token splits, and at most
+// one more in the bf16 decode's balanced walk (each CTA's share of at least
+// 512 tokens may start inside a sequence).  One slot: no partials at all.
+int partial_slots_for(int max_seq_len) {
+  const int s = max_splits_for(max_seq_len);
+  return s <= 1 ? 1 : s + 1;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// The decode workspace, in order: fp32 partial rows [rows][head_dim], their
+// (m, l) pairs [rows][2], and the partial count per (sequence, head) [count],
+// rows = num_seqs * num_q_heads * partial slots.
+struct Partials {
+  float* acc;
+  float* ml;
+  int* np;
+};
+Partials carve_partials(void* workspace, size_t rows, int head_dim) {
+  char* ws = static_cast<char*>(workspace);
+  const size_t acc_b = align256(rows * head_dim * sizeof(float));
+  const size_t ml_b = align256(rows * 2 * sizeof(float));
+  return {reinterpret_cast<float*>(ws), reinterpret_cast<float*>(ws + acc_b),
+          reinterpret_cast<int*>(ws + acc_b + ml_b)};
+}
 
 // Shape checks shared by decode and prefill.
 pkv_status check_heads(int num_q_heads, int num_kv_heads, int head_dim, int block_size,
@@ -121,10 +146,11 @@ pkv_status pkv_kv_append(const void* k_new, const void* v_new, void* k_cache, vo
 
 size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_seq_len) {
   if (num_seqs < 1 || num_q_heads < 1 || head_dim < 1 || max_seq_len < 1) return 0;
-  const int s = max_splits_for(max_seq_len);
+  const int s = partial_slots_for(max_seq_len);
   if (s <= 1) return 0;
   const size_t rows = (size_t)num_seqs * num_q_heads * s;
-  return align256(rows * head_dim * sizeof(float)) + align256(rows * 2 * sizeof(float));
+  return align256(rows * head_dim * sizeof(float)) + align256(rows * 2 * sizeof(float)) +
+         align256((size_t)num_seqs * num_q_heads * sizeof(int));
 }
 
 }  // extern "C"
@@ -159,12 +185,8 @@ pkv_status decode_prepare(pkv::DecodeArgs* out_args, int* out_sms, void* out, co
   int sms = 0;
   st = device_state(&err, &sms);
   if (st != PKV_OK) return st;
-  const int s = max_splits_for(max_seq_len);
-  const size_t rows = (size_t)num_seqs * num_q_heads * s;
-  float* ws_acc = static_cast<float*>(workspace);
-  float* ws_ml = need ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                                 align256(rows * head_dim * sizeof(float)))
-                      : nullptr;
+  const int s = partial_slots_for(max_seq_len);
+  const Partials part = carve_partials(workspace, (size_t)num_seqs * num_q_heads * s, head_dim);
   pkv::DecodeArgs a{};
   a.out = out;
   a.q = q;
@@ -172,8 +194,9 @@ pkv_status decode_prepare(pkv::DecodeArgs* out_args, int* out_sms, void* out, co
   a.v_cache = v_cache;
   a.block_table = block_table;
   a.seq_lens = seq_lens;
-  a.ws_acc = ws_acc;
-  a.ws_ml = ws_ml;
+  a.ws_acc = need ? part.acc : nullptr;
+  a.ws_ml = need ? part.ml : nullptr;
+  a.ws_np = need ? part.np : nullptr;
   a.err = err;
   a.num_seqs = num_seqs;
   a.bt_stride = max_blocks_per_seq;
@@ -384,8 +407,8 @@ pkv_status pkv_paged_decode_attention_fp8(void* out, const void* q, const void* 
   int sms = 0;
   pkv_status st = device_state(&err, &sms);
   if (st != PKV_OK) return st;
-  const int s = max_splits_for(max_seq_len);
-  const size_t rows = (size_t)num_seqs * num_q_heads * s;
+  const int s = partial_slots_for(max_seq_len);
+  const Partials part = carve_partials(workspace, (size_t)num_seqs * num_q_heads * s, head_dim);
   pkv::DecodeArgs a{};
   a.out = out;
   a.q = q;
@@ -393,10 +416,8 @@ pkv_status pkv_paged_decode_attention_fp8(void* out, const void* q, const void* 
   a.v_cache = v_cache;
   a.block_table = block_table;
   a.seq_lens = seq_lens;
-  a.ws_acc = static_cast<float*>(workspace);
-  a.ws_ml = need ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                            align256(rows * head_dim * sizeof(float)))
-                 : nullptr;
+  a.ws_acc = need ? part.acc : nullptr;
+  a.ws_ml = need ? part.ml : nullptr;
   a.err = err;
   a.num_seqs = num_seqs;
   a.bt_stride = max_blocks_per_seq;
@@ -481,8 +502,8 @@ pkv_status pkv_mla_decode_attention(void* out, const void* q, const void* w_k, c
   if (pkv::launch_gemm_heads(q_lat, q, w_k, num_seqs, num_q_heads, false, s) != cudaSuccess)
     return PKV_ECUDA;
   // 2) z_h = softmax(scale q~_h . C^T) C over the latent pool
-  const int splits = max_splits_for(max_seq_len);
-  const size_t rows = (size_t)num_seqs * num_q_heads * splits;
+  const int splits = partial_slots_for(max_seq_len);
+  const Partials pp = carve_partials(part, (size_t)num_seqs * num_q_heads * splits, rank);
   pkv::DecodeArgs a{};
   a.out = z;
   a.q = q_lat;
@@ -490,8 +511,8 @@ pkv_status pkv_mla_decode_attention(void* out, const void* q, const void* w_k, c
   a.v_cache = c_cache;
   a.block_table = block_table;
   a.seq_lens = seq_lens;
-  a.ws_acc = reinterpret_cast<float*>(part);
-  a.ws_ml = reinterpret_cast<float*>(part + align256(rows * rank * sizeof(float)));
+  a.ws_acc = pp.acc;
+  a.ws_ml = pp.ml;
   a.err = err;
   a.num_seqs = num_seqs;
   a.bt_stride = max_blocks_per_seq;

@@ -359,7 +359,10 @@ decode_reduce_kernel(const DecodeArgs a) {
   const int n = a.chunk_prior >= 0 ? a.chunk_prior + b + 1 : a.seq_lens[b];
   const int limit = min(a.max_seq_len, a.max_blocks_per_seq * kBlockSize);
   if (n < 1 || n > limit) return;  // reported by the main kernel
-  const int ns = (n + a.split_tokens - 1) / a.split_tokens;
+  const int h = warp_global - b * a.num_q_heads;
+  const int ns = a.balanced
+                     ? a.ws_np[b * a.num_kv_heads + h / (a.num_q_heads / a.num_kv_heads)]
+                     : (n + a.split_tokens - 1) / a.split_tokens;
   if (ns <= 1) return;              // written directly by the main kernel
   const int64_t base = (int64_t)warp_global * a.max_splits;
   float M = -INFINITY;

@@ -1,6 +1,8 @@
 // Work planning shared by the decode kernels: a ragged batch becomes a flat
 // list of (sequence, KV head, split) units through a prefix sum of splits
-// per sequence, built in shared memory by every CTA.
+// per sequence, built in shared memory by every CTA.  The bf16 decode can
+// instead walk a balanced plan: the same prefix sum over stages (the
+// kernel's load granule), cut into one equal share of stages per CTA.
 #pragma once
 
 #include "common.cuh"
@@ -17,8 +19,10 @@ __device__ __forceinline__ int row_len(const DecodeArgs& a, int b) {
   return a.chunk_prior >= 0 ? a.chunk_prior + b + 1 : a.seq_lens[b];
 }
 
-// Build cu[0..B] (units per sequence, prefix-summed) with warp 0.
-__device__ __forceinline__ void plan_units(const DecodeArgs& a, int* cu) {
+// Build cu[0..B] with warp 0: per sequence, num_kv_heads times the number of
+// split_tokens-token splits (stage_tok = 0) or of stage_tok-token stages,
+// prefix-summed.
+__device__ __forceinline__ void plan_units(const DecodeArgs& a, int* cu, int stage_tok = 0) {
   const int lane = threadIdx.x & 31;
   constexpr unsigned kAll = 0xffffffffu;
   if (threadIdx.x < 32) {
@@ -33,7 +37,8 @@ __device__ __forceinline__ void plan_units(const DecodeArgs& a, int* cu) {
         if (n < 1 || n > limit) {
           record_error(a.err, DEVERR_SEQLEN_RANGE);
         } else {
-          units = a.num_kv_heads * ((n + a.split_tokens - 1) / a.split_tokens);
+          const int per = stage_tok > 0 ? stage_tok : a.split_tokens;
+          units = a.num_kv_heads * ((n + per - 1) / per);
         }
       }
       int x = units;
@@ -65,6 +70,77 @@ __device__ __forceinline__ Unit find_unit(const DecodeArgs& a, const int* cu, in
   u.tok_begin = u.s * a.split_tokens;
   u.tok_end = min(n, u.tok_begin + a.split_tokens);
   return u;
+}
+
+// Largest b with cu[b] <= w (cu non-decreasing, cu[0] = 0 <= w < cu[B]).
+__device__ __forceinline__ int seq_of(const DecodeArgs& a, const int* cu, int64_t w) {
+  int lo = 0, hi = a.num_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cu[mid] <= w) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// A CTA's walk over its work.  Split walk: units blockIdx.x, + gridDim.x, ...
+// Balanced walk: CTA c takes stages [c S / C, (c + 1) S / C) of the S stages
+// of cu (C = gridDim.x), cut where (sequence, KV head) streams change; each
+// such piece is a unit whose s is its index among the pieces of its stream
+// and ns their number (the CTAs its stages fall to).
+struct Walk {
+  bool balanced;
+  int total;     // units (split walk) or stages (balanced walk)
+  int w;         // split walk: next unit
+  int64_t pos;   // balanced walk: next stage, and the end of this CTA's share
+  int64_t end;
+};
+
+// The balanced walk needs a workspace for the piece counts and at least
+// kMinStagesPerCta stages per CTA (so no stream is cut into more pieces than
+// the workspace has partial slots); otherwise the split walk.
+constexpr int kMinStagesPerCta = kSplitTokens / 64;
+
+// The CTA whose share holds stage p.
+__device__ __forceinline__ int cta_of_stage(int64_t p, int64_t total) {
+  return (int)(((p + 1) * (int64_t)gridDim.x - 1) / total);
+}
+
+__device__ __forceinline__ Walk walk_begin(const DecodeArgs& a, const int* cu, bool balanced) {
+  Walk k;
+  k.balanced = balanced;
+  k.total = cu[a.num_seqs];
+  k.w = blockIdx.x;
+  k.pos = (int64_t)blockIdx.x * k.total / gridDim.x;
+  k.end = (int64_t)(blockIdx.x + 1) * k.total / gridDim.x;
+  return k;
+}
+
+// Next unit of this CTA (false when done).  stage_tok: tokens per stage.
+__device__ __forceinline__ bool walk_next(const DecodeArgs& a, const int* cu, int stage_tok,
+                                          Walk& k, Unit& u) {
+  if (!k.balanced) {
+    if (k.w >= k.total) return false;
+    u = find_unit(a, cu, k.w);
+    k.w += gridDim.x;
+    return true;
+  }
+  if (k.pos >= k.end) return false;
+  const int b = seq_of(a, cu, k.pos);
+  const int nst = (cu[b + 1] - cu[b]) / a.num_kv_heads;   // stages of one stream
+  const int rem = (int)(k.pos - cu[b]);
+  const int g = rem / nst;
+  const int st0 = rem - g * nst;
+  const int64_t s_begin = (int64_t)cu[b] + (int64_t)g * nst, s_end = s_begin + nst;
+  const int len = (int)(min(k.end, s_end) - k.pos);
+  const int c0 = cta_of_stage(s_begin, k.total);
+  u.b = b;
+  u.g = g;
+  u.s = (int)blockIdx.x - c0;
+  u.ns = cta_of_stage(s_end - 1, k.total) - c0 + 1;
+  u.tok_begin = st0 * stage_tok;
+  u.tok_end = min(row_len(a, b), (st0 + len) * stage_tok);
+  k.pos += len;
+  return true;
 }
 
 }  // namespace pkv

@@ -160,9 +160,17 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
     *abort_flag = 0;
     fence_mbar_init();
   }
-  plan_units(a, cu);
+  // balanced walk over 64-token stages when the batch gives every CTA at
+  // least kMinStagesPerCta of them; otherwise 512-token splits
+  plan_units(a, cu, a.balanced ? kStageTok : 0);
   __syncthreads();
-  const int total = cu[a.num_seqs];
+  const bool balanced =
+      a.balanced && (int64_t)cu[a.num_seqs] >= (int64_t)kMinStagesPerCta * gridDim.x;
+  if (a.balanced && !balanced) {
+    __syncthreads();
+    plan_units(a, cu);
+    __syncthreads();
+  }
   volatile int* vabort = abort_flag;
 
   if (warp == kCW) {
@@ -174,8 +182,9 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
     const uint64_t policy = policy_evict_first();
     uint32_t issued = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-      const Unit u = find_unit(a, cu, w);
+    Walk wk = walk_begin(a, cu, balanced);
+    Unit u;
+    while (ok && walk_next(a, cu, kStageTok, wk, u)) {
       const int blk0 = u.tok_begin / kBlockSize;
       const int nblk = (u.tok_end - 1) / kBlockSize - blk0 + 1;
       const int32_t* bt_row = a.block_table + (int64_t)u.b * a.bt_stride + blk0;
@@ -245,9 +254,12 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
   const int vhalf = g >> 2;
   uint32_t consumed = 0;
 
-  for (int w = blockIdx.x; w < total; w += gridDim.x) {
-    const Unit u = find_unit(a, cu, w);
+  Walk wk = walk_begin(a, cu, balanced);
+  Unit u;
+  while (walk_next(a, cu, kStageTok, wk, u)) {
     const int hq0 = u.g * G;
+    // the merge reads how many partials this (sequence, KV head) left
+    if (a.balanced && u.s == 0 && tid == 0) a.ws_np[u.b * a.num_kv_heads + u.g] = u.ns;
     // Q^T as B fragments of head 8nt + g, in the lane's K order
     uint4 qf[NT][4];
 #pragma unroll
@@ -514,6 +526,9 @@ cudaError_t launch_g(const DecodeArgs& args, int num_sms, cudaStream_t stream, b
   using C = MCfg<G>;
   DecodeArgs a = args;
   a.keep_partials = dependent ? 0 : 1;
+  // the balanced walk when the decode has the GPU to itself; beside a
+  // prefill the 512-token splits measured faster
+  a.balanced = a.ws_np != nullptr && !dependent;
   CUtensorMap tm_k, tm_v;
   const int64_t rows = a.num_blocks * a.num_kv_heads * kBlockSize;
   if (!encode_pool_map_bf16(&tm_k, a.k_cache, rows) || !encode_pool_map_bf16(&tm_v, a.v_cache, rows))

@@ -51,12 +51,13 @@ struct DecodeArgs {
   const int32_t* seq_lens;  // may be null in chunk mode
   float* ws_acc;            // [B][Hq][max_splits][D] fp32 (unused if max_splits == 1)
   float* ws_ml;             // [B][Hq][max_splits][2] fp32
+  int* ws_np;               // [B][Hkv] partials per (sequence, KV head) (balanced walk)
   int* err;
   int num_seqs;
   int bt_stride;            // elements between block-table rows (0: all rows share one)
   int max_blocks_per_seq;
   int max_seq_len;          // host bound on every sequence length
-  int max_splits;           // ceil(max_seq_len / split_tokens)
+  int max_splits;           // partial slots per row (>= partials of any row)
   int split_tokens;
   int64_t num_blocks;
   int num_q_heads;
@@ -78,6 +79,13 @@ struct DecodeArgs {
   // alone; beside a prefill, whose re-read K/V lives in L2, plain stores
   // measured faster.
   int keep_partials;
+  // 1: the bf16 decode's balanced walk (set by its launcher when ws_np is
+  // given and the decode runs alone): the KV-head stages of all sequences are
+  // cut into equal shares,
+  // one per CTA, and the main kernel records in ws_np how many partials each
+  // (sequence, KV head) left for the merge; 0: 512-token splits, the merge
+  // derives their count from seq_lens.
+  int balanced;
 };
 // True if (dtype, head_dim, group) has a compiled decode kernel.
 bool decode_supported(int is_bf16, int head_dim, int group);

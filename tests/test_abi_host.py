@@ -59,11 +59,13 @@ def test_host_only_functions(lib):
     assert binding.abi_version() == 1
     assert binding.status_str(0) == "ok"
     assert binding.status_str(5) == "unsupported shape"
-    # one split of 512 tokens needs no workspace; more splits need (D + 2) floats per split
+    # one split of 512 tokens needs no workspace; more need (D + 2) floats per
+    # partial slot (ceil(L / 512) + 1 slots per row) and one int per row
     assert binding.decode_workspace_bytes(64, 32, 128, 512) == 0
     n = binding.decode_workspace_bytes(64, 32, 128, 2301)
-    rows = 64 * 32 * 5
-    assert n >= rows * 130 * 4 and n < rows * 130 * 4 + 512
+    rows = 64 * 32 * 6
+    base = rows * 130 * 4 + 64 * 32 * 4
+    assert n >= base and n < base + 768
 
 
 def _nullp():

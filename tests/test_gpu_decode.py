@@ -176,6 +176,65 @@ def test_fused_append_decode_matches_append_then_decode(hq, hkv):
     assert G.max_err(out_f, ref) <= 2e-2
 
 
+def _balanced_lens(seed):
+    """48 seeded lengths in [1, 3000], with 1, 64, 65, 512 and 513 among
+    them: 48 x 8 KV heads x about 24 stages of 64 tokens is more than 8 per
+    CTA of the whole GPU's grid, so the bf16 decode takes its balanced walk,
+    which cuts streams at arbitrary 64-token boundaries."""
+    g = torch.Generator().manual_seed(seed)
+    lens = torch.randint(1, 3001, (48,), generator=g).tolist()
+    lens[:5] = [1, 64, 65, 512, 513]
+    return lens
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_decode_balanced_walk_vs_oracle(seed):
+    """The balanced walk (fused append, then the merge of a variable number of
+    pieces per stream): pools bit-exact against the oracle's scatter, every
+    output within the bf16 tolerance of the fp64 oracle, NaN in unused rows."""
+    w = G.custom_workload(torch.bfloat16, 32, 8, 128, seed=80 + seed)
+    lens = _balanced_lens(seed)
+    lay = W.make_layout(w, seq_lens_after=lens, prefill=(0, 0))
+    x = W.draw_layer(w, lay, 0)
+    G.poison_unused(x.k_cache, x.v_cache, G.used_slot_mask(lay, w.block_size))
+    kc, vc = x.k_cache.cuda(), x.v_cache.cuda()
+    bt = lay.decode_block_table.cuda().contiguous()
+    msl = int(lay.seq_lens.max())
+    ws = B.decode_workspace(len(lens), 32, 128, msl)
+    out = torch.empty_like(x.q_decode).cuda()
+    B.paged_decode_attention_append(out, x.q_decode.cuda(), x.k_new.cuda(), x.v_new.cuda(), kc, vc,
+                                    bt, lay.seq_lens.cuda(), msl, w.scale, ws)
+    torch.cuda.synchronize()
+    assert B.get_device_error() == 0
+    rk, rv = G.oracle_append(lay, x)
+    bits = lambda t: t.cpu().view(torch.int16)
+    assert torch.equal(bits(kc), bits(rk)) and torch.equal(bits(vc), bits(rv))
+    ref = oracle.paged_decode(x.q_decode, rk, rv, lay.decode_block_table, lay.seq_lens, w.scale)
+    assert G.max_err(out, ref) <= 2e-2
+    # the unfused call takes the same walk: identical bits
+    out2 = G.gpu_decode(w, x.q_decode, kc, vc, lay.decode_block_table, lay.seq_lens)
+    assert torch.equal(bits(out), bits(out2))
+
+
+def test_decode_balanced_walk_reports_bad_block_id():
+    """A bad block id in one sequence of a balanced batch: the error word says
+    so and every other sequence is still right."""
+    w = G.custom_workload(torch.bfloat16, 32, 8, 128, seed=83)
+    lens = _balanced_lens(3)
+    lay = W.make_layout(w, seq_lens_after=lens, prefill=(0, 0))
+    x = W.draw_layer(w, lay, 0)
+    kc, vc = G.gpu_append(lay, x)
+    bt = lay.decode_block_table.clone()
+    bad = 7
+    bt[bad, 1] = lay.num_blocks + 3
+    out = G.gpu_decode(w, x.q_decode, kc, vc, bt, lay.seq_lens, check_err=False)
+    assert B.get_device_error() == 2
+    rk, rv = G.oracle_append(lay, x)
+    ref = oracle.paged_decode(x.q_decode, rk, rv, lay.decode_block_table, lay.seq_lens, w.scale)
+    keep = [i for i in range(len(lens)) if i != bad]
+    assert G.max_err(out[keep], ref[keep]) <= 2e-2
+
+
 def test_fused_append_decode_rejects_fp32():
     w = G.custom_workload(torch.float32, 4, 2, 16)
     lay = W.make_layout(w, seq_lens_after=[5], prefill=(0, 0))
