@@ -418,6 +418,7 @@ pkv_status pkv_paged_decode_attention_fp8(void* out, const void* q, const void* 
   a.seq_lens = seq_lens;
   a.ws_acc = need ? part.acc : nullptr;
   a.ws_ml = need ? part.ml : nullptr;
+  a.ws_np = need ? part.np : nullptr;
   a.err = err;
   a.num_seqs = num_seqs;
   a.bt_stride = max_blocks_per_seq;

@@ -151,9 +151,17 @@ decode_fp8_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
     *abort_flag = 0;
     fence_mbar_init();
   }
-  plan_units(a, cu);
+  // balanced walk over 64-token stages when the batch gives every CTA at
+  // least kMinStagesPerCta of them; otherwise 512-token splits
+  plan_units(a, cu, a.balanced ? kStageTok : 0);
   __syncthreads();
-  const int total = cu[a.num_seqs];
+  const bool balanced =
+      a.balanced && (int64_t)cu[a.num_seqs] >= (int64_t)kMinStagesPerCta * gridDim.x;
+  if (a.balanced && !balanced) {
+    __syncthreads();
+    plan_units(a, cu);
+    __syncthreads();
+  }
   volatile int* vabort = abort_flag;
 
   if (warp == kCW) {
@@ -165,8 +173,9 @@ decode_fp8_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
     const uint64_t policy = policy_evict_first();
     uint32_t issued = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-      const Unit u = find_unit(a, cu, w);
+    Walk wk = walk_begin(a, cu, balanced);
+    Unit u;
+    while (ok && walk_next(a, cu, kStageTok, wk, u)) {
       const int blk0 = u.tok_begin / kBlockSize;
       const int nblk = (u.tok_end - 1) / kBlockSize - blk0 + 1;
       const int32_t* bt_row = a.block_table + (int64_t)u.b * a.bt_stride + blk0;
@@ -226,9 +235,12 @@ decode_fp8_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
   __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(a.out);
   uint32_t consumed = 0;
 
-  for (int w = blockIdx.x; w < total; w += gridDim.x) {
-    const Unit u = find_unit(a, cu, w);
+  Walk wk = walk_begin(a, cu, balanced);
+  Unit u;
+  while (walk_next(a, cu, kStageTok, wk, u)) {
     const int hq0 = u.g * G;
+    // the merge reads how many partials this (sequence, KV head) left
+    if (a.balanced && u.s == 0 && tid == 0) a.ws_np[u.b * a.num_kv_heads + u.g] = u.ns;
     const float sl2 = a.scale * __ldg(a.k_scale + u.g) * 1.4426950408889634f;
     const float vscale = __ldg(a.v_scale + u.g);
     // Q^T fragments: head 8nt + g, dims 32t + 4ks + {0,1} (b0) and {2,3} (b1)
@@ -470,8 +482,10 @@ decode_fp8_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
 }
 
 template <int G>
-cudaError_t launch_fp8_g(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
+cudaError_t launch_fp8_g(const DecodeArgs& args, int num_sms, cudaStream_t stream) {
   using C = F8Cfg<G>;
+  DecodeArgs a = args;
+  a.balanced = a.ws_np != nullptr;
   CUtensorMap tm_k, tm_v;
   const int64_t rows = a.num_blocks * a.num_kv_heads * kBlockSize;
   if (!encode_pool_map_u8(&tm_k, a.k_cache, rows) || !encode_pool_map_u8(&tm_v, a.v_cache, rows))

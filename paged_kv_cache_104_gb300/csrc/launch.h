@@ -79,9 +79,9 @@ struct DecodeArgs {
   // alone; beside a prefill, whose re-read K/V lives in L2, plain stores
   // measured faster.
   int keep_partials;
-  // 1: the bf16 decode's balanced walk (set by its launcher when ws_np is
-  // given and the decode runs alone): the KV-head stages of all sequences are
-  // cut into equal shares,
+  // 1: the balanced walk of the bf16 and fp8 decodes (set by their launchers
+  // when ws_np is given and the decode runs alone): the KV-head stages of all
+  // sequences are cut into equal shares,
   // one per CTA, and the main kernel records in ws_np how many partials each
   // (sequence, KV head) left for the merge; 0: 512-token splits, the merge
   // derives their count from seq_lens.
