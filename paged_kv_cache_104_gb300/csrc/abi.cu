@@ -514,6 +514,7 @@ pkv_status pkv_mla_decode_attention(void* out, const void* q, const void* w_k, c
   a.seq_lens = seq_lens;
   a.ws_acc = pp.acc;
   a.ws_ml = pp.ml;
+  a.ws_np = splits > 1 ? pp.np : nullptr;
   a.err = err;
   a.num_seqs = num_seqs;
   a.bt_stride = max_blocks_per_seq;

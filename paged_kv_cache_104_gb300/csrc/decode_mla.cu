@@ -128,9 +128,17 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c) 
     *abort_flag = 0;
     fence_mbar_init();
   }
-  plan_units(a, cu);
+  // balanced walk over 64-token stages when the batch gives every CTA at
+  // least kMinStagesPerCta of them; otherwise 512-token splits
+  plan_units(a, cu, a.balanced ? kStageTokL : 0);
   __syncthreads();
-  const int total = cu[a.num_seqs];
+  const bool balanced =
+      a.balanced && (int64_t)cu[a.num_seqs] >= (int64_t)kMinStagesPerCta * gridDim.x;
+  if (a.balanced && !balanced) {
+    __syncthreads();
+    plan_units(a, cu);
+    __syncthreads();
+  }
   volatile int* vabort = abort_flag;
 
   if (warp >= kCWL) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsRestL));
@@ -142,8 +150,9 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c) 
     const uint64_t policy = policy_evict_first();
     uint32_t issued = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-      const Unit u = find_unit(a, cu, w);
+    Walk wk = walk_begin(a, cu, balanced);
+    Unit u;
+    while (ok && walk_next(a, cu, kStageTokL, wk, u)) {
       const int blk0 = u.tok_begin / kBlockSize;
       const int nblk = (u.tok_end - 1) / kBlockSize - blk0 + 1;
       const int32_t* bt_row = a.block_table + (int64_t)u.b * a.bt_stride + blk0;
@@ -210,8 +219,11 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c) 
   const int vhalf = g >> 2;
   uint32_t consumed = 0;
 
-  for (int w = blockIdx.x; w < total; w += gridDim.x) {
-    const Unit u = find_unit(a, cu, w);
+  Walk wk = walk_begin(a, cu, balanced);
+  Unit u;
+  while (walk_next(a, cu, kStageTokL, wk, u)) {
+    // the merge reads how many partials this sequence left
+    if (a.balanced && u.s == 0 && tid == 0) a.ws_np[u.b] = u.ns;
     // q~ of heads hbase + 8nt + g as B fragments, in the lane's K order
     uint4 qf[kNTL][4];
 #pragma unroll
@@ -433,7 +445,9 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c) 
 
 }  // namespace
 
-cudaError_t launch_decode_mla(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
+cudaError_t launch_decode_mla(const DecodeArgs& args, int num_sms, cudaStream_t stream) {
+  DecodeArgs a = args;
+  a.balanced = a.ws_np != nullptr;
   if (a.chunk_prior >= 0 || a.split_tokens % kStageTokL != 0 || a.num_kv_heads != 1 ||
       a.num_q_heads != kHeads || a.head_dim != kR)
     return cudaErrorInvalidValue;

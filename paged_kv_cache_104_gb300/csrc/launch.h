@@ -79,7 +79,7 @@ struct DecodeArgs {
   // alone; beside a prefill, whose re-read K/V lives in L2, plain stores
   // measured faster.
   int keep_partials;
-  // 1: the balanced walk of the bf16 and fp8 decodes (set by their launchers
+  // 1: the balanced walk of the bf16, fp8 and latent decodes (set by their launchers
   // when ws_np is given and the decode runs alone): the KV-head stages of all
   // sequences are cut into equal shares,
   // one per CTA, and the main kernel records in ws_np how many partials each

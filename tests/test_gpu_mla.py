@@ -45,6 +45,24 @@ def _run(w, lay, x, poison=False):
     return G.cpu(out), rp
 
 
+def test_mla_balanced_walk_nan_in_unused_rows():
+    """80 seeded lengths in [1, 2500] (with 1, 64, 65, 512, 513): more than 8
+    stages of 64 tokens per CTA, so the kernel cuts the sequences into equal
+    per-CTA shares at arbitrary stage boundaries and the merge takes a
+    varying number of pieces per sequence; NaN in every unused pool row."""
+    w = _workload(seed=12)
+    g = torch.Generator().manual_seed(5)
+    lens = torch.randint(1, 2501, (80,), generator=g).tolist()
+    lens[:5] = [1, 64, 65, 512, 513]
+    lay = W.make_layout(w, seq_lens_after=lens, prefill=(0, 0))
+    x = W.draw_latent(w, lay)
+    got, rp = _run(w, lay, x, poison=True)
+    ref = M.mla_decode(G.cpu(x.q), G.cpu(x.w_k), G.cpu(x.w_v), rp, lay.decode_block_table,
+                       lay.seq_lens, w.scale)
+    assert torch.isfinite(got).all()
+    assert G.max_err(got, ref) <= TOL
+
+
 def test_mla_edge_lengths_nan_in_unused_rows():
     """Block (16), stage (64) and split (512) boundaries and one token; NaN
     in every pool row no sequence uses."""
