@@ -8,8 +8,9 @@
 // bottleneck" mentions (section "What the profile said"; the pages give no
 // format).  The cache is half the bytes of bf16, and decode is HBM-bound.
 //
-// Same unit structure as the bf16 kernel -- persistent CTAs over (sequence,
-// KV head, 512-token split) units, one producer warp streaming each block's K
+// Same unit structure as the bf16 kernel -- persistent CTAs walking (sequence,
+// KV head) streams in equal per-CTA shares of 64-token stages, or in 512-token
+// splits for small batches, one producer warp streaming each block's K
 // and V tiles with 2-D TMA (one 16-row x 128-byte box each, 128-byte swizzle)
 // into a 4-stage ring, four consumer warps taking one block per stage -- but
 // the products are turned around: keys are the M side of the m16n8k16 tile

@@ -12,8 +12,9 @@
 // the latent, shared by all Hq query heads.  This kernel computes z (rank 128,
 // 32 query heads).
 //
-// Structure: the bf16 decode kernel's (persistent CTAs over (sequence,
-// 512-token split) units; one TMA producer warp; keys on the M side of the
+// Structure: the bf16 decode kernel's (persistent CTAs walking the sequences
+// in equal per-CTA shares of 64-token stages, or 512-token splits for small
+// batches; one TMA producer warp; keys on the M side of the
 // tile and heads on N; the running max gated by a warp vote; split partials
 // merged by the reduce kernel), with two changes for the 32 heads that share
 // each latent block:

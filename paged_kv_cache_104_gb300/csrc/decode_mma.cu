@@ -17,8 +17,11 @@
 //   O^T = V^T . P^T (A = V^T, 16 dims x 16 keys; B = P^T)
 // which is 8 + 8 products per block for G <= 8.
 //
-// Structure (per CTA: one TMA producer warp + four consumer warps,
-// persistent over a flat list of (sequence, KV head, 512-token split) units):
+// Structure (per CTA: one TMA producer warp + four consumer warps, persistent
+// over (sequence, KV head) streams: run alone on a large enough batch, each
+// CTA takes an equal share of all streams' 64-token stages and a stream cut
+// between CTAs leaves one partial per piece; otherwise (small batches, or
+// beside a prefill) units of 512-token splits go round-robin to the CTAs):
 //  * The producer streams, for each 16-token block, its K and V tiles with
 //    2-D TMA tensor copies (two 64-column halves each, 128-byte swizzle) into
 //    a 2-stage ring of 4 blocks per stage, completing on mbarriers.  It runs
