@@ -564,6 +564,8 @@ def run_mla_decode(args, w, lay, dev, stream, dist, n):
                       "up-projection GEMM)", "bound": "hbm",
             "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": dec_gbs / hbm_peak,
             "traffic": None, "algorithmic_bytes_per_launch": dec_bytes,
+            "traffic_note": "the call is four launches; ncu traffic is recorded for the "
+                            "attention kernel alone (profiles/traffic.json, decode_mla_kernel)",
             "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
             else "fallback 6.8 TB/s",
         },
