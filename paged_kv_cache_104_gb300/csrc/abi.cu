@@ -1,6 +1,7 @@
 // C ABI of libpagedkv.so: argument validation, workspace layout, dispatch to
 // the kernel launchers, and the per-device error word.  The declarations and
 // their contracts are in include/pagedkv.h.
+#include <climits>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -180,6 +181,8 @@ pkv_status decode_prepare(pkv::DecodeArgs* out_args, int* out_sms, void* out, co
     return PKV_EINVAL;
   const size_t need = pkv_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len);
   if (workspace_bytes < need) return PKV_ERANGE;
+  if ((int64_t)num_seqs * num_kv_heads * max_splits_for(max_seq_len) >= (int64_t)INT_MAX)
+    return PKV_ERANGE;  // the kernels' unit list is indexed by int
   if (need > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))) return PKV_EINVAL;
   int* err = nullptr;
   int sms = 0;
@@ -402,6 +405,8 @@ pkv_status pkv_paged_decode_attention_fp8(void* out, const void* q, const void* 
     return PKV_EINVAL;
   const size_t need = pkv_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len);
   if (workspace_bytes < need) return PKV_ERANGE;
+  if ((int64_t)num_seqs * num_kv_heads * max_splits_for(max_seq_len) >= (int64_t)INT_MAX)
+    return PKV_ERANGE;  // the kernels' unit list is indexed by int
   if (need > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))) return PKV_EINVAL;
   int* err = nullptr;
   int sms = 0;
@@ -489,6 +494,8 @@ pkv_status pkv_mla_decode_attention(void* out, const void* q, const void* w_k, c
     return PKV_EINVAL;
   if (workspace_bytes < pkv_mla_workspace_bytes(num_seqs, num_q_heads, rank, max_seq_len))
     return PKV_ERANGE;
+  if ((int64_t)num_seqs * max_splits_for(max_seq_len) >= (int64_t)INT_MAX)
+    return PKV_ERANGE;  // the kernel's unit list is indexed by int
   int* err = nullptr;
   int sms = 0;
   pkv_status st = device_state(&err, &sms);

@@ -5,6 +5,8 @@
 // kernel's load granule), cut into one equal share of stages per CTA.
 #pragma once
 
+#include <climits>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -99,6 +101,13 @@ struct Walk {
 // kMinStagesPerCta stages per CTA (so no stream is cut into more pieces than
 // the workspace has partial slots); otherwise the split walk.
 constexpr int kMinStagesPerCta = kSplitTokens / 64;
+
+// True if the stage prefix sums of this call fit an int: every counted
+// sequence has at most max_seq_len tokens (longer ones are rejected).
+inline bool stage_plan_fits(const DecodeArgs& a, int stage_tok) {
+  return (int64_t)a.num_seqs * a.num_kv_heads * ((a.max_seq_len + stage_tok - 1) / stage_tok) <
+         (int64_t)INT_MAX;
+}
 
 // The CTA whose share holds stage p.
 __device__ __forceinline__ int cta_of_stage(int64_t p, int64_t total) {

@@ -486,7 +486,7 @@ template <int G>
 cudaError_t launch_fp8_g(const DecodeArgs& args, int num_sms, cudaStream_t stream) {
   using C = F8Cfg<G>;
   DecodeArgs a = args;
-  a.balanced = a.ws_np != nullptr;
+  a.balanced = a.ws_np != nullptr && stage_plan_fits(a, kStageTok);
   CUtensorMap tm_k, tm_v;
   const int64_t rows = a.num_blocks * a.num_kv_heads * kBlockSize;
   if (!encode_pool_map_u8(&tm_k, a.k_cache, rows) || !encode_pool_map_u8(&tm_v, a.v_cache, rows))

@@ -448,7 +448,7 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c) 
 
 cudaError_t launch_decode_mla(const DecodeArgs& args, int num_sms, cudaStream_t stream) {
   DecodeArgs a = args;
-  a.balanced = a.ws_np != nullptr;
+  a.balanced = a.ws_np != nullptr && stage_plan_fits(a, kStageTokL);
   if (a.chunk_prior >= 0 || a.split_tokens % kStageTokL != 0 || a.num_kv_heads != 1 ||
       a.num_q_heads != kHeads || a.head_dim != kR)
     return cudaErrorInvalidValue;

@@ -531,7 +531,7 @@ cudaError_t launch_g(const DecodeArgs& args, int num_sms, cudaStream_t stream, b
   a.keep_partials = dependent ? 0 : 1;
   // the balanced walk when the decode has the GPU to itself; beside a
   // prefill the 512-token splits measured faster
-  a.balanced = a.ws_np != nullptr && !dependent;
+  a.balanced = a.ws_np != nullptr && !dependent && stage_plan_fits(a, kStageTok);
   CUtensorMap tm_k, tm_v;
   const int64_t rows = a.num_blocks * a.num_kv_heads * kBlockSize;
   if (!encode_pool_map_bf16(&tm_k, a.k_cache, rows) || !encode_pool_map_bf16(&tm_v, a.v_cache, rows))
