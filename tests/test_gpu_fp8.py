@@ -155,6 +155,30 @@ def test_fp8_decode_edge_lengths_and_groups(hq, hkv):
     assert G.max_err(got, ref) <= 2e-2
 
 
+def test_fp8_decode_balanced_walk_nan_in_unused_rows():
+    """48 seeded lengths in [1, 3000] (with 1, 64, 65, 512, 513): enough
+    64-token stages for the balanced walk, which cuts sequences between CTAs
+    at arbitrary stage boundaries; every output against the oracle, NaN codes
+    in every unused pool row."""
+    w = G.custom_workload(torch.bfloat16, 32, 8, 128, seed=42)
+    g = torch.Generator().manual_seed(9)
+    lens = torch.randint(1, 3001, (48,), generator=g).tolist()
+    lens[:5] = [1, 64, 65, 512, 513]
+    lay = W.make_layout(w, seq_lens_after=lens, prefill=(0, 0))
+    x = W.draw_layer(w, lay, 0, with_pool=False)
+    ks, vs, kc, vc = _pools(w, lay)
+    unused = ~G.used_slot_mask(lay, w.block_size)
+    kc.permute(0, 2, 1, 3)[unused] = NAN_CODE
+    vc.permute(0, 2, 1, 3)[unused] = NAN_CODE
+    gk, gv = _gpu_append(x, kc, vc, ks, vs, lay.slot_mapping)
+    rk, rv = _oracle_append(x, kc, vc, ks, vs, lay.slot_mapping)
+    assert np.array_equal(G.cpu(gk).numpy(), rk) and np.array_equal(G.cpu(gv).numpy(), rv)
+    got = _gpu_decode(w, x.q_decode, gk, gv, ks, vs, lay.decode_block_table, lay.seq_lens)
+    ref = _oracle_decode(w, x.q_decode, rk, rv, ks, vs, lay.decode_block_table, lay.seq_lens)
+    assert torch.isfinite(got).all()
+    assert G.max_err(got, ref) <= 2e-2
+
+
 @pytest.mark.parametrize("name", ["llama8b_decode", "ragged_prefill"])
 def test_fp8_decode_full_size_sampled_sequences(name):
     """One full-size layer in the launch configuration of the step; every
