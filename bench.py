@@ -14,9 +14,23 @@ layer, far larger than L2), so no L2 flush is needed between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
+Per layer the decode and the prefill run side by side on disjoint SMs (the
+prefill's SM count picked by a short trial before warm-up; --side-by-side 0
+runs them one after the other).
+
 Prints one JSON line (rank 0).  `value` is achieved algorithmic HBM GB/s of
-the whole step; decode tokens/s and prefill TFLOP/s ride along.  The
-`reference` arm times the fp64 CPU oracle on a bounded sample of the same
+the whole step; decode tokens/s and prefill TFLOP/s ride along, with:
+  roofline / prefill_roofline  the decode's and the prefill's own rates
+                               against the measured peaks;
+  side_by_side                 the split and each half's time alone;
+  e2e                          the same step through the C ABI from pinned
+                               host buffers, copies included;
+  fp8_decode, mla_decode       the decode over an fp8 cache and over a
+                               latent cache, each with its own roofline;
+  decode_configs               the decode step of the 2,301-token and
+                               32,001-token batches;
+  cpu_baseline                 the oracle on a bounded sample.
+The `reference` arm times the fp64 CPU oracle on a bounded sample of the same
 workload (the pages ship no runnable implementation of this path).
 """
 from __future__ import annotations
