@@ -28,8 +28,11 @@ the whole step; decode tokens/s and prefill TFLOP/s ride along, with:
   fp8_decode, mla_decode       the decode over an fp8 cache and over a
                                latent cache, each with its own roofline;
   decode_configs               the decode step of the 2,301-token and
-                               32,001-token batches;
-  cpu_baseline                 the oracle on a bounded sample.
+                               32,001-token batches, and of the 16-sequence
+                               65-token batch with the L2 flushed before
+                               every timed step;
+  cpu_baseline                 the oracle on a bounded sample, on all host
+                               cores and (single_core) on one.
 The `reference` arm times the fp64 CPU oracle on a bounded sample of the same
 workload (the pages ship no runnable implementation of this path).
 """
@@ -112,7 +115,7 @@ def profiled_traffic(kernel: str, source: str):
 
 # --------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi sampling every 200 ms while the timed region runs."""
+    """nvidia-smi sampling every 50 ms while the timed region runs."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -125,7 +128,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -475,6 +478,80 @@ def run_decode_config(args, name, dev, stream, dist, n):
             "kernel": "paged_decode_attention (split-K main + reduce)", "bound": "hbm",
             "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": dec_gbs / hbm_peak,
             "algorithmic_bytes_per_launch": acct["decode_bytes_layer"],
+            "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+            else "fallback 6.8 TB/s",
+        },
+    }
+
+
+def run_flushed_decode(args, name, dev, stream, dist, n):
+    """Time the bf16 decode step of a configuration whose cache fits in L2
+    (the 16-sequence batch at 65 tokens holds 4.3 MB of keys and values, the
+    L2 129 MB): per layer the fused append + paged decode, every timed step
+    preceded by pkv_l2_flush, which reads a buffer four times the L2's size,
+    so the step reads its cache from HBM.  Only the step is timed (CUDA events
+    right around it); the median over the timed steps is reported."""
+    from paged_kv_cache_104_gb300 import binding as B
+
+    w = W.WORKLOADS[name]
+    lay = W.make_layout(w)
+    acct = step_accounting(w, lay)
+    L, hq, d = w.layers, w.num_q_heads, w.head_dim
+    nd = lay.num_decode_tokens
+    xs = [W.draw_layer(w, lay, li + 1000 * dist_env()[1], device=dev) for li in range(L)]
+    bt = lay.decode_block_table.to(dev).contiguous()
+    sl = lay.seq_lens.to(dev)
+    msl = int(lay.seq_lens.max())
+    wsp = B.decode_workspace(nd, hq, d, msl, device=dev)
+    outs = [torch.empty_like(xs[li].q_decode) for li in range(L)]
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 129 * 2 ** 20)
+    flush = torch.empty((4 * l2 + 15) // 16 * 16, dtype=torch.uint8, device=dev)
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        for li in range(L):
+            x = xs[li]
+            B.paged_decode_attention_append(outs[li], x.q_decode, x.k_new, x.v_new, x.k_cache,
+                                            x.v_cache, bt, sl, msl, w.scale, wsp, stream=stream)
+
+    iters = max(args.steps, 50)
+    for _ in range(max(args.warmup, 3)):
+        B.l2_flush(flush, sink, stream=stream)
+        step()
+    torch.cuda.synchronize(dev)
+    assert B.get_device_error() == 0, f"device error word set during the {name} warm-up"
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(iters)]
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    for e0, e1 in ev:
+        B.l2_flush(flush, sink, stream=stream)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(dist)
+    assert B.get_device_error() == 0, f"device error word set during the {name} steps"
+    ms_step = max_over_ranks(dist, statistics.median(e0.elapsed_time(e1) for e0, e1 in ev))
+    hbm_peak, _, peak_src = measured_peaks()
+    dec_gbs = L * acct["decode_bytes_layer"] / (ms_step / 1e3) / 1e9
+    return {
+        "what": w.description + "; per layer the fused append + paged decode, the L2 flushed "
+                "before every timed step",
+        "ms_per_step": ms_step, "timing": f"median of {iters} steps, CUDA events around each",
+        "value": n * acct["bytes_step"] / (ms_step / 1e3) / 1e9, "unit": "GB/s",
+        "decode_tokens_per_s": n * nd / (ms_step / 1e3),
+        "cached_tokens": int(lay.seq_lens.sum()),
+        "l2": f"flushed before every timed step: pkv_l2_flush reads {flush.numel() / 1e6:.0f} MB "
+              f"(4x the {l2 / 1e6:.0f} MB L2), outside the events",
+        "gpu_launches": iters * L * (2 if msl > 512 else 1),
+        "roofline": {
+            "kernel": "paged_decode_attention (fused append; one launch at this length)",
+            "bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s",
+            "frac": dec_gbs / hbm_peak,
+            "algorithmic_bytes_per_launch": acct["decode_bytes_layer"],
+            "note": "a 4.3 MB launch is latency-bound: launch, the walk's prologue and one "
+                    "stage of HBM latency dominate; reported, not a bandwidth target",
             "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
             else "fallback 6.8 TB/s",
         },
@@ -936,6 +1013,9 @@ def run_ours(args, w, lay, acct):
         for name in ("llama8b_decode", "long_context"):
             line["decode_configs"][name] = run_decode_config(args, name, dev, stream, dist, n)
             torch.cuda.empty_cache()
+        line["decode_configs"]["toy_decode"] = run_flushed_decode(args, "toy_decode", dev,
+                                                                  stream, dist, n)
+        torch.cuda.empty_cache()
 
     # ---- the oracle on this host's cores, bounded sample, rank 0 at N=1 only
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -950,6 +1030,16 @@ def run_ours(args, w, lay, acct):
         line["cpu_baseline"] = {"value": acct["bytes_step"] / t_cpu / 1e9, "unit": "GB/s",
                                 "cores": oracle.num_threads(), "kind": "oracle",
                                 "sample": desc, "seconds": spent}
+        # the same oracle on one core, on a smaller sample of the same step
+        all_threads = oracle.num_threads()
+        oracle.set_threads(1)
+        sub1, xs1 = oracle_prepare(w, lay, args.cpu_single_decode_seqs, device=dev)
+        dec1, pre1, desc1, spent1 = oracle_sample_rates(w, sub1, xs1, args.cpu_single_prefill_rows)
+        oracle.set_threads(all_threads)
+        t1 = oracle_step_estimate(w, lay, acct, dec1, pre1)
+        line["cpu_baseline"]["single_core"] = {
+            "value": acct["bytes_step"] / t1 / 1e9, "unit": "GB/s", "cores": 1,
+            "sample": desc1, "seconds": spent1}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -990,6 +1080,10 @@ def main():
                     help="decode sequences in the oracle sample of cpu_baseline")
     ap.add_argument("--cpu-prefill-rows", type=int, default=256,
                     help="chunk rows in the oracle sample of cpu_baseline")
+    ap.add_argument("--cpu-single-decode-seqs", type=int, default=16,
+                    help="decode sequences in the one-core oracle sample of cpu_baseline")
+    ap.add_argument("--cpu-single-prefill-rows", type=int, default=32,
+                    help="chunk rows in the one-core oracle sample of cpu_baseline")
     ap.add_argument("--ref-decode-seqs", type=int, default=16,
                     help="decode sequences per step of the reference (oracle) arm")
     ap.add_argument("--ref-prefill-rows", type=int, default=32,

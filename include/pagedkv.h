@@ -177,6 +177,9 @@ pkv_status pkv_paged_decode_attention_append(void *out, const void *q, const voi
  *   Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  *   The first call on a device looks up the scratch array's device address
  *   (cudaGetSymbolAddress); make that first call before capturing any stream.
+ *   After a device reset (cudaDeviceReset) the array is gone with the old
+ *   context; the next call looks the address up again in the new one, so it
+ *   too must come before any capture.
  *   All calls share the one array, which keeps the last call's contents (no
  *   part of it needs to start at zero).  Calls whose kernels overlap on the
  *   GPU -- on different streams or from different host threads -- race on it
@@ -391,6 +394,24 @@ int64_t pkv_prefix_plan(const pkv_prefix_cache *cache, const int32_t *tokens, in
  * if clear != 0, reset it to PKV_DEVERR_NONE.  Synchronises the device.
  */
 pkv_status pkv_get_device_error(int *code, int clear);
+
+/*
+ * l2_flush -- measurement helper, not part of the attention path.  Evicts
+ * the L2 cache ahead of a timed launch whose inputs are small enough to stay
+ * in it (the 16-sequence, 65-token decode batch holds 4.3 MB of keys and
+ * values; GB300's L2 is 129 MB): timed without it, such a launch measures
+ * the L2, not HBM.
+ *   buf    device buffer, 16-byte aligned, owned by the caller; read only.
+ *          Pass one several times larger than the L2.
+ *   bytes  its size, a multiple of 16.
+ *   sink   one device int the kernel may write (it never does in practice);
+ *          it keeps the reads from being optimised away.
+ * Reads the whole buffer with 16-byte loads on `stream`, which leaves the L2
+ * holding clean lines of it, so the next launch evicts them without
+ * write-backs.  PKV_EINVAL on a null or misaligned argument; PKV_ECUDA on a
+ * launch error.
+ */
+pkv_status pkv_l2_flush(const void *buf, size_t bytes, int *sink, pkv_stream_t stream);
 
 /* Static description of a status code.  Host-only. */
 const char *pkv_status_str(pkv_status status);

@@ -66,8 +66,16 @@ def _load():
 
 
 def num_threads() -> int:
-    """OpenMP threads the oracle uses (set OMP_NUM_THREADS to change)."""
+    """OpenMP threads the oracle uses (set OMP_NUM_THREADS, or set_threads)."""
     return int(_load().pkv_oracle_num_threads())
+
+
+def set_threads(n: int) -> None:
+    """Run later oracle calls on n threads (timing only; results do not change)."""
+    lib = _load()
+    lib.pkv_oracle_set_threads.argtypes = [ctypes.c_int]
+    lib.pkv_oracle_set_threads.restype = None
+    lib.pkv_oracle_set_threads(int(n))
 
 
 def _cpu(t: torch.Tensor) -> torch.Tensor:

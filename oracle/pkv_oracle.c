@@ -291,3 +291,14 @@ int pkv_oracle_num_threads(void) {
   return 1;
 #endif
 }
+
+/* Set the number of OpenMP threads later calls use (no effect without
+ * OpenMP).  Timing only: the results do not depend on it. */
+void pkv_oracle_set_threads(int n) {
+#ifdef _OPENMP
+  extern void omp_set_num_threads(int);
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}

@@ -31,7 +31,8 @@ EXPORTS = ("pkv_kv_append", "pkv_decode_workspace_bytes", "pkv_paged_decode_atte
            "pkv_latent_append", "pkv_mla_workspace_bytes", "pkv_mla_decode_attention",
            "pkv_fnv1a64", "pkv_prefix_hash_blocks", "pkv_prefix_cache_create",
            "pkv_prefix_cache_destroy", "pkv_prefix_cache_size", "pkv_prefix_cache_insert",
-           "pkv_prefix_cache_evict", "pkv_prefix_cache_match", "pkv_prefix_plan")
+           "pkv_prefix_cache_evict", "pkv_prefix_cache_match", "pkv_prefix_plan",
+           "pkv_l2_flush")
 NOALLOC_SCRATCH_BYTES = 32 << 20  # PKV_NOALLOC_SCRATCH_BYTES
 
 
@@ -58,6 +59,68 @@ class PagedKVError(RuntimeError):
         self.status = status
 
 
+def open_library(path: str):
+    """Load a build of the library at ``path`` and declare its argument types."""
+    lib = ctypes.CDLL(path)
+    p, i, i64, f, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                        ctypes.c_size_t)
+    lib.pkv_kv_append.argtypes = [p, p, p, p, p, i64, i64, i, i, i, i, p]
+    lib.pkv_decode_workspace_bytes.argtypes = [i, i, i, i]
+    lib.pkv_decode_workspace_bytes.restype = sz
+    lib.pkv_paged_decode_attention.argtypes = [p, p, p, p, p, p, i, i, i, i64, i, i, i, i, f,
+                                               p, sz, i, p]
+    lib.pkv_chunked_prefill_attention.argtypes = [p, p, p, p, p, i, i, i, i64, i, i, i, i, f,
+                                                  i, p]
+    lib.pkv_paged_decode_attention_noalloc.argtypes = [p, p, p, p, p, p, i, i, i, i64, i, i,
+                                                       i, i, f, i, p]
+    lib.pkv_paged_decode_attention_append.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i64, i,
+                                                      i, i, i, f, p, sz, i, p]
+    lib.pkv_decode_prefill_attention.argtypes = [ctypes.POINTER(DecodePrefillArgs), p]
+    lib.pkv_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int), i]
+    lib.pkv_l2_flush.argtypes = [p, sz, p, p]
+    lib.pkv_l2_flush.restype = ctypes.c_int
+    lib.pkv_status_str.argtypes = [i]
+    lib.pkv_status_str.restype = ctypes.c_char_p
+    lib.pkv_kv_append_fp8.argtypes = [p, p, p, p, p, p, p, i64, i64, i, i, i, p]
+    lib.pkv_kv_append_fp8.restype = ctypes.c_int
+    lib.pkv_paged_decode_attention_fp8.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i64, i, i,
+                                                   i, i, f, p, sz, p]
+    lib.pkv_paged_decode_attention_fp8.restype = ctypes.c_int
+    lib.pkv_latent_append.argtypes = [p, p, p, i64, i64, i, i, p]
+    lib.pkv_latent_append.restype = ctypes.c_int
+    lib.pkv_mla_workspace_bytes.argtypes = [i, i, i, i]
+    lib.pkv_mla_workspace_bytes.restype = sz
+    lib.pkv_mla_decode_attention.argtypes = [p, p, p, p, p, p, p, i, i, i, i64, i, i, i, i, f,
+                                             p, sz, p]
+    lib.pkv_mla_decode_attention.restype = ctypes.c_int
+    u64p = ctypes.POINTER(ctypes.c_uint64)
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    lib.pkv_fnv1a64.argtypes = [p, sz]
+    lib.pkv_fnv1a64.restype = ctypes.c_uint64
+    lib.pkv_prefix_hash_blocks.argtypes = [i32p, i64, i, ctypes.c_uint64, u64p]
+    lib.pkv_prefix_hash_blocks.restype = i64
+    lib.pkv_prefix_cache_create.argtypes = []
+    lib.pkv_prefix_cache_create.restype = p
+    lib.pkv_prefix_cache_destroy.argtypes = [p]
+    lib.pkv_prefix_cache_destroy.restype = None
+    lib.pkv_prefix_cache_size.argtypes = [p]
+    lib.pkv_prefix_cache_size.restype = i64
+    lib.pkv_prefix_cache_insert.argtypes = [p, u64p, i32p, i64]
+    lib.pkv_prefix_cache_insert.restype = ctypes.c_int
+    lib.pkv_prefix_cache_evict.argtypes = [p, u64p, i64]
+    lib.pkv_prefix_cache_evict.restype = ctypes.c_int
+    lib.pkv_prefix_cache_match.argtypes = [p, u64p, i64, i32p]
+    lib.pkv_prefix_cache_match.restype = i64
+    lib.pkv_prefix_plan.argtypes = [p, i32p, i64, i, i32p, u64p]
+    lib.pkv_prefix_plan.restype = i64
+    for name in ("pkv_kv_append", "pkv_paged_decode_attention",
+                 "pkv_paged_decode_attention_noalloc", "pkv_paged_decode_attention_append",
+                 "pkv_chunked_prefill_attention", "pkv_decode_prefill_attention",
+                 "pkv_get_device_error", "pkv_abi_version"):
+        getattr(lib, name).restype = ctypes.c_int
+    return lib
+
+
 def load():
     """Load the shared library (built by ``paged_kv_cache_104_gb300.build``)."""
     global _lib
@@ -66,63 +129,8 @@ def load():
             return _lib
         if not os.path.exists(LIB_PATH):
             raise ImportError(f"{LIB_PATH} is missing: run `python -m paged_kv_cache_104_gb300.build`")
-        lib = ctypes.CDLL(LIB_PATH)
-        p, i, i64, f, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
-                            ctypes.c_size_t)
-        lib.pkv_kv_append.argtypes = [p, p, p, p, p, i64, i64, i, i, i, i, p]
-        lib.pkv_decode_workspace_bytes.argtypes = [i, i, i, i]
-        lib.pkv_decode_workspace_bytes.restype = sz
-        lib.pkv_paged_decode_attention.argtypes = [p, p, p, p, p, p, i, i, i, i64, i, i, i, i, f,
-                                                   p, sz, i, p]
-        lib.pkv_chunked_prefill_attention.argtypes = [p, p, p, p, p, i, i, i, i64, i, i, i, i, f,
-                                                      i, p]
-        lib.pkv_paged_decode_attention_noalloc.argtypes = [p, p, p, p, p, p, i, i, i, i64, i, i,
-                                                           i, i, f, i, p]
-        lib.pkv_paged_decode_attention_append.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i64, i,
-                                                          i, i, i, f, p, sz, i, p]
-        lib.pkv_decode_prefill_attention.argtypes = [ctypes.POINTER(DecodePrefillArgs), p]
-        lib.pkv_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int), i]
-        lib.pkv_status_str.argtypes = [i]
-        lib.pkv_status_str.restype = ctypes.c_char_p
-        lib.pkv_kv_append_fp8.argtypes = [p, p, p, p, p, p, p, i64, i64, i, i, i, p]
-        lib.pkv_kv_append_fp8.restype = ctypes.c_int
-        lib.pkv_paged_decode_attention_fp8.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i64, i, i,
-                                                       i, i, f, p, sz, p]
-        lib.pkv_paged_decode_attention_fp8.restype = ctypes.c_int
-        lib.pkv_latent_append.argtypes = [p, p, p, i64, i64, i, i, p]
-        lib.pkv_latent_append.restype = ctypes.c_int
-        lib.pkv_mla_workspace_bytes.argtypes = [i, i, i, i]
-        lib.pkv_mla_workspace_bytes.restype = sz
-        lib.pkv_mla_decode_attention.argtypes = [p, p, p, p, p, p, p, i, i, i, i64, i, i, i, i, f,
-                                                 p, sz, p]
-        lib.pkv_mla_decode_attention.restype = ctypes.c_int
-        u64p = ctypes.POINTER(ctypes.c_uint64)
-        i32p = ctypes.POINTER(ctypes.c_int32)
-        lib.pkv_fnv1a64.argtypes = [p, sz]
-        lib.pkv_fnv1a64.restype = ctypes.c_uint64
-        lib.pkv_prefix_hash_blocks.argtypes = [i32p, i64, i, ctypes.c_uint64, u64p]
-        lib.pkv_prefix_hash_blocks.restype = i64
-        lib.pkv_prefix_cache_create.argtypes = []
-        lib.pkv_prefix_cache_create.restype = p
-        lib.pkv_prefix_cache_destroy.argtypes = [p]
-        lib.pkv_prefix_cache_destroy.restype = None
-        lib.pkv_prefix_cache_size.argtypes = [p]
-        lib.pkv_prefix_cache_size.restype = i64
-        lib.pkv_prefix_cache_insert.argtypes = [p, u64p, i32p, i64]
-        lib.pkv_prefix_cache_insert.restype = ctypes.c_int
-        lib.pkv_prefix_cache_evict.argtypes = [p, u64p, i64]
-        lib.pkv_prefix_cache_evict.restype = ctypes.c_int
-        lib.pkv_prefix_cache_match.argtypes = [p, u64p, i64, i32p]
-        lib.pkv_prefix_cache_match.restype = i64
-        lib.pkv_prefix_plan.argtypes = [p, i32p, i64, i, i32p, u64p]
-        lib.pkv_prefix_plan.restype = i64
-        for name in ("pkv_kv_append", "pkv_paged_decode_attention",
-                     "pkv_paged_decode_attention_noalloc", "pkv_paged_decode_attention_append",
-                     "pkv_chunked_prefill_attention", "pkv_decode_prefill_attention",
-                     "pkv_get_device_error", "pkv_abi_version"):
-            getattr(lib, name).restype = ctypes.c_int
-        _lib = lib
-        return lib
+        _lib = open_library(LIB_PATH)
+        return _lib
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -153,6 +161,15 @@ def status_str(status: int) -> str:
 
 def abi_version() -> int:
     return int(load().pkv_abi_version())
+
+
+def l2_flush(buf, sink, stream=None) -> None:
+    """Measurement helper: read the device buffer ``buf`` (several times the
+    L2's size) so the next launch finds none of its inputs in L2; ``sink`` is
+    a device int32 the kernel may write."""
+    st = load().pkv_l2_flush(_ptr(buf), buf.numel() * buf.element_size(), _ptr(sink),
+                             _stream(stream))
+    _check("pkv_l2_flush", st)
 
 
 def kv_append(k_new, v_new, k_cache, v_cache, slot_mapping, stream=None) -> None:

@@ -18,8 +18,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpagedkv.so")
-SOURCES = ["abi.cu", "append.cu", "decode.cu", "decode_fp8.cu", "decode_mla.cu", "decode_mma.cu", "gemm_heads.cu", "decode_noalloc.cu",
-           "prefill_pair.cu", "prefix_cache.cpp", "tmap.cu"]
+SOURCES = ["abi.cu", "append.cu", "decode.cu", "decode_fp8.cu", "decode_mla.cu", "decode_mma.cu",
+           "gemm_heads.cu", "decode_noalloc.cu", "host_cache.cu", "l2_flush.cu", "prefill_pair.cu",
+           "prefix_cache.cpp", "tmap.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -65,6 +66,35 @@ def build(force: bool = False, verbose: bool = False) -> str:
         subprocess.run([nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"], check=True)
         os.replace(tmp, LIB)
     return LIB
+
+
+# A test-only build of the library: the same objects but decode_mma.cu
+# compiled with PKV_TEST_WAIT_TIMEOUT, which shortens every wait limit of that
+# file to about 2 ms and makes the decode kernel's producer withhold its
+# copies, so a test can see a wait run out and the kernel return with
+# PKV_DEVERR_TIMEOUT.  Never loaded by the product.
+WAIT_TEST_DIR = os.path.join(BUILD, "wait_test")
+WAIT_TEST_LIB = os.path.join(WAIT_TEST_DIR, "libpagedkv_wait_test.so")
+
+
+def build_wait_test() -> str:
+    build()
+    os.makedirs(WAIT_TEST_DIR, exist_ok=True)
+    src = os.path.join(CSRC, "decode_mma.cu")
+    obj = os.path.join(WAIT_TEST_DIR, "decode_mma.o")
+    dep_time = max([os.path.getmtime(p) for p in _deps()] + [os.path.getmtime(src)])
+    if not os.path.exists(obj) or os.path.getmtime(obj) < dep_time:
+        subprocess.run([nvcc(), *ARCH, "-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",
+                        "-DPKV_TEST_WAIT_TIMEOUT", "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj],
+                       check=True)
+    objs = [obj] + [os.path.join(BUILD, os.path.splitext(f)[0] + ".o") for f in SOURCES
+                    if f != "decode_mma.cu"]
+    if not os.path.exists(WAIT_TEST_LIB) or os.path.getmtime(WAIT_TEST_LIB) < max(
+            os.path.getmtime(o) for o in objs):
+        tmp = WAIT_TEST_LIB + f".tmp{os.getpid()}"
+        subprocess.run([nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"], check=True)
+        os.replace(tmp, WAIT_TEST_LIB)
+    return WAIT_TEST_LIB
 
 
 if __name__ == "__main__":

@@ -6,6 +6,9 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <mutex>
+
+#include "host_cache.h"
 #include "launch.h"
 #include "pagedkv.h"
 
@@ -16,8 +19,18 @@ constexpr int kMaxDevices = 64;
 // One error word per device: kernels record the first device-side error here.
 __device__ int g_pkv_error_word;
 
-int* g_err_ptr[kMaxDevices];
-int g_num_sms[kMaxDevices];
+// Per device: the context the cached state was resolved in, the device-side
+// address of the error word and the SM count.  Resolved on the first call
+// with that device current, and again after the context changes (a device
+// reset destroys the primary context and the module with it).  Guarded by a
+// mutex: host threads may make their first calls at the same time.
+struct DeviceState {
+  uint64_t ctx;
+  int* err;
+  int num_sms;
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_dev_mu;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -25,22 +38,24 @@ int elem_bytes(pkv_dtype d) { return d == PKV_BF16 ? 2 : 4; }
 
 bool dtype_ok(pkv_dtype d) { return d == PKV_F32 || d == PKV_BF16; }
 
-// Device-side address of this device's error word and its SM count; resolved
-// once per device with that device current.
 pkv_status device_state(int** err, int* num_sms) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_ECUDA;
-  if (!g_err_ptr[dev]) {
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceState& s = g_dev[dev];
+  uint64_t ctx = pkv::current_context_id();
+  if (!s.err || ctx == 0 || ctx != s.ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_pkv_error_word) != cudaSuccess) return PKV_ECUDA;
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return PKV_ECUDA;
-    g_num_sms[dev] = sms;
-    g_err_ptr[dev] = static_cast<int*>(p);
+    s.num_sms = sms;
+    s.err = static_cast<int*>(p);
+    s.ctx = pkv::current_context_id();   // now that the runtime made one current
   }
-  *err = g_err_ptr[dev];
-  *num_sms = g_num_sms[dev];
+  *err = s.err;
+  *num_sms = s.num_sms;
   return PKV_OK;
 }
 

@@ -25,7 +25,13 @@ enum DevErr : int {
 // Wait limits: 2^31 SM cycles (about 1 s at GB300 clocks), checked every 64
 // polls with the SM-local cycle counter (cheap, unlike %globaltimer), and at
 // most 2^28 polls in any case.
+#ifdef PKV_TEST_WAIT_TIMEOUT
+// Test build only (never the shipped library): waits give up after 2^22
+// cycles, about 2 ms, so a test can make one run out quickly.
+constexpr long long kWaitLimitCycles = 1ll << 22;
+#else
 constexpr long long kWaitLimitCycles = 1ll << 31;
+#endif
 constexpr unsigned int kWaitLimitIters = 1u << 28;
 
 __device__ __forceinline__ void record_error(int* err, int code) {

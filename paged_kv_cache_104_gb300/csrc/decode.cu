@@ -39,6 +39,7 @@
 //    first chunk_prior + b + 1 tokens of one block-table row.
 #include "common.cuh"
 #include "decode_common.cuh"
+#include "host_cache.h"
 #include "launch.h"
 
 namespace pkv {
@@ -474,8 +475,7 @@ cudaError_t launch_typed(const DecodeArgs& a, int num_sms, cudaStream_t stream) 
   if (a.split_tokens % C::STAGE_TOK != 0) return cudaErrorInvalidValue;
   const size_t smem = C::FIXED_SMEM + sizeof(int) * (size_t)(a.num_seqs + 1);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<T, D, G>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = allow_dynamic_smem(decode_split_kernel<T, D, G>, (int)smem);
   if (e != cudaSuccess) return e;
   const int per_sm = smem <= 110 * 1024 ? 2 : 1;
   const int64_t upper = (int64_t)a.num_seqs * a.num_kv_heads * a.max_splits;

@@ -33,6 +33,7 @@
 
 #include "common.cuh"
 #include "decode_common.cuh"
+#include "host_cache.h"
 #include "launch.h"
 #include "tmap.h"
 
@@ -493,8 +494,7 @@ cudaError_t launch_fp8_g(const DecodeArgs& args, int num_sms, cudaStream_t strea
     return cudaErrorInvalidValue;
   const size_t smem = C::OFF_CU + sizeof(int) * (size_t)(a.num_seqs + 1) + 1024;
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(decode_fp8_kernel<G>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = allow_dynamic_smem(decode_fp8_kernel<G>, (int)smem);
   if (e != cudaSuccess) return e;
   const int by_smem = (int)((228 * 1024) / (smem + 1024));
   const int per_sm = by_smem < 1 ? 1 : (by_smem > (G <= 8 ? 3 : 2) ? (G <= 8 ? 3 : 2) : by_smem);

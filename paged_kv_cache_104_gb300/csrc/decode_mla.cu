@@ -29,6 +29,7 @@
 
 #include "common.cuh"
 #include "decode_common.cuh"
+#include "host_cache.h"
 #include "launch.h"
 #include "tmap.h"
 
@@ -457,8 +458,7 @@ cudaError_t launch_decode_mla(const DecodeArgs& args, int num_sms, cudaStream_t 
   if (!encode_pool_map_bf16(&tm_c, a.k_cache, rows)) return cudaErrorInvalidValue;
   const size_t smem = OFF_CU_L + sizeof(int) * (size_t)(a.num_seqs + 1) + 1024;
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(decode_mla_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = allow_dynamic_smem(decode_mla_kernel, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t upper = (int64_t)a.num_seqs * a.max_splits;
   const int grid = (int)(upper < (int64_t)num_sms ? upper : (int64_t)num_sms);

@@ -48,6 +48,7 @@
 
 #include "common.cuh"
 #include "decode_common.cuh"
+#include "host_cache.h"
 #include "launch.h"
 #include "tmap.h"
 
@@ -178,6 +179,13 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
 
   if (warp == kCW) {
     // ------------------------------------------------------------ producer
+#ifdef PKV_TEST_WAIT_TIMEOUT
+    // Test build only: the producer withholds every stage before issuing any
+    // copy.  The consumers' first waits then run out with nothing in flight;
+    // they record PKV_DEVERR_TIMEOUT, skip every later wait, and the kernel
+    // returns.
+    return;
+#endif
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
@@ -538,8 +546,7 @@ cudaError_t launch_g(const DecodeArgs& args, int num_sms, cudaStream_t stream, b
     return cudaErrorInvalidValue;
   const size_t smem = C::OFF_CU + sizeof(int) * (size_t)(a.num_seqs + 1) + 1024;
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<G, FUSE>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = allow_dynamic_smem(decode_mma_kernel<G, FUSE>, (int)smem);
   if (e != cudaSuccess) return e;
   const int by_smem = (int)((228 * 1024) / (smem + 1024));
   const int per_sm = by_smem < 1 ? 1 : (by_smem > (G <= 8 ? 3 : 2) ? (G <= 8 ? 3 : 2) : by_smem);

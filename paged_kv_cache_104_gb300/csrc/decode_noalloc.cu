@@ -20,11 +20,14 @@
 // The first call on a device resolves the array's device address with
 // cudaGetSymbolAddress (host code only sees a host-side stand-in for the
 // array, which a kernel must never be given).  Make that first call before
-// capturing any stream.
+// capturing any stream.  After a device reset the next call resolves the
+// address again, in the new context; that call, too, belongs before any
+// capture.
 #include <cuda_runtime.h>
 
 #include <mutex>
 
+#include "host_cache.h"
 #include "pagedkv.h"
 
 namespace {
@@ -33,20 +36,31 @@ constexpr int kMaxDevicesNA = 64;
 
 static __device__ __align__(256) unsigned char g_decode_scratch[PKV_NOALLOC_SCRATCH_BYTES];
 
-void* g_scratch_addr[kMaxDevicesNA];
+// Per device: the array's device address and the context it was resolved in.
+struct ScratchAddr {
+  uint64_t ctx;
+  void* addr;
+};
+ScratchAddr g_scratch_addr[kMaxDevicesNA];
 std::mutex g_scratch_mu;
 
-// Device address of g_decode_scratch on the current device (set up once per device).
+// Device address of g_decode_scratch on the current device.  Resolved on the
+// first call with that device current, and again when the context has
+// changed since (a device reset destroys the primary context, and with it the
+// array; the address resolved before it would point into freed memory).
 pkv_status scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesNA) return PKV_ECUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  ScratchAddr& s = g_scratch_addr[dev];
+  const uint64_t ctx = pkv::current_context_id();
+  if (!s.addr || ctx == 0 || ctx != s.ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p) return PKV_ECUDA;
-    g_scratch_addr[dev] = p;
+    s.addr = p;
+    s.ctx = pkv::current_context_id();
   }
-  *out = g_scratch_addr[dev];
+  *out = s.addr;
   return PKV_OK;
 }
 

@@ -75,6 +75,7 @@
 #include <type_traits>
 
 #include "common.cuh"
+#include "host_cache.h"
 #include "launch.h"
 #include "tc_common.cuh"
 #include "tmap.h"
@@ -607,8 +608,7 @@ cudaError_t launch_prefill_pair(const PrefillArgs& a, cudaStream_t stream, int p
   if (p.q_tiles == 0) return cudaSuccess;
   CUtensorMap tm_q;
   if (!encode_rows_map_bf16(&tm_q, a.q, a.chunk_len, a.num_q_heads)) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  cudaError_t e = allow_dynamic_smem(prefill_pair_kernel, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   p.rows_mode = rows_mode_for(a) ? 1 : 0;
   const int n_x = p.rows_mode ? a.num_q_heads : a.num_q_heads / 2;
