@@ -649,13 +649,14 @@ def run_mla_decode(args, w, lay, dev, stream, dist, n):
         "decode_tokens_per_s": n * nd / (ms_step / 1e3),
         "decode_ms_per_layer": dec_ms,
         "distinct_layer_pools": n_pools, "pool_gb_per_layer": pool_bytes / 1e9,
-        "gpu_launches": args.steps * L * (1 + 3 + (1 if msl > 512 else 0)),
+        # per layer: latent_append, query absorption, attention, merge + up-projection
+        "gpu_launches": args.steps * L * 4,
         "roofline": {
-            "kernel": "mla_decode_attention (absorb GEMM + attention over the latent + merge + "
-                      "up-projection GEMM)", "bound": "hbm",
+            "kernel": "mla_decode_attention (query absorption + tcgen05 attention over the "
+                      "latents + fused merge and up-projection)", "bound": "hbm",
             "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": dec_gbs / hbm_peak,
             "traffic": None, "algorithmic_bytes_per_launch": dec_bytes,
-            "traffic_note": "the call is four launches; ncu traffic is recorded for the "
+            "traffic_note": "the call is three launches; ncu traffic is recorded for the "
                             "attention kernel alone (profiles/traffic.json, decode_mla_kernel)",
             "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
             else "fallback 6.8 TB/s",

@@ -551,10 +551,8 @@ pkv_status pkv_mla_decode_attention(void* out, const void* q, const void* w_k, c
   a.scale = scale;
   a.chunk_prior = -1;
   a.is_bf16 = 1;
-  if (pkv::launch_decode_mla(a, sms, s) != cudaSuccess) return PKV_ECUDA;
-  // 3) o_h = W_V[h] z_h
-  if (pkv::launch_gemm_heads(out, z, w_v, num_seqs, num_q_heads, true, s) != cudaSuccess)
-    return PKV_ECUDA;
+  // 3) merge of the partials fused with o_h = W_V[h] z_h
+  if (pkv::launch_decode_mla(a, w_v, out, sms, s) != cudaSuccess) return PKV_ECUDA;
   return PKV_OK;
 }
 

@@ -22,9 +22,12 @@ __device__ __forceinline__ int row_len(const DecodeArgs& a, int b) {
 }
 
 // Build cu[0..B] with warp 0: per sequence, num_kv_heads times the number of
-// split_tokens-token splits (stage_tok = 0) or of stage_tok-token stages,
-// prefix-summed.
-__device__ __forceinline__ void plan_units(const DecodeArgs& a, int* cu, int stage_tok = 0) {
+// split_tokens-token splits (stage_tok = 0) or of stage_tok-token stages
+// plus `pad` stages that hold no tokens, prefix-summed.  The padding stands
+// for the fixed cost of a piece (loading its queries, writing its result):
+// a CTA whose share starts many short sequences then gets fewer tokens.
+__device__ __forceinline__ void plan_units(const DecodeArgs& a, int* cu, int stage_tok = 0,
+                                           int pad = 0) {
   const int lane = threadIdx.x & 31;
   constexpr unsigned kAll = 0xffffffffu;
   if (threadIdx.x < 32) {
@@ -40,7 +43,7 @@ __device__ __forceinline__ void plan_units(const DecodeArgs& a, int* cu, int sta
           record_error(a.err, DEVERR_SEQLEN_RANGE);
         } else {
           const int per = stage_tok > 0 ? stage_tok : a.split_tokens;
-          units = a.num_kv_heads * ((n + per - 1) / per);
+          units = a.num_kv_heads * ((n + per - 1) / per + (stage_tok > 0 ? pad : 0));
         }
       }
       int x = units;
@@ -104,8 +107,9 @@ constexpr int kMinStagesPerCta = kSplitTokens / 64;
 
 // True if the stage prefix sums of this call fit an int: every counted
 // sequence has at most max_seq_len tokens (longer ones are rejected).
-inline bool stage_plan_fits(const DecodeArgs& a, int stage_tok) {
-  return (int64_t)a.num_seqs * a.num_kv_heads * ((a.max_seq_len + stage_tok - 1) / stage_tok) <
+inline bool stage_plan_fits(const DecodeArgs& a, int stage_tok, int pad = 0) {
+  return (int64_t)a.num_seqs * a.num_kv_heads *
+             ((a.max_seq_len + stage_tok - 1) / stage_tok + pad) <
          (int64_t)INT_MAX;
 }
 
@@ -124,32 +128,41 @@ __device__ __forceinline__ Walk walk_begin(const DecodeArgs& a, const int* cu, b
   return k;
 }
 
-// Next unit of this CTA (false when done).  stage_tok: tokens per stage.
+// Next unit of this CTA (false when done).  stage_tok: tokens per stage;
+// pad: the empty stages plan_units put after every stream (a CTA's share
+// may end, or lie entirely, inside them: those are skipped).
 __device__ __forceinline__ bool walk_next(const DecodeArgs& a, const int* cu, int stage_tok,
-                                          Walk& k, Unit& u) {
+                                          Walk& k, Unit& u, int pad = 0) {
   if (!k.balanced) {
     if (k.w >= k.total) return false;
     u = find_unit(a, cu, k.w);
     k.w += gridDim.x;
     return true;
   }
-  if (k.pos >= k.end) return false;
-  const int b = seq_of(a, cu, k.pos);
-  const int nst = (cu[b + 1] - cu[b]) / a.num_kv_heads;   // stages of one stream
-  const int rem = (int)(k.pos - cu[b]);
-  const int g = rem / nst;
-  const int st0 = rem - g * nst;
-  const int64_t s_begin = (int64_t)cu[b] + (int64_t)g * nst, s_end = s_begin + nst;
-  const int len = (int)(min(k.end, s_end) - k.pos);
-  const int c0 = cta_of_stage(s_begin, k.total);
-  u.b = b;
-  u.g = g;
-  u.s = (int)blockIdx.x - c0;
-  u.ns = cta_of_stage(s_end - 1, k.total) - c0 + 1;
-  u.tok_begin = st0 * stage_tok;
-  u.tok_end = min(row_len(a, b), (st0 + len) * stage_tok);
-  k.pos += len;
-  return true;
+  while (k.pos < k.end) {
+    const int b = seq_of(a, cu, k.pos);
+    const int nst = (cu[b + 1] - cu[b]) / a.num_kv_heads;   // stages of one stream
+    const int real = nst - pad;                              // the stream's own stages
+    const int rem = (int)(k.pos - cu[b]);
+    const int g = rem / nst;
+    const int st0 = rem - g * nst;
+    const int64_t s_begin = (int64_t)cu[b] + (int64_t)g * nst, s_end = s_begin + real;
+    if (st0 >= real) {   // inside the padding: nothing to do up to the next stream
+      k.pos = min(k.end, s_begin + nst);
+      continue;
+    }
+    const int len = (int)(min(k.end, s_end) - k.pos);
+    const int c0 = cta_of_stage(s_begin, k.total);
+    u.b = b;
+    u.g = g;
+    u.s = (int)blockIdx.x - c0;
+    u.ns = cta_of_stage(s_end - 1, k.total) - c0 + 1;
+    u.tok_begin = st0 * stage_tok;
+    u.tok_end = min(row_len(a, b), (st0 + len) * stage_tok);
+    k.pos += len;
+    return true;
+  }
+  return false;
 }
 
 }  // namespace pkv

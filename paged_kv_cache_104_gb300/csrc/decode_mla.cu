@@ -1,5 +1,4 @@
-// Decode attention over a latent (MLA-style) KV cache, on warp-level bf16
-// tensor-core tiles (mma.sync m16n8k16, fp32 accumulate) for sm_103a.
+// Decode attention over a latent (MLA-style) KV cache on tcgen05 (sm_103a).
 //
 // What it computes.  "The KV cache and prefix caching", section "What prefill
 // stores and decode reads", names multi-head latent attention (the DeepSeek
@@ -8,161 +7,293 @@
 // With the projections absorbed -- q~_h = W_K[h]^T q_h before this kernel and
 // o_h = W_V[h] z_h after it -- the attention over the latent is
 //   z_h = sum_j softmax_j(scale * q~_h . c_j) c_j,
-// i.e. grouped-query decode with a single KV head whose key and value are both
-// the latent, shared by all Hq query heads.  This kernel computes z (rank 128,
-// 32 query heads).
+// grouped-query decode with a single KV head whose key and value are both the
+// latent, shared by all 32 query heads.  This kernel computes z (rank 128).
 //
-// Structure: the bf16 decode kernel's (persistent CTAs walking the sequences
-// in equal per-CTA shares of 64-token stages, or 512-token splits for small
-// batches; one TMA producer warp; keys on the M side of the
-// tile and heads on N; the running max gated by a warp vote; split partials
-// merged by the reduce kernel), with two changes for the 32 heads that share
-// each latent block:
-//  * a block is loaded once (16 rows x 256 B) and serves as both the K and the
-//    V operand;
-//  * eight consumer warps: warp w takes block w % 4 of each stage for the
-//    query heads 16 * (w / 4) .. + 15, so each staged block feeds two warps;
-//  * a register split (setmaxnreg): the producer warp and three idle warps
-//    completing its warpgroup drop to 40 registers so the consumers can take
-//    232; at the 168 of the launch the consumers spilled.
+// Every latent byte feeds 32 heads x 2 products, eight times the multiply
+// work per byte of the GQA decode, so the products go to the tensor core and
+// the warps keep only the softmax.  Per 128-key tile of latents (32 KiB):
+//   S^T  = C . Q~^T    M = 128 keys,  N = 32 heads,   K = 128 rank
+//   O^T += C^T . P^T   M = 128 rank,  N = 64 (32 heads, 32 unused), K = 128 keys
+// The tile C is read by both products from the same shared-memory copy: as a
+// K-major A operand for the scores and as an MN-major A operand for P V.
+// S^T and O^T live in TMEM (fp32); P^T goes through shared memory (bf16, the
+// B operand), heads contiguous per key.
+//
+// Layout of a tile.  Each 16-token block (4 KiB) arrives in one TMA box of a
+// 4-D view of the pool (column, row of 8, half, 8-row group) and lands as
+// [row group][half][8 rows][128 B] with the 128-byte swizzle: every 8 keys x
+// 64 rank columns are one 1 KiB swizzle atom.  For the score product the
+// atoms of one half follow each other every 2 KiB along the keys; for P V the
+// two rank halves of an atom pair sit 1 KiB apart and the 8-key atoms 2 KiB
+// apart.  One box per block halves the TMA issue count of two 2 KiB boxes,
+// and eight lanes of the producer warp issue a tile's boxes side by side.
+//
+// Roles (192 threads, one CTA per SM):
+//   warps 0-3  softmax.  Thread j owns key j of each tile (TMEM lane j of
+//              S^T) and rank dimension j of O^T.  The running max per head
+//              (log2 domain) only has to bound the scores to within 2^8: one
+//              barrier reduction (bar.red.or) over the 128 threads decides
+//              whether any score exceeds it, and only then is the exact max
+//              over the tile's keys taken (warp transposes, then shared
+//              memory) and O^T rescaled in TMEM.  Each thread keeps the sum of
+//              its own keys' weights per head; they are added up once per
+//              unit.  Rows of keys past a sequence's end are zeroed in the
+//              tile, so stale pool bytes (even NaN) never meet p = 0 in P V.
+//   warp 4     TMA producer: the unit's q~ (32 rows) into a two-buffer ring,
+//              the latent blocks of each tile into a four-tile ring.
+//   warp 5     TMEM allocator and MMA issuer (converged warp, one elected
+//              lane per instruction).  It polls what S^T of the next tile and
+//              P V of the oldest softmaxed tile wait for and issues whichever
+//              is ready, so the scores of the next tile are in flight while
+//              the softmax of this one runs, and P V never waits for latents
+//              still on their way.
+// Work: persistent CTAs take the balanced walk over 128-token stages (equal
+// shares of all sequences' stages, cut where sequences change) when the
+// batch gives every CTA at least 512 tokens, else 512-token splits; a piece
+// that covers its whole sequence writes z, the others write (m, l, O)
+// partials that the reduce kernel merges.  O^T is double-buffered across
+// pieces, so a piece's epilogue overlaps the next piece's products.
+// Every wait is bounded; on time-out the kernel records an error, stops
+// issuing work, lets its copies and products finish, frees its TMEM and
+// returns.  After an abort the softmax warps still walk their loops
+// (skipping the work), so every named barrier is reached by all of them.
 #include <cuda.h>
 
 #include "common.cuh"
 #include "decode_common.cuh"
 #include "host_cache.h"
 #include "launch.h"
+#include "tc_common.cuh"
 #include "tmap.h"
 
 namespace pkv {
 namespace {
 
-constexpr int kHeads = 32;                       // query heads sharing the latent
-constexpr int kHalfHeads = 16;                   // heads per consumer warp
-constexpr int kNTL = kHalfHeads / 8;             // head tiles of 8 per warp
-constexpr int kBPSL = 4;                         // blocks per stage
-constexpr int kCWL = 2 * kBPSL;                  // consumer warps
-constexpr int kConsumersL = kCWL * 32;
-constexpr int kThreadsL = kConsumersL + 128;     // producer warp + three idle warps (warpgroup 2)
-constexpr int kRegsConsL = 232, kRegsRestL = 40;
-static_assert(kRegsConsL * kConsumersL + kRegsRestL * 128 <= ((65536 / kThreadsL) & ~7) * kThreadsL,
-              "register split within the launch budget");
-constexpr int kStageTokL = kBPSL * kBlockSize;   // 64 tokens
-constexpr int kHalfL = kBlockSize * 128;         // 16 rows x 128 B: one 64-column half
-constexpr int kTileL = 2 * kHalfL;               // one latent block, 4 KiB
-constexpr int kStageL = kBPSL * kTileL;          // 16 KiB
-constexpr int kNSTL = 4;
-constexpr int kRingL = kNSTL * kStageL;
-constexpr int kR = 128;                          // latent rank
-constexpr int kCombRowL = kR + 4;
-constexpr float kLazyL = 8.0f;
-constexpr unsigned kAllL = 0xffffffffu;
+constexpr int kTK = 128;                        // keys per tile
+constexpr int kR = 128;                         // latent rank
+constexpr int kNH = 32;                         // query heads
+constexpr int kNPV = 64;                        // P^T / O^T columns (32 heads + 32 unused)
+constexpr int kBlkPerTile = kTK / kBlockSize;   // 8
+constexpr int kBlockBytes = kBlockSize * kR * 2;   // 4 KiB
+constexpr int kTileBytes = kTK * kR * 2;        // 32 KiB
+constexpr int kNS = 4;                          // latent ring depth (tiles)
+constexpr int kQBytes = kNH * kR * 2;           // 8 KiB: q~ of one sequence
+constexpr int kQHalf = kQBytes / 2;             // one 64-column half, 32 rows
+constexpr int kPBytes = kTK * 128;              // P^T: 128 keys x 128 B (64 columns)
+constexpr int kThreadsT = 192;
+constexpr int kSoft = 128;                      // softmax threads
+constexpr int W_PROD = 4, W_MMA = 5;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t COL_S = 0;                   // S^T of tile parity b at 32 b
+constexpr uint32_t COL_O = 64;                  // O^T of unit parity b at 64 + 64 b
+constexpr float kLazyT = 8.0f;
+constexpr unsigned kAllT = 0xffffffffu;
+constexpr int kStageTokT = kTK;                 // the balanced walk's stage: one tile
+constexpr int kMinStagesT = kSplitTokens / kStageTokT;   // shares of at least 4 stages
+// Empty stages the balanced walk counts after every sequence: what one piece
+// costs on top of its tiles (its queries, its epilogue, the first tile's
+// exact maximum), in tiles.  CTAs whose shares start many short sequences
+// then take fewer tiles.  Shares still hold at least kMinStagesT stages, so
+// a sequence of n tokens still falls to at most ceil(n / 512) + 1 CTAs.
+constexpr int kPadT = 2;
 
-constexpr int OFF_COMB_L = kRingL;                               // [warp][16 heads][132] fp32
-constexpr int OFF_ML_L = OFF_COMB_L + kCWL * kHalfHeads * kCombRowL * 4;
-constexpr int OFF_BAR_L = OFF_ML_L + kCWL * kHalfHeads * 2 * 4;
-constexpr int OFF_CU_L = OFF_BAR_L + 2 * kNSTL * 8 + 16;
+constexpr int OFF_RING = 0;
+constexpr int OFF_Q = OFF_RING + kNS * kTileBytes;          // [2] q~
+constexpr int OFF_P = OFF_Q + 2 * kQBytes;                  // [2] P^T
+constexpr int OFF_RED = OFF_P + 2 * kPBytes;                // [2][32 heads][4 warps] fp32 (max)
+constexpr int OFF_SUM = OFF_RED + 2 * kNH * 4 * 4;          // [2][32 heads][4 warps] fp32 (sums)
+constexpr int OFF_BAR = OFF_SUM + 2 * kNH * 4 * 4;
 
-static_assert(kSplitTokens % kStageTokL == 0, "a split holds whole stages");
-static_assert(32 % kBPSL == 0, "a stage never straddles two block-id windows");
+enum {
+  B_CF = 0,                 // [kNS] latent tile landed
+  B_CE = B_CF + kNS,        // [kNS] latent tile consumed (both products done)
+  B_QF = B_CE + kNS,        // [2]  q~ landed
+  B_QE = B_QF + 2,          // [2]  q~ consumed (last S^T of its unit done)
+  B_SF = B_QE + 2,          // [2]  S^T ready
+  B_SE = B_SF + 2,          // [2]  S^T read out by the softmax
+  B_PF = B_SE + 2,          // [2]  P^T written (and invalid rows of C zeroed)
+  B_PE = B_PF + 2,          // [2]  P V of that tile done (P^T free, O^T settled)
+  B_OF = B_PE + 2,          // [2]  O^T of a unit complete
+  B_OE = B_OF + 2,          // [2]  O^T read out by the epilogue
+  B_DRAIN = B_OE + 2,       // the MMA warp's last products done
+  B_COUNT = B_DRAIN + 1
+};
+constexpr int OFF_TSLOT = OFF_BAR + B_COUNT * 8;
+constexpr int OFF_ABORT = OFF_TSLOT + 4;
+constexpr int OFF_CU = OFF_TSLOT + 16;
+static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "swizzled operands need 1 KiB alignment");
+static_assert(kSplitTokens % kTK == 0, "a split holds whole tiles");
+static_assert(32 % kBlkPerTile == 0, "a tile never straddles two block-id windows");
 
-__device__ __forceinline__ void mma16816l(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+// kind::f16 instruction descriptor with both operands MN-major (A = C^T).
+__host__ __device__ constexpr uint32_t idesc_mn_mn(int m, int n) {
+  return make_idesc(true, m, n) | (1u << 15);
+}
+
+__device__ __forceinline__ void tma4d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int w,
+                                      uint64_t policy) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %3, %3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(0), "r"(w), "l"(policy)
+      : "memory");
 }
-__device__ __forceinline__ uint32_t pack2_bf16l(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-__device__ __forceinline__ uint32_t movm_tl(uint32_t x) {
-  uint32_t d;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(x));
-  return d;
-}
-__device__ __forceinline__ uint32_t prmtl(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t d;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-  return d;
-}
-__device__ __forceinline__ float ex2l(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ uint4 lds128l(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ void tma2d_l(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x,
-                                        int y, uint64_t policy) {
+__device__ __forceinline__ void tma2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x,
+                                      int y) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
       : "memory");
 }
 
-__global__ void __launch_bounds__(kThreadsL, 1)
-decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c) {
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+// OR of `pred` over the `count` threads of named barrier `id` (a barrier too)
+__device__ __forceinline__ bool bar_red_or(bool pred, int id, int count) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, %2, %3, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
+// Lane l returns OP over the warp's lanes of element l of v (v is consumed):
+// a butterfly that halves the elements each lane carries at every step.
+template <bool kMax>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[32], int lane) {
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool upper = (lane & w) != 0;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float send = upper ? v[i] : v[i + w];
+      const float keep = upper ? v[i + w] : v[i];
+      const float got = __shfl_xor_sync(kAllT, send, w);
+      v[i] = kMax ? fmaxf(keep, got) : keep + got;
+    }
+  }
+  return v[0];
+}
+
+// Per-tile facts every role derives the same way from the walk.
+struct TileInfo {
+  int tok0;      // first token of the tile in its sequence
+  int valid;     // keys of the tile inside the piece (1..128)
+  bool first;    // first tile of its piece
+  bool last;     // last tile of its piece
+};
+
+__global__ void __launch_bounds__(kThreadsT, 1)
+decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c,
+                  const __grid_constant__ CUtensorMap tm_q) {
+  extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t sbase = smem_u32(smem);
-  float* comb = reinterpret_cast<float*>(smem + OFF_COMB_L);
-  float* comb_ml = reinterpret_cast<float*>(smem + OFF_ML_L);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR_L);
-  int* abort_flag = reinterpret_cast<int*>(bars + 2 * kNSTL);
-  int* cu = reinterpret_cast<int*>(smem + OFF_CU_L);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TSLOT);
+  int* abort_i = reinterpret_cast<int*>(smem + OFF_ABORT);
+  volatile int* abort_flag = abort_i;
+  int* cu = reinterpret_cast<int*>(smem + OFF_CU);
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+  if (sbase & 1023u) {  // swizzled operand tiles need a 1 KiB-aligned base
+    if (threadIdx.x == 0) record_error(a.err, DEVERR_SMEM_LAYOUT);
+    return;
+  }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kNSTL);
 
   if (tid == 0) {
-    for (int i = 0; i < kNSTL; ++i) {
-      mbar_init(full0 + 8 * i, 1);
-      mbar_init(empty0 + 8 * i, kCWL);
+    for (int i = 0; i < kNS; ++i) {
+      mbar_init(bar(B_CF + i), 1);
+      mbar_init(bar(B_CE + i), 1);
     }
-    *abort_flag = 0;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(B_QF + i), 1);
+      mbar_init(bar(B_QE + i), 1);
+      mbar_init(bar(B_SF + i), 1);
+      mbar_init(bar(B_SE + i), 4);    // one arrival per softmax warp
+      mbar_init(bar(B_PF + i), 4);
+      mbar_init(bar(B_PE + i), 1);
+      mbar_init(bar(B_OF + i), 1);
+      mbar_init(bar(B_OE + i), 4);
+    }
+    mbar_init(bar(B_DRAIN), 1);
+    *abort_i = 0;
     fence_mbar_init();
   }
-  // balanced walk over 64-token stages when the batch gives every CTA at
-  // least kMinStagesPerCta of them; otherwise 512-token splits
-  plan_units(a, cu, a.balanced ? kStageTokL : 0);
+  // P^T columns 32..63 are never written: zero them once (they only feed the
+  // unused O^T columns, but stay finite)
+  for (int i = tid; i < 2 * kPBytes / 16; i += kThreadsT)
+    reinterpret_cast<uint4*>(smem + OFF_P)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
+  if (warp == W_MMA) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  // balanced walk over 128-token stages when the batch gives every CTA at
+  // least 512 tokens; otherwise 512-token splits
+  plan_units(a, cu, a.balanced ? kStageTokT : 0, kPadT);
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
   const bool balanced =
-      a.balanced && (int64_t)cu[a.num_seqs] >= (int64_t)kMinStagesPerCta * gridDim.x;
+      a.balanced && (int64_t)cu[a.num_seqs] >= (int64_t)kMinStagesT * gridDim.x;
   if (a.balanced && !balanced) {
     __syncthreads();
     plan_units(a, cu);
     __syncthreads();
   }
-  volatile int* vabort = abort_flag;
+  const uint32_t tmem = *tmem_slot;
 
-  if (warp >= kCWL) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsRestL));
-  if (warp > kCWL) return;   // idle warps of warpgroup 2
-  if (warp == kCWL) {
+  auto tile_info = [&](const Unit& u, int i, int ntile) {
+    TileInfo ti;
+    ti.tok0 = u.tok_begin + i * kTK;
+    ti.valid = min(kTK, u.tok_end - ti.tok0);
+    ti.first = i == 0;
+    ti.last = i == ntile - 1;
+    return ti;
+  };
+  auto tiles_of = [&](const Unit& u) { return (u.tok_end - u.tok_begin + kTK - 1) / kTK; };
+
+  if (warp == W_PROD) {
     // ------------------------------------------------------------ producer
-    if (lane == 0)
+    if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_c)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
+    }
     const uint64_t policy = policy_evict_first();
-    uint32_t issued = 0;
+    uint32_t t = 0, ui = 0;
     bool ok = true;
     Walk wk = walk_begin(a, cu, balanced);
     Unit u;
-    while (ok && walk_next(a, cu, kStageTokL, wk, u)) {
+    // q~ comes from the kernel before this one in the stream (launched as its
+    // programmatic dependent, this grid may start before it has finished)
+    if (lane == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+    while (ok && walk_next(a, cu, kStageTokT, wk, u, kPadT)) {
+      // this piece's q~ (32 rows of the absorbed queries)
+      if (lane == 0) {
+        if (ui >= 2) ok = wait_or_abort(bar(B_QE + (ui & 1)), ((ui >> 1) - 1) & 1, abort_flag, a.err);
+        if (ok) {
+          const uint32_t qb = sbase + OFF_Q + (ui & 1) * kQBytes;
+          mbar_arrive_expect_tx(bar(B_QF + (ui & 1)), kQBytes);
+          tma2d(qb, &tm_q, bar(B_QF + (ui & 1)), 0, u.b * kNH);
+          tma2d(qb + kQHalf, &tm_q, bar(B_QF + (ui & 1)), 64, u.b * kNH);
+        }
+      }
+      ok = __shfl_sync(kAllT, (int)ok, 0) != 0;
+      if (!ok) break;
+      ++ui;
       const int blk0 = u.tok_begin / kBlockSize;
       const int nblk = (u.tok_end - 1) / kBlockSize - blk0 + 1;
       const int32_t* bt_row = a.block_table + (int64_t)u.b * a.bt_stride + blk0;
+      const int ntile = tiles_of(u);
       int my_blk = 0;
-      const int nst = (nblk + kBPSL - 1) / kBPSL;
-      for (int st = 0; st < nst; ++st, ++issued) {
-        if ((st * kBPSL) % 32 == 0) {  // next window of 32 block ids, one per lane
-          const int idx = st * kBPSL + lane;
+      for (int i = 0; i < ntile; ++i, ++t) {
+        if ((i * kBlkPerTile) % 32 == 0) {  // next window of 32 block ids, one per lane
+          const int idx = i * kBlkPerTile + lane;
           my_blk = 0;
           if (idx < nblk) {
             my_blk = __ldg(bt_row + idx);
@@ -172,300 +303,336 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c) 
             }
           }
         }
-        const int buf = issued % kNSTL;
-        const uint32_t phase = (issued / kNSTL) & 1;
-        if (lane == 0 && issued >= (uint32_t)kNSTL && !*vabort) {
-          if (!mbar_wait(empty0 + 8 * buf, phase ^ 1, a.err)) *vabort = 1;
-        }
+        const int slot = t % kNS;
+        if (lane == 0 && t >= (uint32_t)kNS)
+          ok = wait_or_abort(bar(B_CE + slot), ((t / kNS) - 1) & 1, abort_flag, a.err);
+        ok = __shfl_sync(kAllT, (int)ok, 0) != 0;
+        if (!ok) break;
+        const int nb = min(kBlkPerTile, nblk - i * kBlkPerTile);
+        const int blk = __shfl_sync(kAllT, my_blk, (i * kBlkPerTile + (lane & 7)) & 31);
+        const uint32_t fb = bar(B_CF + slot);
+        if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)(nb * kBlockBytes));
         __syncwarp();
-        if (*vabort) { ok = false; break; }
-        const int nb = min(kBPSL, nblk - st * kBPSL);
-        int rows[kBPSL];
+        if (lane < nb)
+          tma4d(sbase + OFF_RING + slot * kTileBytes + lane * kBlockBytes, &tm_c, fb, 2 * blk, policy);
+      }
+    }
+    if (!ok && lane == 0) {  // after an abort, let the copies already issued land
+      const uint32_t first = t > (uint32_t)kNS ? t - kNS : 0;
+      for (uint32_t i = first; i < t; ++i) mbar_wait(bar(B_CF + (i % kNS)), (i / kNS) & 1, nullptr);
+      const uint32_t qfirst = ui > 2u ? ui - 2 : 0;
+      for (uint32_t i = qfirst; i < ui; ++i) mbar_wait(bar(B_QF + (i & 1)), (i >> 1) & 1, nullptr);
+    }
+  } else if (warp == W_MMA) {
+    // ------------------------------------------------------------- MMA issuer
+    constexpr uint32_t idesc_s = make_idesc(false, kTK, kNH);
+    constexpr uint32_t idesc_o = idesc_mn_mn(kR, kNPV);
+    // Two cursors over the same walk: the next tile whose S^T is to be
+    // issued and the next tile whose P V is.  The warp polls the barriers
+    // both wait on and issues whichever product is ready first (S^T when
+    // both are), so P V of a tile never waits for the next tile's latents
+    // and a tile's ring slot is released as soon as its softmax is done.
+    Walk wks = walk_begin(a, cu, balanced), wkp = walk_begin(a, cu, balanced);
+    Unit us, up;
+    bool has_s = walk_next(a, cu, kStageTokT, wks, us, kPadT);
+    bool has_p = walk_next(a, cu, kStageTokT, wkp, up, kPadT);
+    int is_i = 0, is_n = has_s ? tiles_of(us) : 0;
+    int ip_i = 0, ip_n = has_p ? tiles_of(up) : 0;
+    uint32_t ts = 0, uis = 0, tp = 0, uip = 0;
+    bool idle = false;
+    long long t_idle = 0;
+    while (true) {
+      const bool s_cand = has_s, p_cand = has_p && tp < ts;
+      if (!s_cand && !p_cand) break;
+      // lane 0 probes the barriers; the warp follows its decision
+      int act = 0;   // 1: S^T, 2: P V, 3: give up
+      if (lane == 0) {
+        if (s_cand && mbar_test(bar(B_QF + (uis & 1)), (uis >> 1) & 1) &&
+            mbar_test(bar(B_CF + (ts % kNS)), (ts / kNS) & 1) &&
+            (ts < 2 || mbar_test(bar(B_SE + (ts & 1)), ((ts >> 1) - 1) & 1)))
+          act = 1;
+        else if (p_cand && mbar_test(bar(B_PF + (tp & 1)), (tp >> 1) & 1) &&
+                 (ip_i != 0 || uip < 2 || mbar_test(bar(B_OE + (uip & 1)), ((uip >> 1) - 1) & 1)))
+          act = 2;
+        else if (*abort_flag)
+          act = 3;
+        else if (!idle)
+          t_idle = clock64();
+        else if (clock64() - t_idle > kWaitLimitCycles) {
+          record_error(a.err, DEVERR_TIMEOUT);
+          *abort_flag = 1;
+          act = 3;
+        }
+      }
+      act = __shfl_sync(kAllT, act, 0);
+      if (act == 3) break;   // aborted: nothing more is issued
+      idle = act == 0;
+      if (act == 1) {
+        tc_fence_after();
+        const uint32_t ct = sbase + OFF_RING + (ts % kNS) * kTileBytes;
+        const uint32_t qb = sbase + OFF_Q + (uis & 1) * kQBytes;
 #pragma unroll
-        for (int i = 0; i < kBPSL; ++i)
-          rows[i] = __shfl_sync(kAllL, my_blk, (st * kBPSL + i) & 31) * kBlockSize;
-        if (lane == 0) {
-          const uint32_t fb = full0 + 8 * buf;
-          mbar_arrive_expect_tx(fb, (uint32_t)(nb * kTileL));
-          const uint32_t dst = sbase + buf * kStageL;
+        for (int k = 0; k < kR / 16; ++k) {
+          // A = C (K-major): rank half k/4, 32 bytes per 16 columns; 8-key atoms 2 KiB apart
+          const uint64_t ad = make_sw128_desc(ct + (k >> 2) * 1024 + (k & 3) * 32, 16, 2048);
+          // B = Q~ (K-major): 8-head atoms 1 KiB apart, halves 4 KiB apart
+          const uint64_t bd = make_sw128_desc(qb + (k >> 2) * kQHalf + (k & 3) * 32, 16, 1024);
+          mma_ss_e(tmem + COL_S + (ts & 1) * kNH, ad, bd, idesc_s, k > 0 ? 1u : 0u);
+        }
+        commit_e(bar(B_SF + (ts & 1)));
+        if (is_i == is_n - 1) commit_e(bar(B_QE + (uis & 1)));   // q~ buffer read
+        ++ts;
+        if (++is_i == is_n) {
+          ++uis;
+          has_s = walk_next(a, cu, kStageTokT, wks, us, kPadT);
+          is_i = 0;
+          is_n = has_s ? tiles_of(us) : 0;
+        }
+      } else if (act == 2) {
+        tc_fence_after();
+        const bool first = ip_i == 0, last = ip_i == ip_n - 1;
+        const uint32_t ct = sbase + OFF_RING + (tp % kNS) * kTileBytes;
+        const uint32_t pt = sbase + OFF_P + (tp & 1) * kPBytes;
 #pragma unroll
-          for (int i = 0; i < kBPSL; ++i) {
-            if (i < nb) {
-              tma2d_l(dst + i * kTileL, &tm_c, fb, 0, rows[i], policy);
-              tma2d_l(dst + i * kTileL + kHalfL, &tm_c, fb, 64, rows[i], policy);
-            }
-          }
+        for (int kk = 0; kk < kTK / 16; ++kk) {
+          // A = C^T (MN-major): rank halves 1 KiB apart, 8-key atoms 2 KiB apart
+          const uint64_t ad = make_sw128_desc(ct + kk * 2 * 2048, 1024, 2048);
+          // B = P^T (MN-major): 8-key atoms of 128-byte rows, 1 KiB apart
+          const uint64_t bd = make_sw128_desc(pt + kk * 16 * 128, 16, 1024);
+          mma_ss_e(tmem + COL_O + (uip & 1) * kNPV, ad, bd, idesc_o, (first && kk == 0) ? 0u : 1u);
+        }
+        commit_e(bar(B_CE + (tp % kNS)));
+        commit_e(bar(B_PE + (tp & 1)));
+        if (last) commit_e(bar(B_OF + (uip & 1)));
+        ++tp;
+        if (++ip_i == ip_n) {
+          ++uip;
+          has_p = walk_next(a, cu, kStageTokT, wkp, up, kPadT);
+          ip_i = 0;
+          ip_n = has_p ? tiles_of(up) : 0;
         }
       }
     }
-    if (!ok && lane == 0) {  // on abort, let the copies already issued land
-      const uint32_t first = issued > (uint32_t)kNSTL ? issued - kNSTL : 0;
-      for (uint32_t i = first; i < issued; ++i)
-        mbar_wait(full0 + 8 * (i % kNSTL), (i / kNSTL) & 1, nullptr);
+    // every product this warp issued completes before TMEM is freed
+    commit_e(bar(B_DRAIN));
+    mbar_wait(bar(B_DRAIN), 0, nullptr);
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int wl = warp;                          // 0..3
+    const int j = tid;                            // key of the tile / TMEM lane / rank dim
+    const uint32_t lane_base = tmem + ((uint32_t)(wl * 32) << 16);
+    const float sl2 = a.scale * 1.4426950408889634f;
+    float* red = reinterpret_cast<float*>(smem + OFF_RED);   // [2][32][4]
+    float* sum = reinterpret_cast<float*>(smem + OFF_SUM);   // [2][32][4]
+    unsigned char* prow0 = smem + OFF_P + j * 128;            // P^T row of key j (buffer 0)
+    __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(a.out);
+    // this key's place in a tile: 8-key group j/8 every 2 KiB, row j%8
+    const uint32_t crow = (uint32_t)((j >> 3) * 2048 + (j & 7) * 128);
+    float m[kNH], l[kNH];
+    uint32_t t = 0, ui = 0;
+    Walk wk = walk_begin(a, cu, balanced);
+    Unit u;
+    while (walk_next(a, cu, kStageTokT, wk, u, kPadT)) {
+      // the merge reads how many partials this sequence left
+      if (a.balanced && u.s == 0 && tid == 0) a.ws_np[u.b] = u.ns;
+#pragma unroll
+      for (int h = 0; h < kNH; ++h) {
+        m[h] = -INFINITY;
+        l[h] = 0.f;
+      }
+      const int ntile = tiles_of(u);
+      for (int i = 0; i < ntile; ++i, ++t) {
+        const TileInfo ti = tile_info(u, i, ntile);
+        wait_fast(bar(B_SF + (t & 1)), (t >> 1) & 1, abort_flag, a.err);
+        __syncwarp();
+        tc_fence_after();
+        float x[kNH];
+        tmem_ld32(lane_base + COL_S + (t & 1) * kNH, x);
+        tmem_wait_ld();
+        reg_fence(x);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_SE + (t & 1)));
+        const bool kval = j < ti.valid;
+        // scores in the log2 domain; keys past the piece's end are -inf
+        bool grow = false;
+#pragma unroll
+        for (int h = 0; h < kNH; ++h) {
+          x[h] = kval ? x[h] * sl2 : -INFINITY;
+          grow |= x[h] > m[h] + kLazyT;
+        }
+        if (bar_red_or(grow, 1, kSoft)) {
+          // exact max per head over the tile's keys
+          float tmp[kNH];
+#pragma unroll
+          for (int h = 0; h < kNH; ++h) tmp[h] = x[h];
+          const float wm = warp_transpose_reduce<true>(tmp, lane);   // head `lane`, this warp
+          float* rb = red + (t & 1) * kNH * 4;
+          rb[lane * 4 + wl] = wm;
+          named_bar_sync(1, kSoft);
+          // lane h decides head h (the same on every warp), then the new
+          // maxima and their rescale factors go to every lane.  Per-lane code
+          // keeps this rarely run path short: unrolled over the 32 heads it
+          // missed the instruction cache on every first tile of a piece.
+          const float4 r4 = *reinterpret_cast<const float4*>(rb + lane * 4);
+          const float mx = fmaxf(fmaxf(r4.x, r4.y), fmaxf(r4.z, r4.w));
+          float m_old = m[0];
+#pragma unroll
+          for (int h = 1; h < kNH; ++h) m_old = lane == h ? m[h] : m_old;
+          float m_new = m_old;
+          if (mx > m_new + kLazyT || m_new == -INFINITY) m_new = mx;
+          const float alpha_l = (m_new == m_old) ? 1.f : fast_exp2(m_old - m_new);
+          const bool rescale = __any_sync(kAllT, alpha_l != 1.f);
+          float alpha[kNH];
+#pragma unroll
+          for (int h = 0; h < kNH; ++h) {
+            m[h] = __shfl_sync(kAllT, m_new, h);
+            alpha[h] = __shfl_sync(kAllT, alpha_l, h);
+          }
+          if (rescale) {   // the same on every thread: m is uniform
+#pragma unroll
+            for (int h = 0; h < kNH; ++h) l[h] *= alpha[h];
+            if (!ti.first) {
+              // O^T holds P V of this piece's earlier tiles: rescale it in
+              // place once the last of those products has completed
+              wait_fast(bar(B_PE + ((t - 1) & 1)), ((t - 1) >> 1) & 1, abort_flag, a.err);
+              __syncwarp();
+              tc_fence_after();
+              float o[kNH];
+              const uint32_t oc = lane_base + COL_O + (ui & 1) * kNPV;
+              tmem_ld32(oc, o);
+              tmem_wait_ld();
+              reg_fence(o);
+#pragma unroll
+              for (int h = 0; h < kNH; ++h) o[h] *= alpha[h];
+              tmem_st32(oc, o);
+              tmem_wait_st();
+            }
+          }
+        }
+        // p = 2^(x - m) as bf16 (what P V multiplies; the sums use the same values)
+        uint32_t pk[kNH / 2];
+#pragma unroll
+        for (int h = 0; h < kNH; h += 2) {
+          const uint32_t pp = pack_bf16(fast_exp2(x[h] - m[h]), fast_exp2(x[h + 1] - m[h + 1]));
+          l[h] += bf16lo(pp);
+          l[h + 1] += bf16hi(pp);
+          pk[h / 2] = pp;
+        }
+        // P^T of tile t - 2 has been read by its P V
+        if (t >= 2) wait_fast(bar(B_PE + (t & 1)), ((t >> 1) - 1) & 1, abort_flag, a.err);
+        unsigned char* prow = prow0 + (t & 1) * kPBytes;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          *reinterpret_cast<uint4*>(prow + ((c ^ (j & 7)) << 4)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        if (!kval) {
+          // zero this key's latent row (both halves): stale pool bytes must
+          // not meet p = 0 in P V (0 x NaN)
+          unsigned char* cr = smem + OFF_RING + (t % kNS) * kTileBytes + crow;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            *reinterpret_cast<uint4*>(cr + c * 16) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(cr + 1024 + c * 16) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_PF + (t & 1)));
+      }
+      // ---- end of the piece: sums over all keys, then O^T / l or partials
+      {
+        float tmp[kNH];
+#pragma unroll
+        for (int h = 0; h < kNH; ++h) tmp[h] = l[h];
+        const float ws = warp_transpose_reduce<false>(tmp, lane);   // head `lane`, this warp
+        float* sb = sum + (ui & 1) * kNH * 4;
+        sb[lane * 4 + wl] = ws;
+        named_bar_sync(1, kSoft);
+        // lane h: the sum over all 128 keys of head h, and its reciprocal
+        // (one division per lane; per-lane code keeps this once-per-piece
+        // path short enough to stay in the instruction cache)
+        const float4 s4 = *reinterpret_cast<const float4*>(sb + lane * 4);
+        const float L_l = (s4.x + s4.y) + (s4.z + s4.w);
+        const float inv_l = 1.f / L_l;
+        wait_fast(bar(B_OF + (ui & 1)), (ui >> 1) & 1, abort_flag, a.err);
+        __syncwarp();
+        tc_fence_after();
+        float o[kNH];
+        tmem_ld32(lane_base + COL_O + (ui & 1) * kNPV, o);
+        tmem_wait_ld();
+        reg_fence(o);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_OE + (ui & 1)));
+        if (u.ns == 1) {
+          // the whole sequence: z = O / l
+          __nv_bfloat16* orow = outp + (int64_t)u.b * a.num_q_heads * kR + j;
+#pragma unroll
+          for (int h = 0; h < kNH; ++h)
+            orow[h * kR] = __float2bfloat16_rn(o[h] * __shfl_sync(kAllT, inv_l, h));
+        } else {
+          // a piece: partial (m, l, O) in slot u.s of each head's row
+          const int64_t prow = (int64_t)u.b * a.num_q_heads * a.max_splits + u.s;
+          float* acc = a.ws_acc + prow * kR + j;
+#pragma unroll
+          for (int h = 0; h < kNH; ++h) acc[(int64_t)h * a.max_splits * kR] = o[h];
+          if (wl == 0) {
+            float m_l = m[0];
+#pragma unroll
+            for (int h = 1; h < kNH; ++h) m_l = lane == h ? m[h] : m_l;
+            float* ml = a.ws_ml + (prow + (int64_t)lane * a.max_splits) * 2;
+            ml[0] = m_l;
+            ml[1] = L_l;
+          }
+        }
+      }
+      ++ui;
     }
-    return;
+    tc_fence_before();
   }
-
-  // -------------------------------------------------------------- consumers
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsConsL));
-  const int g = lane >> 2, t = lane & 3;
-  const int bw = warp & (kBPSL - 1);              // block of the stage this warp takes
-  const int hbase = (warp / kBPSL) * kHalfHeads;   // its 16 query heads
-  const float sl2 = a.scale * 1.4426950408889634f;
-  __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(a.out);
-  // latent pieces of this lane, as in the bf16 decode kernel: load step i
-  // takes chunk kc(i) of the 64-column half (t >> 1) for the score products;
-  // rows 2t, 2t+1, 2t+8, 2t+9 at dims 16g + 8 * (j ^ (g & 1)) for P.V
-  const int khalf = t >> 1;
-  const int kc0 = 4 * (t & 1), kx = (t >> 1) << 1;
-  const int vhalf = g >> 2;
-  uint32_t consumed = 0;
-
-  Walk wk = walk_begin(a, cu, balanced);
-  Unit u;
-  while (walk_next(a, cu, kStageTokL, wk, u)) {
-    // the merge reads how many partials this sequence left
-    if (a.balanced && u.s == 0 && tid == 0) a.ws_np[u.b] = u.ns;
-    // q~ of heads hbase + 8nt + g as B fragments, in the lane's K order
-    uint4 qf[kNTL][4];
-#pragma unroll
-    for (int nt = 0; nt < kNTL; ++nt) {
-      const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(a.q) +
-                                  ((int64_t)u.b * a.num_q_heads + hbase + 8 * nt + g) * kR;
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        qf[nt][i] = __ldg(reinterpret_cast<const uint4*>(qrow + 64 * khalf + 8 * (kc0 + (i ^ kx))));
-    }
-    float o[kNTL][8][4];
-#pragma unroll
-    for (int nt = 0; nt < kNTL; ++nt)
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) o[nt][mt][0] = o[nt][mt][1] = o[nt][mt][2] = o[nt][mt][3] = 0.f;
-    float m_run[kNTL][2], l_run[kNTL][2];
-#pragma unroll
-    for (int nt = 0; nt < kNTL; ++nt) {
-      m_run[nt][0] = m_run[nt][1] = -INFINITY;
-      l_run[nt][0] = l_run[nt][1] = 0.f;
-    }
-
-    const int nblk = (u.tok_end - 1) / kBlockSize - u.tok_begin / kBlockSize + 1;
-    const int nst = (nblk + kBPSL - 1) / kBPSL;
-    for (int st = 0; st < nst; ++st, ++consumed) {
-      const int buf = consumed % kNSTL;
-      const uint32_t phase = (consumed / kNSTL) & 1;
-      if (!*vabort) {
-        if (!mbar_wait(full0 + 8 * buf, phase, a.err)) *vabort = 1;
-      }
-      const int tok0 = u.tok_begin + (st * kBPSL + bw) * kBlockSize;
-      const int valid = min(kBlockSize, u.tok_end - tok0);
-      if (valid <= 0) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty0 + 8 * buf);
-        continue;
-      }
-      const uint32_t ct = sbase + buf * kStageL + bw * kTileL;
-      // ---- the latent as the K operand: keys g and g + 8
-      uint4 kg[4], kh[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int c = kc0 + (i ^ kx);
-        kg[i] = lds128l(ct + khalf * kHalfL + g * 128 + ((c ^ g) << 4));
-        kh[i] = lds128l(ct + khalf * kHalfL + (g + 8) * 128 + ((c ^ g) << 4));
-      }
-      float s[kNTL][4], s2[kNTL][4];
-#pragma unroll
-      for (int nt = 0; nt < kNTL; ++nt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) s[nt][i] = s2[nt][i] = 0.f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int nt = 0; nt < kNTL; ++nt) {
-          mma16816l(s[nt], kg[i].x, kh[i].x, kg[i].y, kh[i].y, qf[nt][i].x, qf[nt][i].y);
-          mma16816l(s2[nt], kg[i].z, kh[i].z, kg[i].w, kh[i].w, qf[nt][i].z, qf[nt][i].w);
-        }
-      // ---- the same latent rows as the V operand
-      uint4 va[2], vb[2], vc[2], vd[2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int c = 2 * (g & 3) + (j ^ (g & 1));
-        const uint32_t base = ct + vhalf * kHalfL;
-        va[j] = lds128l(base + (2 * t) * 128 + ((c ^ (2 * t)) << 4));
-        vb[j] = lds128l(base + (2 * t + 1) * 128 + ((c ^ (2 * t + 1)) << 4));
-        vc[j] = lds128l(base + (2 * t + 8) * 128 + ((c ^ (2 * t)) << 4));
-        vd[j] = lds128l(base + (2 * t + 9) * 128 + ((c ^ (2 * t + 1)) << 4));
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * buf);
-#pragma unroll
-      for (int nt = 0; nt < kNTL; ++nt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) s[nt][i] += s2[nt][i];
-
-      // ---- online softmax per head; this lane holds keys g, g+8
-      const bool k0ok = g < valid, k1ok = g + 8 < valid;
-      float v[kNTL][4];
-      bool grow = false;
-#pragma unroll
-      for (int nt = 0; nt < kNTL; ++nt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          v[nt][i] = (i < 2 ? k0ok : k1ok) ? s[nt][i] * sl2 : -INFINITY;
-          grow |= v[nt][i] > m_run[nt][i & 1] + kLazyL;
-        }
-      if (__any_sync(kAllL, grow)) {
-        bool rescale = false;
-        float alpha[kNTL][2];
-#pragma unroll
-        for (int nt = 0; nt < kNTL; ++nt)
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            float mx = fmaxf(v[nt][j], v[nt][j + 2]);
-            mx = fmaxf(mx, __shfl_xor_sync(kAllL, mx, 4));
-            mx = fmaxf(mx, __shfl_xor_sync(kAllL, mx, 8));
-            mx = fmaxf(mx, __shfl_xor_sync(kAllL, mx, 16));
-            float m_new = m_run[nt][j];
-            if (mx > m_new + kLazyL || m_new == -INFINITY) m_new = mx;
-            alpha[nt][j] = (m_new == m_run[nt][j]) ? 1.f : ex2l(m_run[nt][j] - m_new);
-            rescale |= alpha[nt][j] != 1.f;
-            m_run[nt][j] = m_new;
-          }
-        if (__any_sync(kAllL, rescale)) {
-#pragma unroll
-          for (int nt = 0; nt < kNTL; ++nt) {
-            l_run[nt][0] *= alpha[nt][0];
-            l_run[nt][1] *= alpha[nt][1];
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-              o[nt][mt][0] *= alpha[nt][0];
-              o[nt][mt][1] *= alpha[nt][1];
-              o[nt][mt][2] *= alpha[nt][0];
-              o[nt][mt][3] *= alpha[nt][1];
-            }
-          }
-        }
-      }
-      uint32_t pb0[kNTL], pb1[kNTL];
-#pragma unroll
-      for (int nt = 0; nt < kNTL; ++nt) {
-        const uint32_t x0 = pack2_bf16l(ex2l(v[nt][0] - m_run[nt][0]), ex2l(v[nt][1] - m_run[nt][1]));
-        const uint32_t x1 = pack2_bf16l(ex2l(v[nt][2] - m_run[nt][0]), ex2l(v[nt][3] - m_run[nt][1]));
-        l_run[nt][0] += bf16lo(x0) + bf16lo(x1);
-        l_run[nt][1] += bf16hi(x0) + bf16hi(x1);
-        pb0[nt] = movm_tl(x0);
-        pb1[nt] = movm_tl(x1);
-      }
-      if (valid < kBlockSize) {
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          if (2 * t >= valid) va[j] = make_uint4(0, 0, 0, 0);
-          if (2 * t + 1 >= valid) vb[j] = make_uint4(0, 0, 0, 0);
-          if (2 * t + 8 >= valid) vc[j] = make_uint4(0, 0, 0, 0);
-          if (2 * t + 9 >= valid) vd[j] = make_uint4(0, 0, 0, 0);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const uint32_t aw[4] = {va[j].x, va[j].y, va[j].z, va[j].w};
-        const uint32_t bw4[4] = {vb[j].x, vb[j].y, vb[j].z, vb[j].w};
-        const uint32_t cw[4] = {vc[j].x, vc[j].y, vc[j].z, vc[j].w};
-        const uint32_t dw[4] = {vd[j].x, vd[j].y, vd[j].z, vd[j].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const uint32_t a0 = prmtl(aw[e], bw4[e], 0x5410u);
-          const uint32_t a1 = prmtl(aw[e], bw4[e], 0x7632u);
-          const uint32_t a2 = prmtl(cw[e], dw[e], 0x5410u);
-          const uint32_t a3 = prmtl(cw[e], dw[e], 0x7632u);
-#pragma unroll
-          for (int nt = 0; nt < kNTL; ++nt) mma16816l(o[nt][4 * j + e], a0, a1, a2, a3, pb0[nt], pb1[nt]);
-        }
-      }
-    }
-
-    // ---- merge: the four warps of each head half
-#pragma unroll
-    for (int nt = 0; nt < kNTL; ++nt)
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        l_run[nt][j] += __shfl_xor_sync(kAllL, l_run[nt][j], 4);
-        l_run[nt][j] += __shfl_xor_sync(kAllL, l_run[nt][j], 8);
-        l_run[nt][j] += __shfl_xor_sync(kAllL, l_run[nt][j], 16);
-      }
-#pragma unroll
-    for (int nt = 0; nt < kNTL; ++nt)
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int hl = 8 * nt + 2 * t + j;          // head within this warp's half
-        if (g == 0) {
-          comb_ml[(warp * kHalfHeads + hl) * 2 + 0] = m_run[nt][j];
-          comb_ml[(warp * kHalfHeads + hl) * 2 + 1] = l_run[nt][j];
-        }
-        float* crow = comb + (warp * kHalfHeads + hl) * kCombRowL + 16 * g;
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt)
-          *reinterpret_cast<float2*>(crow + 8 * ((mt >> 2) ^ (g & 1)) + 2 * (mt & 3)) =
-              make_float2(o[nt][mt][j], o[nt][mt][j + 2]);
-      }
-    named_bar_sync(1, kConsumersL);
-    const bool direct = (u.ns == 1);
-    for (int h = warp; h < kHeads; h += kCWL) {
-      const int half = h / kHalfHeads, hl = h % kHalfHeads;
-      float M = -INFINITY;
-#pragma unroll
-      for (int k = 0; k < kBPSL; ++k)
-        M = fmaxf(M, comb_ml[((half * kBPSL + k) * kHalfHeads + hl) * 2]);
-      float wk[kBPSL], L = 0.f;
-#pragma unroll
-      for (int k = 0; k < kBPSL; ++k) {
-        const float mk = comb_ml[((half * kBPSL + k) * kHalfHeads + hl) * 2];
-        wk[k] = (mk == -INFINITY) ? 0.f : ex2l(mk - M);
-        L = fmaf(wk[k], comb_ml[((half * kBPSL + k) * kHalfHeads + hl) * 2 + 1], L);
-      }
-      const float rl = 1.f / L;
-      const int64_t row = (int64_t)u.b * a.num_q_heads + h;
-      const int64_t pidx = row * a.max_splits + u.s;
-#pragma unroll
-      for (int i = 0; i < kR / 32; ++i) {
-        const int d = lane + 32 * i;
-        float O = 0.f;
-#pragma unroll
-        for (int k = 0; k < kBPSL; ++k)
-          O = fmaf(wk[k], comb[((half * kBPSL + k) * kHalfHeads + hl) * kCombRowL + d], O);
-        if (direct)
-          outp[row * kR + d] = __float2bfloat16_rn(O * rl);
-        else
-          a.ws_acc[pidx * kR + d] = O;
-      }
-      if (!direct && lane == 0) {
-        a.ws_ml[pidx * 2 + 0] = M;
-        a.ws_ml[pidx * 2 + 1] = L;
-      }
-    }
-    named_bar_sync(1, kConsumersL);
+  __syncthreads();
+  if (warp == W_MMA) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols));
   }
 }
 
 }  // namespace
 
-cudaError_t launch_decode_mla(const DecodeArgs& args, int num_sms, cudaStream_t stream) {
+cudaError_t launch_decode_mla(const DecodeArgs& args, const void* w_v, void* out, int num_sms,
+                              cudaStream_t stream) {
   DecodeArgs a = args;
-  a.balanced = a.ws_np != nullptr && stage_plan_fits(a, kStageTokL);
-  if (a.chunk_prior >= 0 || a.split_tokens % kStageTokL != 0 || a.num_kv_heads != 1 ||
-      a.num_q_heads != kHeads || a.head_dim != kR)
+  a.balanced = a.ws_np != nullptr && stage_plan_fits(a, kStageTokT, kPadT);
+  if (a.chunk_prior >= 0 || a.split_tokens % kTK != 0 || a.num_kv_heads != 1 ||
+      a.num_q_heads != kNH || a.head_dim != kR)
     return cudaErrorInvalidValue;
-  CUtensorMap tm_c;
-  const int64_t rows = a.num_blocks * kBlockSize;
-  if (!encode_pool_map_bf16(&tm_c, a.k_cache, rows)) return cudaErrorInvalidValue;
-  const size_t smem = OFF_CU_L + sizeof(int) * (size_t)(a.num_seqs + 1) + 1024;
+  CUtensorMap tm_c, tm_q;
+  if (!encode_latent_block_map(&tm_c, a.k_cache, a.num_blocks)) return cudaErrorInvalidValue;
+  if (!encode_rows32_map_bf16(&tm_q, a.q, (int64_t)a.num_seqs * kNH)) return cudaErrorInvalidValue;
+  const size_t smem = OFF_CU + sizeof(int) * (size_t)(a.num_seqs + 1);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
   cudaError_t e = allow_dynamic_smem(decode_mla_kernel, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t upper = (int64_t)a.num_seqs * a.max_splits;
-  const int grid = (int)(upper < (int64_t)num_sms ? upper : (int64_t)num_sms);
-  decode_mla_kernel<<<grid, kThreadsL, smem, stream>>>(a, tm_c);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(upper < (int64_t)num_sms ? upper : (int64_t)num_sms));
+  cfg.blockDim = dim3(kThreadsT);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, decode_mla_kernel, a, tm_c, tm_q);
+  if (e != cudaSuccess) return e;
   e = cudaGetLastError();
-  if (e != cudaSuccess || a.max_splits <= 1) return e;
-  return launch_decode_reduce_bf16_128(a, stream);
+  if (e != cudaSuccess) return e;
+  return launch_merge_project(a, w_v, out, stream);
 }
 
 }  // namespace pkv

@@ -44,6 +44,9 @@ __global__ void __launch_bounds__(128) gemm_heads_kernel(__nv_bfloat16* __restri
                                                          const __nv_bfloat16* __restrict__ x,
                                                          const __nv_bfloat16* __restrict__ wts,
                                                          int rows, int heads) {
+  // a kernel launched next as a programmatic dependent (the latent
+  // attention) may start now; it waits for this grid before reading y
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int kQ = 32;                 // output columns per CTA
   // [K][N]: 128 k-rows x 32 columns (row 40 elements); [N][K]: 32 n-rows x 128 k
   __shared__ __align__(16) __nv_bfloat16 ws[W_IS_NK ? kQ * kGRow : kGD * (kQ + 8)];
@@ -113,7 +116,127 @@ __global__ void __launch_bounds__(128) gemm_heads_kernel(__nv_bfloat16* __restri
   }
 }
 
+// Merge of the latent attention's split partials fused with the output
+// up-projection: for 16 sequences and one head h per CTA,
+//   z[b][h] = sum_s 2^(m_s - M) acc_s / sum_s 2^(m_s - M) l_s   (M = max_s m_s)
+// (or the z row the attention wrote itself, for a sequence it covered in one
+// piece), rounded to bf16, then o[b][h] = W_V[h] z[b][h] on m16n8k16 tiles
+// with W_V[h] ([D][r] = [N][K]) staged in padded shared memory; warp w
+// computes output columns 32w .. 32w + 31.  W_V[h] is loaded before the
+// grid waits for the attention kernel it depends on (programmatic dependent
+// launch), so that load overlaps the attention's tail.
+constexpr int kMRows = 16;
+
+__global__ void __launch_bounds__(128) merge_project_kernel(const DecodeArgs a,
+                                                            const __nv_bfloat16* __restrict__ wts,
+                                                            __nv_bfloat16* __restrict__ y) {
+  __shared__ __align__(16) __nv_bfloat16 ws[kGD * kGRow];
+  __shared__ __align__(16) __nv_bfloat16 zs[kMRows * kGRow];
+  const int h = blockIdx.y, b0 = blockIdx.x * kMRows;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const __nv_bfloat16* wh = wts + (int64_t)h * kGD * kGD;
+  for (int i = tid; i < kGD * 16; i += 128) {
+    const int r = i >> 4, c = i & 15;
+    *reinterpret_cast<uint4*>(ws + r * kGRow + c * 8) =
+        __ldg(reinterpret_cast<const uint4*>(wh + (int64_t)r * kGD) + c);
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // ---- z rows: warp w merges rows 4w .. 4w + 3; lane = 4 of the 128 columns
+  const int limit = min(a.max_seq_len, a.max_blocks_per_seq * kBlockSize);
+  const __nv_bfloat16* z = static_cast<const __nv_bfloat16*>(a.out);
+  for (int rr = 0; rr < kMRows / 4; ++rr) {
+    const int r = warp * (kMRows / 4) + rr, b = b0 + r;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int n = b < a.num_seqs ? a.seq_lens[b] : 0;
+    if (n >= 1 && n <= limit) {
+      const int ns = a.balanced ? a.ws_np[b] : (n + a.split_tokens - 1) / a.split_tokens;
+      const int64_t row = (int64_t)b * a.num_q_heads + h;
+      if (ns <= 1) {
+        const uint2 v = *reinterpret_cast<const uint2*>(z + row * kGD + 4 * lane);
+        o = make_float4(bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y));
+      } else {
+        const int64_t base = row * a.max_splits;
+        float M = -INFINITY;
+        for (int s = lane; s < ns; s += 32) M = fmaxf(M, a.ws_ml[(base + s) * 2]);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        float L = 0.f;
+        for (int s = 0; s < ns; ++s) {
+          const float ms = a.ws_ml[(base + s) * 2];
+          const float w = ms == -INFINITY ? 0.f : exp2f(ms - M);
+          const float4 v = reinterpret_cast<const float4*>(a.ws_acc + (base + s) * kGD)[lane];
+          L = fmaf(w, a.ws_ml[(base + s) * 2 + 1], L);
+          o.x = fmaf(w, v.x, o.x);
+          o.y = fmaf(w, v.y, o.y);
+          o.z = fmaf(w, v.z, o.z);
+          o.w = fmaf(w, v.w, o.w);
+        }
+        const float inv = 1.f / L;
+        o = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+      }
+    }
+    __nv_bfloat162* zr = reinterpret_cast<__nv_bfloat162*>(zs + r * kGRow + 4 * lane);
+    zr[0] = __floats2bfloat162_rn(o.x, o.y);
+    zr[1] = __floats2bfloat162_rn(o.z, o.w);
+  }
+  __syncthreads();
+  // ---- o = z W_V[h]^T for the 16 rows: this warp's 32 columns
+  const int g = lane >> 2, t = lane & 3;
+  const uint32_t wbase = smem_u32(ws), zbase = smem_u32(zs);
+  const int mi = lane >> 3, rr8 = lane & 7;
+  const int n0 = warp * 32;
+  float acc[4][4];
+#pragma unroll
+  for (int n = 0; n < 4; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    uint32_t af[4];
+    ldsm4(zbase + (uint32_t)((rr8 + ((mi & 1) << 3)) * kGRow + ks * 16 + ((mi >> 1) << 3)) * 2, af);
+#pragma unroll
+    for (int np = 0; np < 2; ++np) {
+      uint32_t b[4];
+      const int n = n0 + np * 16 + ((mi >> 1) << 3) + rr8;
+      const int k = ks * 16 + ((mi & 1) << 3);
+      ldsm4(wbase + (uint32_t)(n * kGRow + k) * 2, b);
+      mma16816g(acc[2 * np], af[0], af[1], af[2], af[3], b[0], b[1]);
+      mma16816g(acc[2 * np + 1], af[0], af[1], af[2], af[3], b[2], b[3]);
+    }
+  }
+  const int ra = b0 + g, rb = b0 + g + 8;
+#pragma unroll
+  for (int n = 0; n < 4; ++n) {
+    const int col = n0 + n * 8 + 2 * t;
+    if (ra < a.num_seqs)
+      *reinterpret_cast<__nv_bfloat162*>(y + ((int64_t)ra * a.num_q_heads + h) * kGD + col) =
+          __floats2bfloat162_rn(acc[n][0], acc[n][1]);
+    if (rb < a.num_seqs)
+      *reinterpret_cast<__nv_bfloat162*>(y + ((int64_t)rb * a.num_q_heads + h) * kGD + col) =
+          __floats2bfloat162_rn(acc[n][2], acc[n][3]);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_merge_project(const DecodeArgs& a, const void* w_v, void* out,
+                                 cudaStream_t stream) {
+  if (a.num_seqs <= 0) return cudaSuccess;
+  if (a.head_dim != kGD || a.num_kv_heads != 1) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.num_seqs + kMRows - 1) / kMRows, a.num_q_heads);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, merge_project_kernel, a,
+                                           static_cast<const __nv_bfloat16*>(w_v),
+                                           static_cast<__nv_bfloat16*>(out));
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gemm_heads(void* y, const void* x, const void* w, int rows, int heads,
                               bool w_is_nk, cudaStream_t stream) {

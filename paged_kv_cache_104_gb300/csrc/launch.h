@@ -101,13 +101,25 @@ cudaError_t launch_paged_decode_mma(const DecodeArgs& a, int num_sms, cudaStream
 // fp8 (E4M3) cache, bf16 q/out, head_dim 128, group in {1,2,4,8,16}; uses
 // DecodeArgs with k_scale / v_scale set.
 cudaError_t launch_paged_decode_fp8(const DecodeArgs& a, int num_sms, cudaStream_t stream);
-// Attention over a latent (MLA-style) cache: one pool of rank-128 latents,
-// 32 query heads, q already absorbed; a.k_cache is the latent pool.
-cudaError_t launch_decode_mla(const DecodeArgs& a, int num_sms, cudaStream_t stream);
+// Attention over a latent (MLA-style) cache and the output projection: one
+// pool of rank-128 latents, 32 query heads, q already absorbed into a.q;
+// a.k_cache is the latent pool, a.out receives z for sequences covered in one
+// piece (the others leave partials); then the merge + up-projection writes
+// o = W_V z into `out`.  The attention is launched as the programmatic
+// dependent of the kernel before it in the stream (the query absorption),
+// and waits for it only before reading a.q.
+cudaError_t launch_decode_mla(const DecodeArgs& a, const void* w_v, void* out, int num_sms,
+                              cudaStream_t stream);
 // y[r][h] = x[r][h] . W[h] (W[h] 128 x 128 bf16, stored [K][N], or [N][K]
-// when w_is_nk), bf16 in and out.
+// when w_is_nk), bf16 in and out.  Each CTA signals at its start that a
+// programmatic dependent launch may begin.
 cudaError_t launch_gemm_heads(void* y, const void* x, const void* w, int rows, int heads,
                               bool w_is_nk, cudaStream_t stream);
+// The latent attention's merge of split partials fused with the output
+// up-projection o_h = W_V[h] z_h (launched as the attention's programmatic
+// dependent).
+cudaError_t launch_merge_project(const DecodeArgs& a, const void* w_v, void* out,
+                                 cudaStream_t stream);
 // Merge of split partials for bf16 / head_dim 128 (used by the mma decode).
 cudaError_t launch_decode_reduce_bf16_128(const DecodeArgs& a, cudaStream_t stream);
 

@@ -100,4 +100,33 @@ bool encode_rows_map_bf16(CUtensorMap* map, const void* base, int64_t n, int hea
   });
 }
 
+bool encode_latent_block_map(CUtensorMap* map, const void* base, int64_t num_blocks) {
+  EncodeTiledFn f = encode_fn();
+  if (!f || num_blocks <= 0 || 2 * num_blocks >= (1ll << 31) - 1) return false;
+  return cached(map, kPoolBlocksBf16, base, num_blocks, 0, [&](CUtensorMap* m) {
+    // element (x, y, z, w) = column x of half z of row y of 8-row group w
+    cuuint64_t dims[4] = {64, 8, 2, (cuuint64_t)(2 * num_blocks)};
+    cuuint64_t strides[3] = {256, 128, 2048};
+    cuuint32_t box[4] = {64, 8, 2, 2};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  });
+}
+
+bool encode_rows32_map_bf16(CUtensorMap* map, const void* base, int64_t rows) {
+  EncodeTiledFn f = encode_fn();
+  if (!f || rows <= 0 || rows >= (1ll << 31) - 1) return false;
+  return cached(map, kRows32Bf16, base, rows, 0, [&](CUtensorMap* m) {
+    cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {128 * 2};
+    cuuint32_t box[2] = {64, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  });
+}
+
 }  // namespace pkv
