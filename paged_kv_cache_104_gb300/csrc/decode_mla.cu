@@ -29,25 +29,25 @@
 // apart.  One box per block halves the TMA issue count of two 2 KiB boxes,
 // and eight lanes of the producer warp issue a tile's boxes side by side.
 //
-// Roles (192 threads, one CTA per SM):
+// Roles (224 threads, one CTA per SM):
 //   warps 0-3  softmax.  Thread j owns key j of each tile (TMEM lane j of
 //              S^T) and rank dimension j of O^T.  The running max per head
 //              (log2 domain) only has to bound the scores to within 2^8: one
 //              barrier reduction (bar.red.or) over the 128 threads decides
 //              whether any score exceeds it, and only then is the exact max
-//              over the tile's keys taken (warp transposes, then shared
+//              over the tile's keys taken (warp reductions, then shared
 //              memory) and O^T rescaled in TMEM.  Each thread keeps the sum of
 //              its own keys' weights per head; they are added up once per
 //              unit.  Rows of keys past a sequence's end are zeroed in the
 //              tile, so stale pool bytes (even NaN) never meet p = 0 in P V.
 //   warp 4     TMA producer: the unit's q~ (32 rows) into a two-buffer ring,
 //              the latent blocks of each tile into a four-tile ring.
-//   warp 5     TMEM allocator and MMA issuer (converged warp, one elected
-//              lane per instruction).  It polls what S^T of the next tile and
-//              P V of the oldest softmaxed tile wait for and issues whichever
-//              is ready, so the scores of the next tile are in flight while
-//              the softmax of this one runs, and P V never waits for latents
-//              still on their way.
+//   warp 5     TMEM allocator and issuer of the score products S^T (converged
+//              warp, one elected lane per instruction), as soon as a tile's
+//              latents are in: the scores of the next tiles are computed
+//              while the softmax of this one runs.
+//   warp 6     issuer of P V, as soon as a tile's softmax is done (its own
+//              warp, so it never waits behind latents still on their way).
 // Work: persistent CTAs take the balanced walk over 128-token stages (equal
 // shares of all sequences' stages, cut where sequences change) when the
 // batch gives every CTA at least 512 tokens, else 512-token splits; a piece
@@ -81,9 +81,9 @@ constexpr int kNS = 4;                          // latent ring depth (tiles)
 constexpr int kQBytes = kNH * kR * 2;           // 8 KiB: q~ of one sequence
 constexpr int kQHalf = kQBytes / 2;             // one 64-column half, 32 rows
 constexpr int kPBytes = kTK * 128;              // P^T: 128 keys x 128 B (64 columns)
-constexpr int kThreadsT = 192;
+constexpr int kThreadsT = 224;
 constexpr int kSoft = 128;                      // softmax threads
-constexpr int W_PROD = 4, W_MMA = 5;
+constexpr int W_PROD = 4, W_MMA = 5, W_PV = 6;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t COL_S = 0;                   // S^T of tile parity b at 32 b
 constexpr uint32_t COL_O = 64;                  // O^T of unit parity b at 64 + 64 b
@@ -96,7 +96,7 @@ constexpr int kMinStagesT = kSplitTokens / kStageTokT;   // shares of at least 4
 // exact maximum), in tiles.  CTAs whose shares start many short sequences
 // then take fewer tiles.  Shares still hold at least kMinStagesT stages, so
 // a sequence of n tokens still falls to at most ceil(n / 512) + 1 CTAs.
-constexpr int kPadT = 2;
+constexpr int kPadT = 6;
 
 constexpr int OFF_RING = 0;
 constexpr int OFF_Q = OFF_RING + kNS * kTileBytes;          // [2] q~
@@ -116,8 +116,8 @@ enum {
   B_PE = B_PF + 2,          // [2]  P V of that tile done (P^T free, O^T settled)
   B_OF = B_PE + 2,          // [2]  O^T of a unit complete
   B_OE = B_OF + 2,          // [2]  O^T read out by the epilogue
-  B_DRAIN = B_OE + 2,       // the MMA warp's last products done
-  B_COUNT = B_DRAIN + 1
+  B_DRAIN = B_OE + 2,       // [2] each issuer's last products done
+  B_COUNT = B_DRAIN + 2
 };
 constexpr int OFF_TSLOT = OFF_BAR + B_COUNT * 8;
 constexpr int OFF_ABORT = OFF_TSLOT + 4;
@@ -160,10 +160,17 @@ __device__ __forceinline__ bool bar_red_or(bool pred, int id, int count) {
   return r != 0;
 }
 
-// Lane l returns OP over the warp's lanes of element l of v (v is consumed):
-// a butterfly that halves the elements each lane carries at every step.
-template <bool kMax>
-__device__ __forceinline__ float warp_transpose_reduce(float (&v)[32], int lane) {
+// Maximum of v over the warp (every lane gets it); -inf inputs are ordinary.
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+// Lane l returns the sum over the warp's lanes of element l of v (v is
+// consumed): a butterfly that halves the elements each lane carries at every
+// step.
+__device__ __forceinline__ float warp_transpose_sum(float (&v)[32], int lane) {
 #pragma unroll
   for (int w = 16; w >= 1; w >>= 1) {
     const bool upper = (lane & w) != 0;
@@ -172,7 +179,7 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[32], int lane)
       const float send = upper ? v[i] : v[i + w];
       const float keep = upper ? v[i + w] : v[i];
       const float got = __shfl_xor_sync(kAllT, send, w);
-      v[i] = kMax ? fmaxf(keep, got) : keep + got;
+      v[i] = keep + got;
     }
   }
   return v[0];
@@ -219,6 +226,7 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c,
       mbar_init(bar(B_OE + i), 4);
     }
     mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(B_DRAIN + 1), 1);
     *abort_i = 0;
     fence_mbar_init();
   }
@@ -267,55 +275,82 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c,
     const uint64_t policy = policy_evict_first();
     uint32_t t = 0, ui = 0;
     bool ok = true;
+    // 32 block ids of piece v from its block `first` on, one per lane
+    auto load_ids = [&](const Unit& v, int first) {
+      const int blk0 = v.tok_begin / kBlockSize;
+      const int nblk = (v.tok_end - 1) / kBlockSize - blk0 + 1;
+      int id = 0;
+      if (first + lane < nblk) {
+        id = __ldg(a.block_table + (int64_t)v.b * a.bt_stride + blk0 + first + lane);
+        if (id < 0 || (int64_t)id >= a.num_blocks) {
+          record_error(a.err, DEVERR_BLOCK_RANGE);
+          id = 0;  // read a valid block instead; the error word reports it
+        }
+      }
+      return id;
+    };
+    // The walk is looked at one piece ahead: the next piece's first block ids
+    // are requested when this piece starts, so a switch between pieces does
+    // not wait for a block-table read.
     Walk wk = walk_begin(a, cu, balanced);
-    Unit u;
-    // q~ comes from the kernel before this one in the stream (launched as its
-    // programmatic dependent, this grid may start before it has finished)
-    if (lane == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
-    while (ok && walk_next(a, cu, kStageTokT, wk, u, kPadT)) {
-      // this piece's q~ (32 rows of the absorbed queries)
+    Unit u, nu;
+    bool have = walk_next(a, cu, kStageTokT, wk, u, kPadT);
+    int ids = have ? load_ids(u, 0) : 0;
+    // this piece's q~ (32 rows of the absorbed queries)
+    auto load_q = [&](const Unit& v) {
       if (lane == 0) {
         if (ui >= 2) ok = wait_or_abort(bar(B_QE + (ui & 1)), ((ui >> 1) - 1) & 1, abort_flag, a.err);
         if (ok) {
           const uint32_t qb = sbase + OFF_Q + (ui & 1) * kQBytes;
           mbar_arrive_expect_tx(bar(B_QF + (ui & 1)), kQBytes);
-          tma2d(qb, &tm_q, bar(B_QF + (ui & 1)), 0, u.b * kNH);
-          tma2d(qb + kQHalf, &tm_q, bar(B_QF + (ui & 1)), 64, u.b * kNH);
+          tma2d(qb, &tm_q, bar(B_QF + (ui & 1)), 0, v.b * kNH);
+          tma2d(qb + kQHalf, &tm_q, bar(B_QF + (ui & 1)), 64, v.b * kNH);
         }
       }
       ok = __shfl_sync(kAllT, (int)ok, 0) != 0;
-      if (!ok) break;
-      ++ui;
-      const int blk0 = u.tok_begin / kBlockSize;
-      const int nblk = (u.tok_end - 1) / kBlockSize - blk0 + 1;
-      const int32_t* bt_row = a.block_table + (int64_t)u.b * a.bt_stride + blk0;
+      if (ok) ++ui;
+    };
+    // q~ comes from the kernel before this one in the stream: launched as its
+    // programmatic dependent, this grid may start before that one has
+    // finished.  The latents do not depend on it, so the first piece's first
+    // tiles are requested before waiting for it; its q~ right after.
+    bool first_piece = true;
+    while (ok && have) {
+      const bool have_next = walk_next(a, cu, kStageTokT, wk, nu, kPadT);
+      const int next_ids = have_next ? load_ids(nu, 0) : 0;
+      const int nblk = (u.tok_end - 1) / kBlockSize - u.tok_begin / kBlockSize + 1;
       const int ntile = tiles_of(u);
-      int my_blk = 0;
+      const int q_after = first_piece ? min(ntile, kNS) : 0;   // tiles issued before its q~
+      if (q_after == 0) load_q(u);
+      if (!ok) break;
       for (int i = 0; i < ntile; ++i, ++t) {
-        if ((i * kBlkPerTile) % 32 == 0) {  // next window of 32 block ids, one per lane
-          const int idx = i * kBlkPerTile + lane;
-          my_blk = 0;
-          if (idx < nblk) {
-            my_blk = __ldg(bt_row + idx);
-            if (my_blk < 0 || (int64_t)my_blk >= a.num_blocks) {
-              record_error(a.err, DEVERR_BLOCK_RANGE);
-              my_blk = 0;  // read a valid block instead; the error word reports it
-            }
-          }
+        if (i == q_after && q_after > 0) {
+          if (lane == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+          load_q(u);
+          if (!ok) break;
         }
+        if (i > 0 && (i * kBlkPerTile) % 32 == 0) ids = load_ids(u, i * kBlkPerTile);
         const int slot = t % kNS;
         if (lane == 0 && t >= (uint32_t)kNS)
           ok = wait_or_abort(bar(B_CE + slot), ((t / kNS) - 1) & 1, abort_flag, a.err);
         ok = __shfl_sync(kAllT, (int)ok, 0) != 0;
         if (!ok) break;
         const int nb = min(kBlkPerTile, nblk - i * kBlkPerTile);
-        const int blk = __shfl_sync(kAllT, my_blk, (i * kBlkPerTile + (lane & 7)) & 31);
+        const int blk = __shfl_sync(kAllT, ids, (i * kBlkPerTile + (lane & 7)) & 31);
         const uint32_t fb = bar(B_CF + slot);
         if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)(nb * kBlockBytes));
         __syncwarp();
         if (lane < nb)
           tma4d(sbase + OFF_RING + slot * kTileBytes + lane * kBlockBytes, &tm_c, fb, 2 * blk, policy);
       }
+      if (ok && q_after == ntile) {   // a first piece of at most kNS tiles
+        if (lane == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+        load_q(u);
+      }
+      first_piece = false;
+      u = nu;
+      have = have_next;
+      ids = next_ids;
     }
     if (!ok && lane == 0) {  // after an abort, let the copies already issued land
       const uint32_t first = t > (uint32_t)kNS ? t - kNS : 0;
@@ -323,99 +358,72 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c,
       const uint32_t qfirst = ui > 2u ? ui - 2 : 0;
       for (uint32_t i = qfirst; i < ui; ++i) mbar_wait(bar(B_QF + (i & 1)), (i >> 1) & 1, nullptr);
     }
-  } else if (warp == W_MMA) {
-    // ------------------------------------------------------------- MMA issuer
+  } else if (warp == W_MMA || warp == W_PV) {
+    // ------------------------------------------------------------- MMA issuers
+    // Warp W_MMA issues S^T of every tile as soon as its latents, its q~ and
+    // the S^T buffer are there; warp W_PV issues P V of every tile as soon as
+    // its softmax is done.  Two issuers, each blocking on its own barriers,
+    // keep P V from waiting behind the next tile's latents (one warp polling
+    // both sets of barriers measured slower: each non-blocking probe of an
+    // mbarrier costs on the order of a hundred cycles).
     constexpr uint32_t idesc_s = make_idesc(false, kTK, kNH);
     constexpr uint32_t idesc_o = idesc_mn_mn(kR, kNPV);
-    // Two cursors over the same walk: the next tile whose S^T is to be
-    // issued and the next tile whose P V is.  The warp polls the barriers
-    // both wait on and issues whichever product is ready first (S^T when
-    // both are), so P V of a tile never waits for the next tile's latents
-    // and a tile's ring slot is released as soon as its softmax is done.
-    Walk wks = walk_begin(a, cu, balanced), wkp = walk_begin(a, cu, balanced);
-    Unit us, up;
-    bool has_s = walk_next(a, cu, kStageTokT, wks, us, kPadT);
-    bool has_p = walk_next(a, cu, kStageTokT, wkp, up, kPadT);
-    int is_i = 0, is_n = has_s ? tiles_of(us) : 0;
-    int ip_i = 0, ip_n = has_p ? tiles_of(up) : 0;
-    uint32_t ts = 0, uis = 0, tp = 0, uip = 0;
-    bool idle = false;
-    long long t_idle = 0;
-    while (true) {
-      const bool s_cand = has_s, p_cand = has_p && tp < ts;
-      if (!s_cand && !p_cand) break;
-      // lane 0 probes the barriers; the warp follows its decision
-      int act = 0;   // 1: S^T, 2: P V, 3: give up
-      if (lane == 0) {
-        if (s_cand && mbar_test(bar(B_QF + (uis & 1)), (uis >> 1) & 1) &&
-            mbar_test(bar(B_CF + (ts % kNS)), (ts / kNS) & 1) &&
-            (ts < 2 || mbar_test(bar(B_SE + (ts & 1)), ((ts >> 1) - 1) & 1)))
-          act = 1;
-        else if (p_cand && mbar_test(bar(B_PF + (tp & 1)), (tp >> 1) & 1) &&
-                 (ip_i != 0 || uip < 2 || mbar_test(bar(B_OE + (uip & 1)), ((uip >> 1) - 1) & 1)))
-          act = 2;
-        else if (*abort_flag)
-          act = 3;
-        else if (!idle)
-          t_idle = clock64();
-        else if (clock64() - t_idle > kWaitLimitCycles) {
-          record_error(a.err, DEVERR_TIMEOUT);
-          *abort_flag = 1;
-          act = 3;
+    const bool is_s = warp == W_MMA;
+    bool ok = true;
+    uint32_t t = 0, ui = 0;
+    Walk wk = walk_begin(a, cu, balanced);
+    Unit u;
+    while (ok && walk_next(a, cu, kStageTokT, wk, u, kPadT)) {
+      const int ntile = tiles_of(u);
+      if (is_s) {
+        ok = __all_sync(kAllT, wait_or_abort(bar(B_QF + (ui & 1)), (ui >> 1) & 1, abort_flag, a.err));
+        if (!ok) break;
+      }
+      const uint32_t qb = sbase + OFF_Q + (ui & 1) * kQBytes;
+      for (int i = 0; i < ntile && ok; ++i, ++t) {
+        const uint32_t ct = sbase + OFF_RING + (t % kNS) * kTileBytes;
+        if (is_s) {
+          ok = __all_sync(kAllT, wait_fast(bar(B_CF + (t % kNS)), (t / kNS) & 1, abort_flag, a.err));
+          if (ok && t >= 2)
+            ok = __all_sync(kAllT, wait_fast(bar(B_SE + (t & 1)), ((t >> 1) - 1) & 1, abort_flag, a.err));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < kR / 16; ++k) {
+            // A = C (K-major): rank half k/4, 32 bytes per 16 columns; 8-key atoms 2 KiB apart
+            const uint64_t ad = make_sw128_desc(ct + (k >> 2) * 1024 + (k & 3) * 32, 16, 2048);
+            // B = Q~ (K-major): 8-head atoms 1 KiB apart, halves 4 KiB apart
+            const uint64_t bd = make_sw128_desc(qb + (k >> 2) * kQHalf + (k & 3) * 32, 16, 1024);
+            mma_ss_e(tmem + COL_S + (t & 1) * kNH, ad, bd, idesc_s, k > 0 ? 1u : 0u);
+          }
+          commit_e(bar(B_SF + (t & 1)));
+          if (i == ntile - 1) commit_e(bar(B_QE + (ui & 1)));   // q~ buffer read
+        } else {
+          ok = __all_sync(kAllT, wait_fast(bar(B_PF + (t & 1)), (t >> 1) & 1, abort_flag, a.err));
+          if (ok && i == 0 && ui >= 2)   // O^T of two pieces back has been read out
+            ok = __all_sync(kAllT, wait_fast(bar(B_OE + (ui & 1)), ((ui >> 1) - 1) & 1, abort_flag, a.err));
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t pt = sbase + OFF_P + (t & 1) * kPBytes;
+#pragma unroll
+          for (int kk = 0; kk < kTK / 16; ++kk) {
+            // A = C^T (MN-major): rank halves 1 KiB apart, 8-key atoms 2 KiB apart
+            const uint64_t ad = make_sw128_desc(ct + kk * 2 * 2048, 1024, 2048);
+            // B = P^T (MN-major): 8-key atoms of 128-byte rows, 1 KiB apart
+            const uint64_t bd = make_sw128_desc(pt + kk * 16 * 128, 16, 1024);
+            mma_ss_e(tmem + COL_O + (ui & 1) * kNPV, ad, bd, idesc_o, (i == 0 && kk == 0) ? 0u : 1u);
+          }
+          commit_e(bar(B_CE + (t % kNS)));
+          commit_e(bar(B_PE + (t & 1)));
+          if (i == ntile - 1) commit_e(bar(B_OF + (ui & 1)));
         }
       }
-      act = __shfl_sync(kAllT, act, 0);
-      if (act == 3) break;   // aborted: nothing more is issued
-      idle = act == 0;
-      if (act == 1) {
-        tc_fence_after();
-        const uint32_t ct = sbase + OFF_RING + (ts % kNS) * kTileBytes;
-        const uint32_t qb = sbase + OFF_Q + (uis & 1) * kQBytes;
-#pragma unroll
-        for (int k = 0; k < kR / 16; ++k) {
-          // A = C (K-major): rank half k/4, 32 bytes per 16 columns; 8-key atoms 2 KiB apart
-          const uint64_t ad = make_sw128_desc(ct + (k >> 2) * 1024 + (k & 3) * 32, 16, 2048);
-          // B = Q~ (K-major): 8-head atoms 1 KiB apart, halves 4 KiB apart
-          const uint64_t bd = make_sw128_desc(qb + (k >> 2) * kQHalf + (k & 3) * 32, 16, 1024);
-          mma_ss_e(tmem + COL_S + (ts & 1) * kNH, ad, bd, idesc_s, k > 0 ? 1u : 0u);
-        }
-        commit_e(bar(B_SF + (ts & 1)));
-        if (is_i == is_n - 1) commit_e(bar(B_QE + (uis & 1)));   // q~ buffer read
-        ++ts;
-        if (++is_i == is_n) {
-          ++uis;
-          has_s = walk_next(a, cu, kStageTokT, wks, us, kPadT);
-          is_i = 0;
-          is_n = has_s ? tiles_of(us) : 0;
-        }
-      } else if (act == 2) {
-        tc_fence_after();
-        const bool first = ip_i == 0, last = ip_i == ip_n - 1;
-        const uint32_t ct = sbase + OFF_RING + (tp % kNS) * kTileBytes;
-        const uint32_t pt = sbase + OFF_P + (tp & 1) * kPBytes;
-#pragma unroll
-        for (int kk = 0; kk < kTK / 16; ++kk) {
-          // A = C^T (MN-major): rank halves 1 KiB apart, 8-key atoms 2 KiB apart
-          const uint64_t ad = make_sw128_desc(ct + kk * 2 * 2048, 1024, 2048);
-          // B = P^T (MN-major): 8-key atoms of 128-byte rows, 1 KiB apart
-          const uint64_t bd = make_sw128_desc(pt + kk * 16 * 128, 16, 1024);
-          mma_ss_e(tmem + COL_O + (uip & 1) * kNPV, ad, bd, idesc_o, (first && kk == 0) ? 0u : 1u);
-        }
-        commit_e(bar(B_CE + (tp % kNS)));
-        commit_e(bar(B_PE + (tp & 1)));
-        if (last) commit_e(bar(B_OF + (uip & 1)));
-        ++tp;
-        if (++ip_i == ip_n) {
-          ++uip;
-          has_p = walk_next(a, cu, kStageTokT, wkp, up, kPadT);
-          ip_i = 0;
-          ip_n = has_p ? tiles_of(up) : 0;
-        }
-      }
+      ++ui;
     }
     // every product this warp issued completes before TMEM is freed
-    commit_e(bar(B_DRAIN));
-    mbar_wait(bar(B_DRAIN), 0, nullptr);
+    const int drain = is_s ? B_DRAIN : B_DRAIN + 1;
+    commit_e(bar(drain));
+    mbar_wait(bar(drain), 0, nullptr);
     __syncwarp();
   } else {
     // ------------------------------------------------------------- softmax
@@ -464,10 +472,14 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c,
         }
         if (bar_red_or(grow, 1, kSoft)) {
           // exact max per head over the tile's keys
-          float tmp[kNH];
+          // per head, the maximum over this warp's 32 keys (one warp
+          // reduction each); lane h keeps head h's
+          float wm = -INFINITY;
 #pragma unroll
-          for (int h = 0; h < kNH; ++h) tmp[h] = x[h];
-          const float wm = warp_transpose_reduce<true>(tmp, lane);   // head `lane`, this warp
+          for (int h = 0; h < kNH; ++h) {
+            const float r = warp_max(x[h]);
+            wm = lane == h ? r : wm;
+          }
           float* rb = red + (t & 1) * kNH * 4;
           rb[lane * 4 + wl] = wm;
           named_bar_sync(1, kSoft);
@@ -547,7 +559,7 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c,
         float tmp[kNH];
 #pragma unroll
         for (int h = 0; h < kNH; ++h) tmp[h] = l[h];
-        const float ws = warp_transpose_reduce<false>(tmp, lane);   // head `lane`, this warp
+        const float ws = warp_transpose_sum(tmp, lane);   // head `lane`, this warp
         float* sb = sum + (ui & 1) * kNH * 4;
         sb[lane * 4 + wl] = ws;
         named_bar_sync(1, kSoft);

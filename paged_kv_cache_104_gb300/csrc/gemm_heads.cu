@@ -121,90 +121,145 @@ __global__ void __launch_bounds__(128) gemm_heads_kernel(__nv_bfloat16* __restri
 //   z[b][h] = sum_s 2^(m_s - M) acc_s / sum_s 2^(m_s - M) l_s   (M = max_s m_s)
 // (or the z row the attention wrote itself, for a sequence it covered in one
 // piece), rounded to bf16, then o[b][h] = W_V[h] z[b][h] on m16n8k16 tiles
-// with W_V[h] ([D][r] = [N][K]) staged in padded shared memory; warp w
-// computes output columns 32w .. 32w + 31.  W_V[h] is loaded before the
-// grid waits for the attention kernel it depends on (programmatic dependent
-// launch), so that load overlaps the attention's tail.
+// with W_V[h] ([D][r] = [N][K]) staged in padded shared memory.  Eight warps:
+// warp w merges rows 2w and 2w + 1 (lane = 4 of the 128 columns; the split
+// weights are formed one split per lane), then computes output columns
+// 16w .. 16w + 15.  W_V[h] is loaded before the grid waits for
+// the attention kernel it depends on (programmatic dependent launch), so that
+// load overlaps the attention's tail.
 constexpr int kMRows = 16;
+constexpr int kMThreads = 256;
 
-__global__ void __launch_bounds__(128) merge_project_kernel(const DecodeArgs a,
-                                                            const __nv_bfloat16* __restrict__ wts,
-                                                            __nv_bfloat16* __restrict__ y) {
+// z of rows b[0], b[1] (lane = 4 of the 128 columns).  Every load a row may
+// need -- its length, its partial count, its z row, the (m, l) pair of split
+// `lane` and the first eight partial rows -- is issued before any is used
+// (all lie inside the row's slots, so the ones the row turns out not to need
+// are harmless), so the two rows cost about one memory latency, not three
+// each.
+__device__ __forceinline__ void merge_rows2(const DecodeArgs& a, const __nv_bfloat16* z,
+                                            const int (&b)[2], int h, int lane, int limit,
+                                            float4 (&o)[2]) {
+  constexpr int kPre = 8;
+  int n[2], np[2];
+  int64_t base[2];
+  uint2 zr[2];
+  float ms[2], ls[2];
+  float4 v[2][kPre];
+  const float4* acc4 = reinterpret_cast<const float4*>(a.ws_acc);
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const bool in = b[r] < a.num_seqs;
+    const int64_t row = (int64_t)(in ? b[r] : 0) * a.num_q_heads + h;
+    base[r] = row * a.max_splits;
+    n[r] = in ? a.seq_lens[b[r]] : 0;
+    np[r] = in && a.balanced ? a.ws_np[b[r]] : 0;
+    zr[r] = *reinterpret_cast<const uint2*>(z + row * kGD + 4 * lane);
+    ms[r] = -INFINITY;
+    ls[r] = 0.f;
+    if (a.max_splits > 1 && lane < a.max_splits) {
+      ms[r] = a.ws_ml[(base[r] + lane) * 2];
+      ls[r] = a.ws_ml[(base[r] + lane) * 2 + 1];
+    }
+#pragma unroll
+    for (int i = 0; i < kPre; ++i)
+      v[r][i] = (a.max_splits > 1 && i < a.max_splits) ? acc4[(base[r] + i) * (kGD / 4) + lane]
+                                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    o[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (n[r] < 1 || n[r] > limit) continue;   // reported by the attention kernel
+    const int ns = a.balanced ? np[r] : (n[r] + a.split_tokens - 1) / a.split_tokens;
+    if (ns <= 1) {
+      o[r] = make_float4(bf16lo(zr[r].x), bf16hi(zr[r].x), bf16lo(zr[r].y), bf16hi(zr[r].y));
+      continue;
+    }
+    float M = lane < ns ? ms[r] : -INFINITY;
+    for (int s = lane + 32; s < ns; s += 32) M = fmaxf(M, a.ws_ml[(base[r] + s) * 2]);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < ns; s0 += 32) {
+      float wl = 0.f;
+      if (s0 + lane < ns) {
+        const float m_s = s0 == 0 ? ms[r] : a.ws_ml[(base[r] + s0 + lane) * 2];
+        const float l_s = s0 == 0 ? ls[r] : a.ws_ml[(base[r] + s0 + lane) * 2 + 1];
+        wl = m_s == -INFINITY ? 0.f : exp2f(m_s - M);
+        L = fmaf(wl, l_s, L);
+      }
+      const int cnt = min(32, ns - s0);
+      for (int k = 0; k < cnt; k += kPre) {
+#pragma unroll
+        for (int i = 0; i < kPre; ++i) {
+          if (k + i >= cnt) break;
+          const float4 x = (s0 == 0 && k == 0) ? v[r][i]
+                                               : acc4[(base[r] + s0 + k + i) * (kGD / 4) + lane];
+          const float wgt = __shfl_sync(0xffffffffu, wl, (k + i) & 31);
+          acc.x = fmaf(wgt, x.x, acc.x);
+          acc.y = fmaf(wgt, x.y, acc.y);
+          acc.z = fmaf(wgt, x.z, acc.z);
+          acc.w = fmaf(wgt, x.w, acc.w);
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    const float inv = 1.f / L;
+    o[r] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  }
+}
+
+__global__ void __launch_bounds__(kMThreads) merge_project_kernel(const DecodeArgs a,
+                                                                  const __nv_bfloat16* __restrict__ wts,
+                                                                  __nv_bfloat16* __restrict__ y) {
   __shared__ __align__(16) __nv_bfloat16 ws[kGD * kGRow];
   __shared__ __align__(16) __nv_bfloat16 zs[kMRows * kGRow];
   const int h = blockIdx.y, b0 = blockIdx.x * kMRows;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const __nv_bfloat16* wh = wts + (int64_t)h * kGD * kGD;
-  for (int i = tid; i < kGD * 16; i += 128) {
+  for (int i = tid; i < kGD * 16; i += kMThreads) {
     const int r = i >> 4, c = i & 15;
     *reinterpret_cast<uint4*>(ws + r * kGRow + c * 8) =
         __ldg(reinterpret_cast<const uint4*>(wh + (int64_t)r * kGD) + c);
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // ---- z rows: warp w merges rows 4w .. 4w + 3; lane = 4 of the 128 columns
+  // ---- z rows 2w, 2w + 1
   const int limit = min(a.max_seq_len, a.max_blocks_per_seq * kBlockSize);
   const __nv_bfloat16* z = static_cast<const __nv_bfloat16*>(a.out);
-  for (int rr = 0; rr < kMRows / 4; ++rr) {
-    const int r = warp * (kMRows / 4) + rr, b = b0 + r;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    const int n = b < a.num_seqs ? a.seq_lens[b] : 0;
-    if (n >= 1 && n <= limit) {
-      const int ns = a.balanced ? a.ws_np[b] : (n + a.split_tokens - 1) / a.split_tokens;
-      const int64_t row = (int64_t)b * a.num_q_heads + h;
-      if (ns <= 1) {
-        const uint2 v = *reinterpret_cast<const uint2*>(z + row * kGD + 4 * lane);
-        o = make_float4(bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y));
-      } else {
-        const int64_t base = row * a.max_splits;
-        float M = -INFINITY;
-        for (int s = lane; s < ns; s += 32) M = fmaxf(M, a.ws_ml[(base + s) * 2]);
+  {
+    const int rows[2] = {b0 + 2 * warp, b0 + 2 * warp + 1};
+    float4 o[2];
+    merge_rows2(a, z, rows, h, lane, limit, o);
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        float L = 0.f;
-        for (int s = 0; s < ns; ++s) {
-          const float ms = a.ws_ml[(base + s) * 2];
-          const float w = ms == -INFINITY ? 0.f : exp2f(ms - M);
-          const float4 v = reinterpret_cast<const float4*>(a.ws_acc + (base + s) * kGD)[lane];
-          L = fmaf(w, a.ws_ml[(base + s) * 2 + 1], L);
-          o.x = fmaf(w, v.x, o.x);
-          o.y = fmaf(w, v.y, o.y);
-          o.z = fmaf(w, v.z, o.z);
-          o.w = fmaf(w, v.w, o.w);
-        }
-        const float inv = 1.f / L;
-        o = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
-      }
+    for (int rr = 0; rr < 2; ++rr) {
+      __nv_bfloat162* zr = reinterpret_cast<__nv_bfloat162*>(zs + (2 * warp + rr) * kGRow + 4 * lane);
+      zr[0] = __floats2bfloat162_rn(o[rr].x, o[rr].y);
+      zr[1] = __floats2bfloat162_rn(o[rr].z, o[rr].w);
     }
-    __nv_bfloat162* zr = reinterpret_cast<__nv_bfloat162*>(zs + r * kGRow + 4 * lane);
-    zr[0] = __floats2bfloat162_rn(o.x, o.y);
-    zr[1] = __floats2bfloat162_rn(o.z, o.w);
   }
   __syncthreads();
-  // ---- o = z W_V[h]^T for the 16 rows: this warp's 32 columns
+  // ---- o = z W_V[h]^T for the 16 rows: this warp's 16 columns
   const int g = lane >> 2, t = lane & 3;
   const uint32_t wbase = smem_u32(ws), zbase = smem_u32(zs);
   const int mi = lane >> 3, rr8 = lane & 7;
-  const int n0 = warp * 32;
-  float acc[4][4];
+  const int n0 = warp * 16;
+  float acc[2][4];
 #pragma unroll
-  for (int n = 0; n < 4; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+  for (int n = 0; n < 2; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
-    uint32_t af[4];
+    uint32_t af[4], b[4];
     ldsm4(zbase + (uint32_t)((rr8 + ((mi & 1) << 3)) * kGRow + ks * 16 + ((mi >> 1) << 3)) * 2, af);
-#pragma unroll
-    for (int np = 0; np < 2; ++np) {
-      uint32_t b[4];
-      const int n = n0 + np * 16 + ((mi >> 1) << 3) + rr8;
-      const int k = ks * 16 + ((mi & 1) << 3);
-      ldsm4(wbase + (uint32_t)(n * kGRow + k) * 2, b);
-      mma16816g(acc[2 * np], af[0], af[1], af[2], af[3], b[0], b[1]);
-      mma16816g(acc[2 * np + 1], af[0], af[1], af[2], af[3], b[2], b[3]);
-    }
+    const int n = n0 + ((mi >> 1) << 3) + rr8;
+    const int k = ks * 16 + ((mi & 1) << 3);
+    ldsm4(wbase + (uint32_t)(n * kGRow + k) * 2, b);
+    mma16816g(acc[0], af[0], af[1], af[2], af[3], b[0], b[1]);
+    mma16816g(acc[1], af[0], af[1], af[2], af[3], b[2], b[3]);
   }
   const int ra = b0 + g, rb = b0 + g + 8;
 #pragma unroll
-  for (int n = 0; n < 4; ++n) {
+  for (int n = 0; n < 2; ++n) {
     const int col = n0 + n * 8 + 2 * t;
     if (ra < a.num_seqs)
       *reinterpret_cast<__nv_bfloat162*>(y + ((int64_t)ra * a.num_q_heads + h) * kGD + col) =
@@ -223,7 +278,7 @@ cudaError_t launch_merge_project(const DecodeArgs& a, const void* w_v, void* out
   if (a.head_dim != kGD || a.num_kv_heads != 1) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((a.num_seqs + kMRows - 1) / kMRows, a.num_q_heads);
-  cfg.blockDim = dim3(128);
+  cfg.blockDim = dim3(kMThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
