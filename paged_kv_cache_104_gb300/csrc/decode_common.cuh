@@ -34,26 +34,37 @@ __device__ __forceinline__ void plan_units(const DecodeArgs& a, int* cu, int sta
     int carry = 0;
     if (lane == 0) cu[0] = 0;
     const int limit = min(a.max_seq_len, a.max_blocks_per_seq * kBlockSize);
-    for (int base = 0; base < a.num_seqs; base += 32) {
-      const int b = base + lane;
-      int units = 0;
-      if (b < a.num_seqs) {
-        const int n = row_len(a, b);
-        if (n < 1 || n > limit) {
-          record_error(a.err, DEVERR_SEQLEN_RANGE);
-        } else {
-          const int per = stage_tok > 0 ? stage_tok : a.split_tokens;
-          units = a.num_kv_heads * ((n + per - 1) / per + (stage_tok > 0 ? pad : 0));
-        }
-      }
-      int x = units;
+    // eight windows of 32 lengths are requested before the first is scanned,
+    // so their load latencies overlap
+    for (int base = 0; base < a.num_seqs; base += 256) {
+      int n[8];
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(kAll, x, o);
-        if (lane >= o) x += y;
+      for (int k = 0; k < 8; ++k) {
+        const int b = base + 32 * k + lane;
+        n[k] = b < a.num_seqs ? row_len(a, b) : 0;
       }
-      if (b < a.num_seqs) cu[b + 1] = carry + x;
-      carry += __shfl_sync(kAll, x, 31);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (base + 32 * k >= a.num_seqs) break;
+        const int b = base + 32 * k + lane;
+        int units = 0;
+        if (b < a.num_seqs) {
+          if (n[k] < 1 || n[k] > limit) {
+            record_error(a.err, DEVERR_SEQLEN_RANGE);
+          } else {
+            const int per = stage_tok > 0 ? stage_tok : a.split_tokens;
+            units = a.num_kv_heads * ((n[k] + per - 1) / per + (stage_tok > 0 ? pad : 0));
+          }
+        }
+        int x = units;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(kAll, x, o);
+          if (lane >= o) x += y;
+        }
+        if (b < a.num_seqs) cu[b + 1] = carry + x;
+        carry += __shfl_sync(kAll, x, 31);
+      }
     }
   }
 }

@@ -14,11 +14,13 @@
 // work per byte of the GQA decode, so the products go to the tensor core and
 // the warps keep only the softmax.  Per 128-key tile of latents (32 KiB):
 //   S^T  = C . Q~^T    M = 128 keys,  N = 32 heads,   K = 128 rank
-//   O^T += C^T . P^T   M = 128 rank,  N = 64 (32 heads, 32 unused), K = 128 keys
+//   O^T += C^T . P^T   M = 128 rank,  N = 32 heads,   K = 128 keys
 // The tile C is read by both products from the same shared-memory copy: as a
 // K-major A operand for the scores and as an MN-major A operand for P V.
 // S^T and O^T live in TMEM (fp32); P^T goes through shared memory (bf16, the
-// B operand), heads contiguous per key.
+// B operand), heads contiguous per key: two tiles' P^T share one buffer of
+// 128-byte rows, a half each, which leaves room for a five-tile latent ring
+// (the ring's depth sets how many bytes are in flight per SM).
 //
 // Layout of a tile.  Each 16-token block (4 KiB) arrives in one TMA box of a
 // 4-D view of the pool (column, row of 8, half, 8-row group) and lands as
@@ -73,20 +75,22 @@ namespace {
 constexpr int kTK = 128;                        // keys per tile
 constexpr int kR = 128;                         // latent rank
 constexpr int kNH = 32;                         // query heads
-constexpr int kNPV = 64;                        // P^T / O^T columns (32 heads + 32 unused)
+constexpr int kNPV = 32;                        // P^T / O^T columns: the 32 heads
 constexpr int kBlkPerTile = kTK / kBlockSize;   // 8
 constexpr int kBlockBytes = kBlockSize * kR * 2;   // 4 KiB
 constexpr int kTileBytes = kTK * kR * 2;        // 32 KiB
-constexpr int kNS = 4;                          // latent ring depth (tiles)
+constexpr int kNS = 5;                          // latent ring depth (tiles)
 constexpr int kQBytes = kNH * kR * 2;           // 8 KiB: q~ of one sequence
 constexpr int kQHalf = kQBytes / 2;             // one 64-column half, 32 rows
-constexpr int kPBytes = kTK * 128;              // P^T: 128 keys x 128 B (64 columns)
+// P^T of two tiles in one buffer of 128 keys x 128-byte rows: tile parity b
+// holds its 32 heads in bytes 64 b .. 64 b + 63 of each row
+constexpr int kPBytes = kTK * 128;
 constexpr int kThreadsT = 224;
 constexpr int kSoft = 128;                      // softmax threads
 constexpr int W_PROD = 4, W_MMA = 5, W_PV = 6;
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 128;
 constexpr uint32_t COL_S = 0;                   // S^T of tile parity b at 32 b
-constexpr uint32_t COL_O = 64;                  // O^T of unit parity b at 64 + 64 b
+constexpr uint32_t COL_O = 64;                  // O^T of unit parity b at 64 + 32 b
 constexpr float kLazyT = 8.0f;
 constexpr unsigned kAllT = 0xffffffffu;
 constexpr int kStageTokT = kTK;                 // the balanced walk's stage: one tile
@@ -100,8 +104,8 @@ constexpr int kPadT = 6;
 
 constexpr int OFF_RING = 0;
 constexpr int OFF_Q = OFF_RING + kNS * kTileBytes;          // [2] q~
-constexpr int OFF_P = OFF_Q + 2 * kQBytes;                  // [2] P^T
-constexpr int OFF_RED = OFF_P + 2 * kPBytes;                // [2][32 heads][4 warps] fp32 (max)
+constexpr int OFF_P = OFF_Q + 2 * kQBytes;                  // P^T of both tile parities
+constexpr int OFF_RED = OFF_P + kPBytes;                    // [2][32 heads][4 warps] fp32 (max)
 constexpr int OFF_SUM = OFF_RED + 2 * kNH * 4 * 4;          // [2][32 heads][4 warps] fp32 (sums)
 constexpr int OFF_BAR = OFF_SUM + 2 * kNH * 4 * 4;
 
@@ -230,9 +234,8 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c,
     *abort_i = 0;
     fence_mbar_init();
   }
-  // P^T columns 32..63 are never written: zero them once (they only feed the
-  // unused O^T columns, but stay finite)
-  for (int i = tid; i < 2 * kPBytes / 16; i += kThreadsT)
+  // P^T starts finite (every byte a product reads is written before it is read)
+  for (int i = tid; i < kPBytes / 16; i += kThreadsT)
     reinterpret_cast<uint4*>(smem + OFF_P)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   if (warp == W_MMA) {
@@ -255,6 +258,9 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c,
     __syncthreads();
   }
   const uint32_t tmem = *tmem_slot;
+  // the merge + up-projection launched next may start now: it stages W_V
+  // while this grid runs and waits for it to finish before reading results
+  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   auto tile_info = [&](const Unit& u, int i, int ntile) {
     TileInfo ti;
@@ -275,19 +281,14 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c,
     const uint64_t policy = policy_evict_first();
     uint32_t t = 0, ui = 0;
     bool ok = true;
-    // 32 block ids of piece v from its block `first` on, one per lane
+    // 32 block ids of piece v from its block `first` on, one per lane (the
+    // range check comes at use, so a look-ahead request does not wait)
     auto load_ids = [&](const Unit& v, int first) {
       const int blk0 = v.tok_begin / kBlockSize;
       const int nblk = (v.tok_end - 1) / kBlockSize - blk0 + 1;
-      int id = 0;
-      if (first + lane < nblk) {
-        id = __ldg(a.block_table + (int64_t)v.b * a.bt_stride + blk0 + first + lane);
-        if (id < 0 || (int64_t)id >= a.num_blocks) {
-          record_error(a.err, DEVERR_BLOCK_RANGE);
-          id = 0;  // read a valid block instead; the error word reports it
-        }
-      }
-      return id;
+      return first + lane < nblk
+                 ? __ldg(a.block_table + (int64_t)v.b * a.bt_stride + blk0 + first + lane)
+                 : 0;
     };
     // The walk is looked at one piece ahead: the next piece's first block ids
     // are requested when this piece starts, so a switch between pieces does
@@ -336,7 +337,11 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c,
         ok = __shfl_sync(kAllT, (int)ok, 0) != 0;
         if (!ok) break;
         const int nb = min(kBlkPerTile, nblk - i * kBlkPerTile);
-        const int blk = __shfl_sync(kAllT, ids, (i * kBlkPerTile + (lane & 7)) & 31);
+        int blk = __shfl_sync(kAllT, ids, (i * kBlkPerTile + (lane & 7)) & 31);
+        if (lane < nb && (blk < 0 || (int64_t)blk >= a.num_blocks)) {
+          record_error(a.err, DEVERR_BLOCK_RANGE);
+          blk = 0;  // read a valid block instead; the error word reports it
+        }
         const uint32_t fb = bar(B_CF + slot);
         if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)(nb * kBlockBytes));
         __syncwarp();
@@ -404,12 +409,13 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c,
             ok = __all_sync(kAllT, wait_fast(bar(B_OE + (ui & 1)), ((ui >> 1) - 1) & 1, abort_flag, a.err));
           if (!ok) break;
           tc_fence_after();
-          const uint32_t pt = sbase + OFF_P + (t & 1) * kPBytes;
+          const uint32_t pt = sbase + OFF_P + (t & 1) * 64;
 #pragma unroll
           for (int kk = 0; kk < kTK / 16; ++kk) {
             // A = C^T (MN-major): rank halves 1 KiB apart, 8-key atoms 2 KiB apart
             const uint64_t ad = make_sw128_desc(ct + kk * 2 * 2048, 1024, 2048);
-            // B = P^T (MN-major): 8-key atoms of 128-byte rows, 1 KiB apart
+            // B = P^T (MN-major, N = 32): this tile parity's half of the
+            // 128-byte rows, 8-key atoms 1 KiB apart
             const uint64_t bd = make_sw128_desc(pt + kk * 16 * 128, 16, 1024);
             mma_ss_e(tmem + COL_O + (ui & 1) * kNPV, ad, bd, idesc_o, (i == 0 && kk == 0) ? 0u : 1u);
           }
@@ -534,10 +540,9 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c,
         }
         // P^T of tile t - 2 has been read by its P V
         if (t >= 2) wait_fast(bar(B_PE + (t & 1)), ((t >> 1) - 1) & 1, abort_flag, a.err);
-        unsigned char* prow = prow0 + (t & 1) * kPBytes;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
-          *reinterpret_cast<uint4*>(prow + ((c ^ (j & 7)) << 4)) =
+          *reinterpret_cast<uint4*>(prow0 + (((c + 4 * (t & 1)) ^ (j & 7)) << 4)) =
               make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
         if (!kval) {
           // zero this key's latent row (both halves): stale pool bytes must

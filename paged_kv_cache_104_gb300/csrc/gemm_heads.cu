@@ -54,6 +54,19 @@ __global__ void __launch_bounds__(128) gemm_heads_kernel(__nv_bfloat16* __restri
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
   const __nv_bfloat16* wh = wts + (int64_t)h * kGD * kGD;
+  // this warp's 16 rows of x first: their loads overlap the staging of W
+  const int r0 = blockIdx.x * 64 + warp * 16;
+  uint32_t af[8][4];
+  const int ra = r0 + g, rb = r0 + g + 8;
+  const uint32_t* xa = reinterpret_cast<const uint32_t*>(x + ((int64_t)ra * heads + h) * kGD);
+  const uint32_t* xb = reinterpret_cast<const uint32_t*>(x + ((int64_t)rb * heads + h) * kGD);
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    af[ks][0] = ra < rows ? __ldg(xa + ks * 8 + t) : 0u;
+    af[ks][1] = rb < rows ? __ldg(xb + ks * 8 + t) : 0u;
+    af[ks][2] = ra < rows ? __ldg(xa + ks * 8 + 4 + t) : 0u;
+    af[ks][3] = rb < rows ? __ldg(xb + ks * 8 + 4 + t) : 0u;
+  }
   if (W_IS_NK) {   // rows n0 .. n0+31 of W[n][k], 16 chunks each
     for (int i = tid; i < kQ * 16; i += 128) {
       const int r = i >> 4, c = i & 15;
@@ -68,19 +81,7 @@ __global__ void __launch_bounds__(128) gemm_heads_kernel(__nv_bfloat16* __restri
     }
   }
   __syncthreads();
-  const int r0 = blockIdx.x * 64 + warp * 16;
   if (r0 >= rows) return;
-  uint32_t af[8][4];
-  const int ra = r0 + g, rb = r0 + g + 8;
-  const uint32_t* xa = reinterpret_cast<const uint32_t*>(x + ((int64_t)ra * heads + h) * kGD);
-  const uint32_t* xb = reinterpret_cast<const uint32_t*>(x + ((int64_t)rb * heads + h) * kGD);
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    af[ks][0] = ra < rows ? __ldg(xa + ks * 8 + t) : 0u;
-    af[ks][1] = rb < rows ? __ldg(xb + ks * 8 + t) : 0u;
-    af[ks][2] = ra < rows ? __ldg(xa + ks * 8 + 4 + t) : 0u;
-    af[ks][3] = rb < rows ? __ldg(xb + ks * 8 + 4 + t) : 0u;
-  }
   const uint32_t wbase = smem_u32(ws);
   const int mi = lane >> 3, rr = lane & 7;
   float acc[4][4];
