@@ -522,7 +522,7 @@ pkv_status pkv_mla_decode_attention(void* out, const void* q, const void* w_k, c
   void* z = ws + vec;        // attention over the latent [B][Hq][rank] bf16
   char* part = ws + 2 * vec;
   // 1) q~_h = W_K[h]^T q_h
-  if (pkv::launch_gemm_heads(q_lat, q, w_k, num_seqs, num_q_heads, false, s) != cudaSuccess)
+  if (pkv::launch_gemm_heads(q_lat, q, w_k, num_seqs, num_q_heads, s) != cudaSuccess)
     return PKV_ECUDA;
   // 2) z_h = softmax(scale q~_h . C^T) C over the latent pool
   const int splits = partial_slots_for(max_seq_len);

@@ -26,8 +26,10 @@ __device__ __forceinline__ int row_len(const DecodeArgs& a, int b) {
 // plus `pad` stages that hold no tokens, prefix-summed.  The padding stands
 // for the fixed cost of a piece (loading its queries, writing its result):
 // a CTA whose share starts many short sequences then gets fewer tokens.
+// lens (optional, shared memory): every sequence's length is kept there too,
+// so the walk does not read it from global memory at each unit.
 __device__ __forceinline__ void plan_units(const DecodeArgs& a, int* cu, int stage_tok = 0,
-                                           int pad = 0) {
+                                           int pad = 0, int* lens = nullptr) {
   const int lane = threadIdx.x & 31;
   constexpr unsigned kAll = 0xffffffffu;
   if (threadIdx.x < 32) {
@@ -62,14 +64,18 @@ __device__ __forceinline__ void plan_units(const DecodeArgs& a, int* cu, int sta
           const int y = __shfl_up_sync(kAll, x, o);
           if (lane >= o) x += y;
         }
-        if (b < a.num_seqs) cu[b + 1] = carry + x;
+        if (b < a.num_seqs) {
+          cu[b + 1] = carry + x;
+          if (lens) lens[b] = n[k];
+        }
         carry += __shfl_sync(kAll, x, 31);
       }
     }
   }
 }
 
-__device__ __forceinline__ Unit find_unit(const DecodeArgs& a, const int* cu, int w) {
+__device__ __forceinline__ Unit find_unit(const DecodeArgs& a, const int* cu, int w,
+                                          const int* lens = nullptr) {
   // largest b with cu[b] <= w  (cu is non-decreasing, cu[0] = 0 <= w < cu[B])
   int lo = 0, hi = a.num_seqs - 1;
   while (lo < hi) {
@@ -82,7 +88,7 @@ __device__ __forceinline__ Unit find_unit(const DecodeArgs& a, const int* cu, in
   u.ns = (cu[lo + 1] - cu[lo]) / a.num_kv_heads;
   u.g = rem / u.ns;
   u.s = rem - u.g * u.ns;
-  const int n = row_len(a, lo);
+  const int n = lens ? lens[lo] : row_len(a, lo);
   u.tok_begin = u.s * a.split_tokens;
   u.tok_end = min(n, u.tok_begin + a.split_tokens);
   return u;
@@ -105,6 +111,7 @@ __device__ __forceinline__ int seq_of(const DecodeArgs& a, const int* cu, int64_
 // and ns their number (the CTAs its stages fall to).
 struct Walk {
   bool balanced;
+  const int* lens;   // sequence lengths in shared memory, or null (read seq_lens)
   int total;     // units (split walk) or stages (balanced walk)
   int w;         // split walk: next unit
   int64_t pos;   // balanced walk: next stage, and the end of this CTA's share
@@ -124,14 +131,22 @@ inline bool stage_plan_fits(const DecodeArgs& a, int stage_tok, int pad = 0) {
          (int64_t)INT_MAX;
 }
 
-// The CTA whose share holds stage p.
+// The CTA whose share holds stage p.  Units of work are cut where streams
+// change, so every role of every CTA evaluates this at each of its units:
+// 32-bit division when the operands fit (they do for any realistic batch), as
+// a 64-bit division takes hundreds of cycles.
 __device__ __forceinline__ int cta_of_stage(int64_t p, int64_t total) {
-  return (int)(((p + 1) * (int64_t)gridDim.x - 1) / total);
+  const uint64_t num = (uint64_t)(p + 1) * gridDim.x - 1;
+  if ((num >> 32) == 0 && ((uint64_t)total >> 32) == 0)
+    return (int)((uint32_t)num / (uint32_t)total);
+  return (int)(num / (uint64_t)total);
 }
 
-__device__ __forceinline__ Walk walk_begin(const DecodeArgs& a, const int* cu, bool balanced) {
+__device__ __forceinline__ Walk walk_begin(const DecodeArgs& a, const int* cu, bool balanced,
+                                           const int* lens = nullptr) {
   Walk k;
   k.balanced = balanced;
+  k.lens = lens;
   k.total = cu[a.num_seqs];
   k.w = blockIdx.x;
   k.pos = (int64_t)blockIdx.x * k.total / gridDim.x;
@@ -146,7 +161,7 @@ __device__ __forceinline__ bool walk_next(const DecodeArgs& a, const int* cu, in
                                           Walk& k, Unit& u, int pad = 0) {
   if (!k.balanced) {
     if (k.w >= k.total) return false;
-    u = find_unit(a, cu, k.w);
+    u = find_unit(a, cu, k.w, k.lens);
     k.w += gridDim.x;
     return true;
   }
@@ -169,7 +184,7 @@ __device__ __forceinline__ bool walk_next(const DecodeArgs& a, const int* cu, in
     u.s = (int)blockIdx.x - c0;
     u.ns = cta_of_stage(s_end - 1, k.total) - c0 + 1;
     u.tok_begin = st0 * stage_tok;
-    u.tok_end = min(row_len(a, b), (st0 + len) * stage_tok);
+    u.tok_end = min(k.lens ? k.lens[b] : row_len(a, b), (st0 + len) * stage_tok);
     k.pos += len;
     return true;
   }

@@ -102,6 +102,12 @@ constexpr int kMinStagesT = kSplitTokens / kStageTokT;   // shares of at least 4
 // a sequence of n tokens still falls to at most ceil(n / 512) + 1 CTAs.
 constexpr int kPadT = 6;
 
+// The producer walks the CTA's share and publishes each piece (sequence,
+// piece index and count, token range) in a small ring; the other roles read
+// it there instead of walking themselves.  Measured: the walk's code, run
+// once per piece by the softmax warps, cost them about 1.5 us per piece
+// boundary (it is too rarely run to stay in the instruction cache).
+constexpr int kND = 4;
 constexpr int OFF_RING = 0;
 constexpr int OFF_Q = OFF_RING + kNS * kTileBytes;          // [2] q~
 constexpr int OFF_P = OFF_Q + 2 * kQBytes;                  // P^T of both tile parities
@@ -121,9 +127,13 @@ enum {
   B_OF = B_PE + 2,          // [2]  O^T of a unit complete
   B_OE = B_OF + 2,          // [2]  O^T read out by the epilogue
   B_DRAIN = B_OE + 2,       // [2] each issuer's last products done
-  B_COUNT = B_DRAIN + 2
+  B_DF = B_DRAIN + 2,       // [kND] a piece descriptor published
+  B_DE = B_DF + kND,        // [kND] a piece descriptor read by every role
+  B_COUNT = B_DE + kND
 };
-constexpr int OFF_TSLOT = OFF_BAR + B_COUNT * 8;
+constexpr int OFF_PD = OFF_BAR + B_COUNT * 8;               // [kND] piece descriptors, 8 ints each
+constexpr int OFF_SP = OFF_PD + kND * 32;                   // [2] the softmax warps' copy
+constexpr int OFF_TSLOT = OFF_SP + 2 * 32;
 constexpr int OFF_ABORT = OFF_TSLOT + 4;
 constexpr int OFF_CU = OFF_TSLOT + 16;
 static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "swizzled operands need 1 KiB alignment");
@@ -231,6 +241,10 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c,
     }
     mbar_init(bar(B_DRAIN), 1);
     mbar_init(bar(B_DRAIN + 1), 1);
+    for (int i = 0; i < kND; ++i) {
+      mbar_init(bar(B_DF + i), 1);
+      mbar_init(bar(B_DE + i), 3);   // the two issuers and the softmax warps' leader
+    }
     *abort_i = 0;
     fence_mbar_init();
   }
@@ -246,7 +260,10 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c,
   }
   // balanced walk over 128-token stages when the batch gives every CTA at
   // least 512 tokens; otherwise 512-token splits
-  plan_units(a, cu, a.balanced ? kStageTokT : 0, kPadT);
+  // the sequence lengths after the prefix sums, when they fit (the launcher
+  // sized shared memory for them if so)
+  int* lens = a.lens_in_smem ? cu + a.num_seqs + 1 : nullptr;
+  plan_units(a, cu, a.balanced ? kStageTokT : 0, kPadT, lens);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -254,10 +271,11 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c,
       a.balanced && (int64_t)cu[a.num_seqs] >= (int64_t)kMinStagesT * gridDim.x;
   if (a.balanced && !balanced) {
     __syncthreads();
-    plan_units(a, cu);
+    plan_units(a, cu, 0, 0, lens);
     __syncthreads();
   }
   const uint32_t tmem = *tmem_slot;
+  int* pd = reinterpret_cast<int*>(smem + OFF_PD);
   // the merge + up-projection launched next may start now: it stages W_V
   // while this grid runs and waits for it to finish before reading results
   if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -293,7 +311,7 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c,
     // The walk is looked at one piece ahead: the next piece's first block ids
     // are requested when this piece starts, so a switch between pieces does
     // not wait for a block-table read.
-    Walk wk = walk_begin(a, cu, balanced);
+    Walk wk = walk_begin(a, cu, balanced, lens);
     Unit u, nu;
     bool have = walk_next(a, cu, kStageTokT, wk, u, kPadT);
     int ids = have ? load_ids(u, 0) : 0;
@@ -311,12 +329,33 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c,
       ok = __shfl_sync(kAllT, (int)ok, 0) != 0;
       if (ok) ++ui;
     };
+    // publish piece v (or, with end set, the end of the walk) to the others
+    uint32_t di = 0;
+    auto publish = [&](const Unit& v, bool end) {
+      if (lane == 0) {
+        if (di >= (uint32_t)kND)
+          ok = ok && wait_or_abort(bar(B_DE + di % kND), ((di / kND) - 1) & 1, abort_flag, a.err);
+        if (ok) {
+          int* d = pd + (di % kND) * 8;
+          d[0] = end ? -1 : v.b;
+          d[1] = v.s;
+          d[2] = v.ns;
+          d[3] = v.tok_begin;
+          d[4] = v.tok_end;
+          mbar_arrive(bar(B_DF + di % kND));   // release: the descriptor is visible to its readers
+        }
+      }
+      ok = __shfl_sync(kAllT, (int)ok, 0) != 0;
+      ++di;
+    };
     // q~ comes from the kernel before this one in the stream: launched as its
     // programmatic dependent, this grid may start before that one has
     // finished.  The latents do not depend on it, so the first piece's first
     // tiles are requested before waiting for it; its q~ right after.
     bool first_piece = true;
     while (ok && have) {
+      publish(u, false);
+      if (!ok) break;
       const bool have_next = walk_next(a, cu, kStageTokT, wk, nu, kPadT);
       const int next_ids = have_next ? load_ids(nu, 0) : 0;
       const int nblk = (u.tok_end - 1) / kBlockSize - u.tok_begin / kBlockSize + 1;
@@ -357,6 +396,7 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c,
       have = have_next;
       ids = next_ids;
     }
+    if (ok) publish(u, true);
     if (!ok && lane == 0) {  // after an abort, let the copies already issued land
       const uint32_t first = t > (uint32_t)kNS ? t - kNS : 0;
       for (uint32_t i = first; i < t; ++i) mbar_wait(bar(B_CF + (i % kNS)), (i / kNS) & 1, nullptr);
@@ -376,9 +416,20 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c,
     const bool is_s = warp == W_MMA;
     bool ok = true;
     uint32_t t = 0, ui = 0;
-    Walk wk = walk_begin(a, cu, balanced);
-    Unit u;
-    while (ok && walk_next(a, cu, kStageTokT, wk, u, kPadT)) {
+    while (ok) {
+      // the next piece, as the producer published it
+      ok = __all_sync(kAllT, wait_or_abort(bar(B_DF + ui % kND), (ui / kND) & 1, abort_flag, a.err));
+      if (!ok) break;
+      Unit u;
+      const int* d = pd + (ui % kND) * 8;
+      u.b = d[0];
+      u.s = d[1];
+      u.ns = d[2];
+      u.tok_begin = d[3];
+      u.tok_end = d[4];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_DE + ui % kND));
+      if (u.b < 0) break;   // the end of the walk
       const int ntile = tiles_of(u);
       if (is_s) {
         ok = __all_sync(kAllT, wait_or_abort(bar(B_QF + (ui & 1)), (ui >> 1) & 1, abort_flag, a.err));
@@ -445,9 +496,33 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c,
     const uint32_t crow = (uint32_t)((j >> 3) * 2048 + (j & 7) * 128);
     float m[kNH], l[kNH];
     uint32_t t = 0, ui = 0;
-    Walk wk = walk_begin(a, cu, balanced);
-    Unit u;
-    while (walk_next(a, cu, kStageTokT, wk, u, kPadT)) {
+    int* sp = reinterpret_cast<int*>(smem + OFF_SP);
+    while (true) {
+      // the next piece: the leader takes it from the producer's ring and
+      // hands it to the four warps, which then agree on it even after an
+      // abort (every named barrier must be reached by all of them)
+      if (tid == 0) {
+        int* dst = sp + (ui & 1) * 8;
+        if (wait_or_abort(bar(B_DF + ui % kND), (ui / kND) & 1, abort_flag, a.err)) {
+          const int* d = pd + (ui % kND) * 8;
+#pragma unroll
+          for (int k = 0; k < 5; ++k) dst[k] = d[k];
+          mbar_arrive(bar(B_DE + ui % kND));
+        } else {
+          dst[0] = -1;
+        }
+      }
+      named_bar_sync(1, kSoft);
+      Unit u;
+      {
+        const int* d = sp + (ui & 1) * 8;
+        u.b = d[0];
+        u.s = d[1];
+        u.ns = d[2];
+        u.tok_begin = d[3];
+        u.tok_end = d[4];
+      }
+      if (u.b < 0) break;   // the end of the walk (or an abort)
       // the merge reads how many partials this sequence left
       if (a.balanced && u.s == 0 && tid == 0) a.ws_np[u.b] = u.ns;
 #pragma unroll
@@ -500,18 +575,17 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c,
           for (int h = 1; h < kNH; ++h) m_old = lane == h ? m[h] : m_old;
           float m_new = m_old;
           if (mx > m_new + kLazyT || m_new == -INFINITY) m_new = mx;
-          const float alpha_l = (m_new == m_old) ? 1.f : fast_exp2(m_old - m_new);
-          const bool rescale = __any_sync(kAllT, alpha_l != 1.f);
-          float alpha[kNH];
 #pragma unroll
-          for (int h = 0; h < kNH; ++h) {
-            m[h] = __shfl_sync(kAllT, m_new, h);
-            alpha[h] = __shfl_sync(kAllT, alpha_l, h);
-          }
-          if (rescale) {   // the same on every thread: m is uniform
+          for (int h = 0; h < kNH; ++h) m[h] = __shfl_sync(kAllT, m_new, h);
+          // the first tile of a piece has no sums or O^T to rescale yet
+          const float alpha_l = (ti.first || m_new == m_old) ? 1.f : fast_exp2(m_old - m_new);
+          if (__any_sync(kAllT, alpha_l != 1.f)) {   // the same on every thread: m is uniform
+            float alpha[kNH];
+#pragma unroll
+            for (int h = 0; h < kNH; ++h) alpha[h] = __shfl_sync(kAllT, alpha_l, h);
 #pragma unroll
             for (int h = 0; h < kNH; ++h) l[h] *= alpha[h];
-            if (!ti.first) {
+            {
               // O^T holds P V of this piece's earlier tiles: rescale it in
               // place once the last of those products has completed
               wait_fast(bar(B_PE + ((t - 1) & 1)), ((t - 1) >> 1) & 1, abort_flag, a.err);
@@ -630,8 +704,10 @@ cudaError_t launch_decode_mla(const DecodeArgs& args, const void* w_v, void* out
   CUtensorMap tm_c, tm_q;
   if (!encode_latent_block_map(&tm_c, a.k_cache, a.num_blocks)) return cudaErrorInvalidValue;
   if (!encode_rows32_map_bf16(&tm_q, a.q, (int64_t)a.num_seqs * kNH)) return cudaErrorInvalidValue;
-  const size_t smem = OFF_CU + sizeof(int) * (size_t)(a.num_seqs + 1);
+  size_t smem = OFF_CU + sizeof(int) * (size_t)(a.num_seqs + 1);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  a.lens_in_smem = smem + sizeof(int) * (size_t)a.num_seqs <= 227 * 1024;
+  if (a.lens_in_smem) smem += sizeof(int) * (size_t)a.num_seqs;
   cudaError_t e = allow_dynamic_smem(decode_mla_kernel, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t upper = (int64_t)a.num_seqs * a.max_splits;

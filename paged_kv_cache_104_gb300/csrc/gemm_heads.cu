@@ -1,15 +1,15 @@
 // Per-head projections for the latent (MLA-style) cache, on warp-level bf16
-// tensor-core tiles: Y[b][h][:] = X[b][h][:] . W[h] for every row b and head
-// h, with W[h] a 128 x 128 matrix.
-//   * the query absorption q~_h = W_K[h]^T q_h takes W_K[h] stored [D][r]
-//     as [K][N] (W_IS_NK = false);
-//   * the output up-projection o_h = W_V[h] z_h takes W_V[h] stored [D][r]
-//     as [N][K] (W_IS_NK = true).
-// One CTA of 4 warps covers one head, 64 rows and a quarter (32 columns) of
+// tensor-core tiles (mma.sync m16n8k16, fp32 accumulate).
+//   * The query absorption q~_h = W_K[h]^T q_h: Y[b][h][:] = X[b][h][:] . W[h]
+//     for every row b and head h, with W[h] = W_K[h] stored [D][r] = [K][N].
+//   * The merge of the latent attention's split partials fused with the
+//     output up-projection o_h = W_V[h] z_h (W_V[h] stored [D][r] = [N][K]);
+//     see merge_project_kernel.
+// Absorption: one CTA of 4 warps covers one head, 64 rows and a quarter (32 columns) of
 // the output, so that a decode batch of 64-128 rows still spreads over 256-512
 // CTAs.  The CTA's 32 columns of W[h] are staged in shared memory with rows
-// padded to 16 bytes beyond their length, so the ldmatrix reads of the B
-// fragments (transposed for [K][N]) are free of bank conflicts; a warp computes
+// padded to 16 bytes beyond their length, so the transposing ldmatrix reads of
+// the B fragments are free of bank conflicts; a warp computes
 // a 16 x 32 tile with 32 m16n8k16 products.  bf16 out, fp32 accumulation.
 #include "common.cuh"
 #include "launch.h"
@@ -39,7 +39,6 @@ __device__ __forceinline__ void ldsm4_t(uint32_t addr, uint32_t (&r)[4]) {
                : "r"(addr));
 }
 
-template <bool W_IS_NK>
 __global__ void __launch_bounds__(128) gemm_heads_kernel(__nv_bfloat16* __restrict__ y,
                                                          const __nv_bfloat16* __restrict__ x,
                                                          const __nv_bfloat16* __restrict__ wts,
@@ -48,8 +47,8 @@ __global__ void __launch_bounds__(128) gemm_heads_kernel(__nv_bfloat16* __restri
   // attention) may start now; it waits for this grid before reading y
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int kQ = 32;                 // output columns per CTA
-  // [K][N]: 128 k-rows x 32 columns (row 40 elements); [N][K]: 32 n-rows x 128 k
-  __shared__ __align__(16) __nv_bfloat16 ws[W_IS_NK ? kQ * kGRow : kGD * (kQ + 8)];
+  // 128 k-rows x this CTA's 32 columns (rows of 40 elements)
+  __shared__ __align__(16) __nv_bfloat16 ws[kGD * (kQ + 8)];
   const int h = blockIdx.y, n0 = blockIdx.z * kQ;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -67,18 +66,11 @@ __global__ void __launch_bounds__(128) gemm_heads_kernel(__nv_bfloat16* __restri
     af[ks][2] = ra < rows ? __ldg(xa + ks * 8 + 4 + t) : 0u;
     af[ks][3] = rb < rows ? __ldg(xb + ks * 8 + 4 + t) : 0u;
   }
-  if (W_IS_NK) {   // rows n0 .. n0+31 of W[n][k], 16 chunks each
-    for (int i = tid; i < kQ * 16; i += 128) {
-      const int r = i >> 4, c = i & 15;
-      *reinterpret_cast<uint4*>(ws + r * kGRow + c * 8) =
-          __ldg(reinterpret_cast<const uint4*>(wh + (int64_t)(n0 + r) * kGD) + c);
-    }
-  } else {         // columns n0 .. n0+31 of every row of W[k][n], 4 chunks each
-    for (int i = tid; i < kGD * 4; i += 128) {
-      const int r = i >> 2, c = i & 3;
-      *reinterpret_cast<uint4*>(ws + r * (kQ + 8) + c * 8) =
-          __ldg(reinterpret_cast<const uint4*>(wh + (int64_t)r * kGD + n0) + c);
-    }
+  // columns n0 .. n0+31 of every row of W[k][n], 4 chunks each
+  for (int i = tid; i < kGD * 4; i += 128) {
+    const int r = i >> 2, c = i & 3;
+    *reinterpret_cast<uint4*>(ws + r * (kQ + 8) + c * 8) =
+        __ldg(reinterpret_cast<const uint4*>(wh + (int64_t)r * kGD + n0) + c);
   }
   __syncthreads();
   if (r0 >= rows) return;
@@ -92,15 +84,9 @@ __global__ void __launch_bounds__(128) gemm_heads_kernel(__nv_bfloat16* __restri
 #pragma unroll
     for (int np = 0; np < 2; ++np) {      // pairs of 8-column n-tiles within the 32
       uint32_t b[4];
-      if (W_IS_NK) {
-        const int n = np * 16 + ((mi >> 1) << 3) + rr;
-        const int k = ks * 16 + ((mi & 1) << 3);
-        ldsm4(wbase + (uint32_t)(n * kGRow + k) * 2, b);
-      } else {
-        const int k = ks * 16 + ((mi & 1) << 3) + rr;
-        const int n = np * 16 + ((mi >> 1) << 3);
-        ldsm4_t(wbase + (uint32_t)(k * (kQ + 8) + n) * 2, b);
-      }
+      const int k = ks * 16 + ((mi & 1) << 3) + rr;
+      const int n = np * 16 + ((mi >> 1) << 3);
+      ldsm4_t(wbase + (uint32_t)(k * (kQ + 8) + n) * 2, b);
       mma16816g(acc[2 * np], af[ks][0], af[ks][1], af[ks][2], af[ks][3], b[0], b[1]);
       mma16816g(acc[2 * np + 1], af[ks][0], af[ks][1], af[ks][2], af[ks][3], b[2], b[3]);
     }
@@ -295,17 +281,12 @@ cudaError_t launch_merge_project(const DecodeArgs& a, const void* w_v, void* out
 }
 
 cudaError_t launch_gemm_heads(void* y, const void* x, const void* w, int rows, int heads,
-                              bool w_is_nk, cudaStream_t stream) {
+                              cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
   const dim3 grid((rows + 63) / 64, heads, kGD / 32);
-  if (w_is_nk)
-    gemm_heads_kernel<true><<<grid, 128, 0, stream>>>(
-        static_cast<__nv_bfloat16*>(y), static_cast<const __nv_bfloat16*>(x),
-        static_cast<const __nv_bfloat16*>(w), rows, heads);
-  else
-    gemm_heads_kernel<false><<<grid, 128, 0, stream>>>(
-        static_cast<__nv_bfloat16*>(y), static_cast<const __nv_bfloat16*>(x),
-        static_cast<const __nv_bfloat16*>(w), rows, heads);
+  gemm_heads_kernel<<<grid, 128, 0, stream>>>(static_cast<__nv_bfloat16*>(y),
+                                              static_cast<const __nv_bfloat16*>(x),
+                                              static_cast<const __nv_bfloat16*>(w), rows, heads);
   return cudaGetLastError();
 }
 

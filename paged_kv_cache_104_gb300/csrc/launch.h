@@ -86,6 +86,9 @@ struct DecodeArgs {
   // (sequence, KV head) left for the merge; 0: 512-token splits, the merge
   // derives their count from seq_lens.
   int balanced;
+  // 1: the kernel keeps every sequence's length in shared memory after its
+  // unit prefix sums (set by a launcher that sized shared memory for it)
+  int lens_in_smem;
 };
 // True if (dtype, head_dim, group) has a compiled decode kernel.
 bool decode_supported(int is_bf16, int head_dim, int group);
@@ -110,11 +113,11 @@ cudaError_t launch_paged_decode_fp8(const DecodeArgs& a, int num_sms, cudaStream
 // and waits for it only before reading a.q.
 cudaError_t launch_decode_mla(const DecodeArgs& a, const void* w_v, void* out, int num_sms,
                               cudaStream_t stream);
-// y[r][h] = x[r][h] . W[h] (W[h] 128 x 128 bf16, stored [K][N], or [N][K]
-// when w_is_nk), bf16 in and out.  Each CTA signals at its start that a
-// programmatic dependent launch may begin.
+// y[r][h] = x[r][h] . W[h] (W[h] 128 x 128 bf16, stored [K][N]), bf16 in and
+// out.  Each CTA signals at its start that a programmatic dependent launch
+// may begin.
 cudaError_t launch_gemm_heads(void* y, const void* x, const void* w, int rows, int heads,
-                              bool w_is_nk, cudaStream_t stream);
+                              cudaStream_t stream);
 // The latent attention's merge of split partials fused with the output
 // up-projection o_h = W_V[h] z_h (launched as the attention's programmatic
 // dependent).
