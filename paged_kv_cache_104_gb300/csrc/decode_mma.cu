@@ -166,13 +166,15 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
   }
   // balanced walk over 64-token stages when the batch gives every CTA at
   // least kMinStagesPerCta of them; otherwise 512-token splits
-  plan_units(a, cu, a.balanced ? kStageTok : 0);
+  // the sequence lengths after the prefix sums, when the launcher made room
+  int* lens = a.lens_in_smem ? cu + a.num_seqs + 1 : nullptr;
+  plan_units(a, cu, a.balanced ? kStageTok : 0, 0, lens);
   __syncthreads();
   const bool balanced =
       a.balanced && (int64_t)cu[a.num_seqs] >= (int64_t)kMinStagesPerCta * gridDim.x;
   if (a.balanced && !balanced) {
     __syncthreads();
-    plan_units(a, cu);
+    plan_units(a, cu, 0, 0, lens);
     __syncthreads();
   }
   volatile int* vabort = abort_flag;
@@ -193,7 +195,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
     const uint64_t policy = policy_evict_first();
     uint32_t issued = 0;
     bool ok = true;
-    Walk wk = walk_begin(a, cu, balanced);
+    Walk wk = walk_begin(a, cu, balanced, lens);
     Unit u;
     while (ok && walk_next(a, cu, kStageTok, wk, u)) {
       const int blk0 = u.tok_begin / kBlockSize;
@@ -265,7 +267,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
   const int vhalf = g >> 2;
   uint32_t consumed = 0;
 
-  Walk wk = walk_begin(a, cu, balanced);
+  Walk wk = walk_begin(a, cu, balanced, lens);
   Unit u;
   while (walk_next(a, cu, kStageTok, wk, u)) {
     const int hq0 = u.g * G;
@@ -544,7 +546,14 @@ cudaError_t launch_g(const DecodeArgs& args, int num_sms, cudaStream_t stream, b
   const int64_t rows = a.num_blocks * a.num_kv_heads * kBlockSize;
   if (!encode_pool_map_bf16(&tm_k, a.k_cache, rows) || !encode_pool_map_bf16(&tm_v, a.v_cache, rows))
     return cudaErrorInvalidValue;
-  const size_t smem = C::OFF_CU + sizeof(int) * (size_t)(a.num_seqs + 1) + 1024;
+  size_t smem = C::OFF_CU + sizeof(int) * (size_t)(a.num_seqs + 1) + 1024;
+  // the sequence lengths go to shared memory too unless that costs a CTA per SM
+  {
+    const size_t with = smem + sizeof(int) * (size_t)a.num_seqs;
+    a.lens_in_smem = with <= 227 * 1024 &&
+                     (228 * 1024) / (with + 1024) >= (228 * 1024) / (smem + 1024);
+    if (a.lens_in_smem) smem = with;
+  }
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
   cudaError_t e = allow_dynamic_smem(decode_mma_kernel<G, FUSE>, (int)smem);
   if (e != cudaSuccess) return e;
