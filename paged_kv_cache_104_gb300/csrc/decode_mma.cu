@@ -528,6 +528,10 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
     }
     named_bar_sync(1, kConsumersM);
   }
+  // This CTA's work is done: the split merge launched next (a programmatic
+  // dependent that waits for this grid to complete before it reads) may be
+  // scheduled as SMs free up, instead of after the last CTA has exited.
+  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // Launched as the programmatic dependent of a persistent prefill on the
   // other SMs, this grid finishes only after that one, so the launches that
   // follow in the stream see both.  Without such a launch it returns at once.
