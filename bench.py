@@ -292,6 +292,47 @@ def run_reference(args, w, lay, acct):
 
 
 # --------------------------------------------------------------------------- our arm
+def graphs_of(step, L, nev, dev, stream):
+    """Capture the step twice: a clean CUDA graph for the timed region, and one
+    with event-record nodes around each layer's calls (nev per layer), replayed
+    only after the timed region for the per-call breakdown.  Event nodes inside
+    a graph break the kernel-to-kernel edges between layers and add a few
+    microseconds per node, so the timed graph holds none.  Returns (clean,
+    instrumented or None, its events)."""
+    try:
+        gev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(nev)]
+               for _ in range(L)]
+    except TypeError:
+        gev = None
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    graphs = []
+    for ev in (None, gev) if gev is not None else (None,):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                step(ev, s=cap)
+        graphs.append(g)
+    stream.wait_stream(cap)
+    for g in graphs:
+        g.replay()
+    torch.cuda.synchronize(dev)
+    return graphs[0], (graphs[1] if len(graphs) > 1 else None), gev
+
+
+def breakdown_events(g_ev, gev, step, L, nev, dev):
+    """Replay the instrumented graph once (or run one eager step when this
+    torch has no graph event nodes) and return its per-layer events."""
+    if g_ev is not None:
+        g_ev.replay()
+        torch.cuda.synchronize(dev)
+        return gev
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(L)]
+    step(ev)
+    torch.cuda.synchronize(dev)
+    return ev
+
+
 def run_fp8_decode(args, w, lay, inputs, dev, stream, dist, n):
     """Time the decode path over an fp8 (E4M3, per-KV-head scales) cache:
     per layer kv_append_fp8 of the decode tokens, then decode attention
@@ -338,20 +379,7 @@ def run_fp8_decode(args, w, lay, inputs, dev, stream, dist, n):
         step()
     torch.cuda.synchronize(dev)
     assert B.get_device_error() == 0, "device error word set during the fp8 warm-up"
-    try:
-        gev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
-               for _ in range(L)]
-    except TypeError:
-        gev = None
-    graph = torch.cuda.CUDAGraph()
-    cap = torch.cuda.Stream(dev)
-    cap.wait_stream(stream)
-    with torch.cuda.stream(cap):
-        with torch.cuda.graph(graph, stream=cap):
-            step(gev, s=cap)
-    stream.wait_stream(cap)
-    graph.replay()
-    torch.cuda.synchronize(dev)
+    graph, g_ev, gev = graphs_of(step, L, 2, dev, stream)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist)
     torch.cuda.synchronize(dev)
@@ -363,27 +391,33 @@ def run_fp8_decode(args, w, lay, inputs, dev, stream, dist, n):
     barrier(dist)
     ms_step = max_over_ranks(dist, t0.elapsed_time(t1)) / args.steps
     assert B.get_device_error() == 0, "device error word set during the fp8 steps"
-    if gev is None:
-        gev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(L)]
-        step(gev)
-        torch.cuda.synchronize(dev)
+    gev = breakdown_events(g_ev, gev, step, L, 2, dev)
     dec_ms = sum(gev[li][0].elapsed_time(gev[li][1]) for li in range(L)) / L
     hbm_peak, _, peak_src = measured_peaks()
-    dec_gbs = dec_bytes / (dec_ms / 1e3) / 1e9
+    # the timed step is L x (append + decode call) and nothing else: one
+    # layer's time is the step's time over L
+    layer_ms = ms_step / L
+    leg_gbs = (dec_bytes + app_bytes) / (layer_ms / 1e3) / 1e9
     return {
         "what": "decode path over an fp8 E4M3 cache with per-KV-head scales: kv_append_fp8 of "
                 "the decode tokens + decode attention (main + reduce), all layers, one CUDA graph",
         "ms_per_step": ms_step,
         "value": n * L * (dec_bytes + app_bytes) / (ms_step / 1e3) / 1e9, "unit": "GB/s",
         "decode_tokens_per_s": n * nd / (ms_step / 1e3),
-        "decode_ms_per_layer": dec_ms,
+        "layer_ms": layer_ms,
+        "decode_ms_per_layer_events": dec_ms,
         "distinct_layer_pools": n_pools, "pool_gb_per_layer": pool_bytes / 1e9,
         "gpu_launches": args.steps * L * (2 + (1 if msl > 512 else 0)),
         "roofline": {
-            "kernel": "paged_decode_attention_fp8 (split-K main + reduce)", "bound": "hbm",
-            "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": dec_gbs / hbm_peak,
+            "kernel": "kv_append_fp8 + paged_decode_attention_fp8 (split-K main + reduce), one "
+                      "layer", "bound": "hbm",
+            "achieved": leg_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": leg_gbs / hbm_peak,
             "traffic": profiled_traffic("decode_fp8_kernel", "decode_fp8.cu"),
-            "algorithmic_bytes_per_launch": dec_bytes,
+            "algorithmic_bytes_per_launch": dec_bytes + app_bytes,
+            "timing": "one layer's append + decode call = the timed step over L (CUDA events "
+                      "around the replays of a graph with no other work); "
+                      "decode_ms_per_layer_events brackets the decode call alone in a separately "
+                      "replayed graph with event nodes",
             "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
             else "fallback 6.8 TB/s",
         },
@@ -432,20 +466,7 @@ def run_decode_config(args, name, dev, stream, dist, n):
         step()
     torch.cuda.synchronize(dev)
     assert B.get_device_error() == 0, f"device error word set during the {name} warm-up"
-    try:
-        gev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
-               for _ in range(L)]
-    except TypeError:
-        gev = None
-    graph = torch.cuda.CUDAGraph()
-    cap = torch.cuda.Stream(dev)
-    cap.wait_stream(stream)
-    with torch.cuda.stream(cap):
-        with torch.cuda.graph(graph, stream=cap):
-            step(gev, s=cap)
-    stream.wait_stream(cap)
-    graph.replay()
-    torch.cuda.synchronize(dev)
+    graph, g_ev, gev = graphs_of(step, L, 2, dev, stream)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist)
     torch.cuda.synchronize(dev)
@@ -457,12 +478,12 @@ def run_decode_config(args, name, dev, stream, dist, n):
     barrier(dist)
     ms_step = max_over_ranks(dist, t0.elapsed_time(t1)) / args.steps
     assert B.get_device_error() == 0, f"device error word set during the {name} steps"
-    if gev is None:
-        gev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(L)]
-        step(gev)
-        torch.cuda.synchronize(dev)
-    dec_ms = sum(gev[li][0].elapsed_time(gev[li][1]) for li in range(L)) / L
+    gev = breakdown_events(g_ev, gev, step, L, 2, dev)
+    ev_ms = sum(gev[li][0].elapsed_time(gev[li][1]) for li in range(L)) / L
     hbm_peak, _, peak_src = measured_peaks()
+    # the timed step is L decode calls and nothing else: one call's average
+    # duration is the step's time over L
+    dec_ms = ms_step / L
     dec_gbs = acct["decode_bytes_layer"] / (dec_ms / 1e3) / 1e9
     return {
         "what": w.description + "; per layer the fused append + paged decode (main + reduce), "
@@ -471,6 +492,10 @@ def run_decode_config(args, name, dev, stream, dist, n):
         "value": n * acct["bytes_step"] / (ms_step / 1e3) / 1e9, "unit": "GB/s",
         "decode_tokens_per_s": n * nd / (ms_step / 1e3),
         "decode_ms_per_layer": dec_ms,
+        "decode_ms_per_layer_events": ev_ms,
+        "timing": "decode_ms_per_layer = the timed step over L (the step is L decode calls, one "
+                  "CUDA graph with no other nodes); decode_ms_per_layer_events brackets each call "
+                  "in a separately replayed graph with event nodes",
         "cached_tokens": int(lay.seq_lens.sum()),
         "distinct_layer_pools": n_pools, "pool_gb_per_layer": pool_bytes / 1e9,
         "gpu_launches": args.steps * L * (2 if msl > 512 else 1),
@@ -608,20 +633,7 @@ def run_mla_decode(args, w, lay, dev, stream, dist, n):
         step()
     torch.cuda.synchronize(dev)
     assert B.get_device_error() == 0, "device error word set during the latent warm-up"
-    try:
-        gev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
-               for _ in range(L)]
-    except TypeError:
-        gev = None
-    graph = torch.cuda.CUDAGraph()
-    cap = torch.cuda.Stream(dev)
-    cap.wait_stream(stream)
-    with torch.cuda.stream(cap):
-        with torch.cuda.graph(graph, stream=cap):
-            step(gev, s=cap)
-    stream.wait_stream(cap)
-    graph.replay()
-    torch.cuda.synchronize(dev)
+    graph, g_ev, gev = graphs_of(step, L, 2, dev, stream)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist)
     torch.cuda.synchronize(dev)
@@ -633,13 +645,12 @@ def run_mla_decode(args, w, lay, dev, stream, dist, n):
     barrier(dist)
     ms_step = max_over_ranks(dist, t0.elapsed_time(t1)) / args.steps
     assert B.get_device_error() == 0, "device error word set during the latent steps"
-    if gev is None:
-        gev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(L)]
-        step(gev)
-        torch.cuda.synchronize(dev)
+    gev = breakdown_events(g_ev, gev, step, L, 2, dev)
     dec_ms = sum(gev[li][0].elapsed_time(gev[li][1]) for li in range(L)) / L
     hbm_peak, _, peak_src = measured_peaks()
-    dec_gbs = dec_bytes / (dec_ms / 1e3) / 1e9
+    # the timed step is L x (latent append + decode call) and nothing else
+    layer_ms = ms_step / L
+    leg_gbs = (dec_bytes + app_bytes) / (layer_ms / 1e3) / 1e9
     return {
         "what": "decode over a latent (MLA-style) cache, rank 128, 32 query heads with per-head "
                 "up-projections: latent_append of the decode tokens + decode call (absorb, "
@@ -647,15 +658,21 @@ def run_mla_decode(args, w, lay, dev, stream, dist, n):
         "ms_per_step": ms_step,
         "value": n * L * (dec_bytes + app_bytes) / (ms_step / 1e3) / 1e9, "unit": "GB/s",
         "decode_tokens_per_s": n * nd / (ms_step / 1e3),
-        "decode_ms_per_layer": dec_ms,
+        "layer_ms": layer_ms,
+        "decode_ms_per_layer_events": dec_ms,
         "distinct_layer_pools": n_pools, "pool_gb_per_layer": pool_bytes / 1e9,
         # per layer: latent_append, query absorption, attention, merge + up-projection
         "gpu_launches": args.steps * L * 4,
         "roofline": {
-            "kernel": "mla_decode_attention (query absorption + tcgen05 attention over the "
-                      "latents + fused merge and up-projection)", "bound": "hbm",
-            "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": dec_gbs / hbm_peak,
-            "traffic": None, "algorithmic_bytes_per_launch": dec_bytes,
+            "kernel": "latent_append + mla_decode_attention (query absorption + tcgen05 attention "
+                      "over the latents + fused merge and up-projection), one layer",
+            "bound": "hbm",
+            "achieved": leg_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": leg_gbs / hbm_peak,
+            "traffic": None, "algorithmic_bytes_per_launch": dec_bytes + app_bytes,
+            "timing": "one layer's append + decode call = the timed step over L (CUDA events "
+                      "around the replays of a graph with no other work); "
+                      "decode_ms_per_layer_events brackets the decode call alone in a separately "
+                      "replayed graph with event nodes",
             "traffic_note": "the call is three launches; ncu traffic is recorded for the "
                             "attention kernel alone (profiles/traffic.json, decode_mla_kernel)",
             "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
@@ -724,15 +741,16 @@ def run_ours(args, w, lay, acct):
             x = inputs[li]
             kc, vc = pools[li % n_pools]
             if side and not serial:
-                # the chunk's tokens by kv_append; then the decode (appending
-                # its tokens) and the prefill side by side
-                B.kv_append(k_new_pre[li], v_new_pre[li], kc, vc, slot_pre, stream=s)
+                # one call: it appends the chunk's tokens, then runs the decode
+                # (appending its tokens) and the prefill side by side
                 if ev is not None:
                     ev[li][0].record(s)
                 B.decode_prefill_attention(out_dec[li], x.q_decode, k_new_dec[li], v_new_dec[li],
                                            kc, vc, bt_dec, seq_lens, max_seq, out_pre[li],
                                            x.q_prefill, bt_pre, w.prefill_prior, w.scale, wsp,
-                                           prefill_sms=split["prefill_sms"], stream=s)
+                                           prefill_sms=split["prefill_sms"], stream=s,
+                                           chunk_k_new=k_new_pre[li], chunk_v_new=v_new_pre[li],
+                                           chunk_slots=slot_pre)
                 if ev is not None:
                     ev[li][1].record(s)
                     ev[li][2].record(s)
@@ -794,23 +812,11 @@ def run_ours(args, w, lay, acct):
     assert B.get_device_error() == 0, "device error word set during warm-up"
     graph = None
     if args.graph:
-        # one CUDA graph per step (all layers); the per-kernel events are
-        # captured into it as well
-        # timing events inside a graph must be external event-record nodes
-        try:
-            graph_events = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)]
-                            for _ in range(L)]
-        except TypeError:
-            graph_events = None
-        graph = torch.cuda.CUDAGraph()
-        cap = torch.cuda.Stream(dev)
-        cap.wait_stream(stream)
-        with torch.cuda.stream(cap):
-            with torch.cuda.graph(graph, stream=cap):
-                step(graph_events, s=cap)
-        stream.wait_stream(cap)
-        for _ in range(2):
-            graph.replay()
+        # one CUDA graph per step (all layers), with no event nodes; the
+        # per-call breakdown comes from a second, instrumented graph replayed
+        # after the timed region
+        graph, g_ev, graph_events = graphs_of(step, L, 3, dev, stream)
+        graph.replay()
         torch.cuda.synchronize(dev)
 
     evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(L)]
@@ -832,14 +838,10 @@ def run_ours(args, w, lay, acct):
     total_ms = max_over_ranks(dist, total_ms)
     assert B.get_device_error() == 0, "device error word set during the timed steps"
     if graph is not None:
-        if graph_events is not None:   # the last replay's event nodes
-            evs = [graph_events]
-        else:
-            # no external events in this torch: the per-kernel breakdown
-            # comes from one eager step right after the timed region
-            evs = [evs[0]]
-            step(evs[0])
-            torch.cuda.synchronize(dev)
+        # the per-call breakdown: one replay of the instrumented graph (or,
+        # without graph event nodes in this torch, one eager step)
+        evs = [breakdown_events(g_ev, graph_events, step, L, 3, dev)]
+        assert B.get_device_error() == 0, "device error word set during the breakdown replay"
     nsteps_ev = len(evs)
     dec_ms = [evs[k][li][0].elapsed_time(evs[k][li][1]) for k in range(nsteps_ev) for li in range(L)]
     pre_ms = ([evs[k][li][1].elapsed_time(evs[k][li][2]) for k in range(nsteps_ev)
@@ -861,8 +863,15 @@ def run_ours(args, w, lay, acct):
     n = ws
     value = n * acct["bytes_step"] / (ms_step / 1e3) / 1e9
     hbm_peak, bf16_peak, peak_src = measured_peaks()
-    dec_avg = sum(dec_ms) / len(dec_ms)
-    dec_gbs = acct["decode_bytes_layer"] / (dec_avg / 1e3) / 1e9
+    dec_avg = sum(dec_ms) / len(dec_ms)   # event brackets (the breakdown)
+    if side and graph is not None:
+        # the timed graph is L side-by-side calls (each appends the chunk's
+        # keys and values, then runs the pair) and nothing else: a layer's
+        # time is the step's over L
+        roof_ms = ms_step / L
+    else:
+        roof_ms = dec_avg
+    dec_gbs = acct["decode_bytes_layer"] / (roof_ms / 1e3) / 1e9
     traffic = profiled_traffic("decode_mma_kernel", "decode_mma.cu")
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": n, "steps": args.steps,
@@ -884,7 +893,8 @@ def run_ours(args, w, lay, acct):
         "prefill_tflops": (acct["prefill_flops_layer"] / (sum(pre_ms) / len(pre_ms) / 1e3) / 1e12
                            if pre_ms else None),
         "prefill_ms_per_layer": sum(pre_ms) / len(pre_ms) if pre_ms else None,
-        "decode_ms_per_layer": dec_avg,
+        "decode_ms_per_layer": roof_ms,
+        "decode_ms_per_layer_events": dec_avg,
         "roofline": {
             "kernel": "paged_decode_attention (split-K main + reduce)",
             "bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s",
@@ -916,14 +926,24 @@ def run_ours(args, w, lay, acct):
                     "SMs, the decode as their programmatic dependent on the rest",
             "prefill_sms": split["prefill_sms"], "decode_sms": nsm - split["prefill_sms"],
             "split_trials_ms_per_step": split.get("trials_ms"),
-            "pair_ms_per_layer": dec_avg,
+            "layer_ms": roof_ms,
+            "pair_ms_per_layer_events": dec_avg,
+            # from the previous layer's end event to this layer's start event
+            # (instrumented replay): the gap between calls
+            "between_calls_ms_events": (
+                sum(evs[0][li - 1][2].elapsed_time(evs[0][li][0]) for li in range(1, L)) / (L - 1)
+                if L > 1 else None),
             "decode_ms_per_layer_alone": ser_dec,
             "decode_gbs_alone": acct["decode_bytes_layer"] / (ser_dec / 1e3) / 1e9,
             "prefill_ms_per_layer_alone": line["prefill_ms_per_layer"],
         }
-        line["roofline"]["note"] = ("timed steps: the decode runs side by side with the prefill and "
-                                    "spans the pair, so achieved = its bytes / the pair's event time "
-                                    "(a lower bound on its own rate)")
+        line["roofline"]["note"] = (
+            "the decode runs side by side with the prefill and spans the pair; achieved = the "
+            "decode's bytes / one layer's time, which is the timed step over L (one CUDA graph "
+            "with no event nodes: per layer one side-by-side call, which also appends the chunk's "
+            "keys and values), a lower bound on the decode's own rate" if graph is not None else
+            "the decode runs side by side with the prefill and spans the pair; achieved = the "
+            "decode's bytes / the event time of the pair (a lower bound on its own rate)")
         if line["prefill_roofline"]:
             line["prefill_roofline"]["note"] = ("prefill measured alone, on all SMs, in one serial "
                                                 "step right after the timed region")
@@ -954,11 +974,12 @@ def run_ours(args, w, lay, acct):
         ev_in = [torch.cuda.Event() for _ in range(L)]
         ev_done = [torch.cuda.Event() for _ in range(L)]
 
-        def e2e_step():
+        def e2e_step(s=None):
             # a step's copies start after the previous step's kernels (its
             # input buffers are reused) and after the timer's start event
-            h2d_s.wait_stream(stream)
-            d2h_s.wait_stream(stream)
+            s = stream if s is None else s
+            h2d_s.wait_stream(s)
+            d2h_s.wait_stream(s)
             with torch.cuda.stream(h2d_s):
                 for hsrc, dst in zip(h_meta, d_meta):
                     dst.copy_(hsrc, non_blocking=True)
@@ -968,33 +989,53 @@ def run_ours(args, w, lay, acct):
                         dst.copy_(hsrc, non_blocking=True)
                     ev_in[li].record(h2d_s)
             for li in range(L):
-                stream.wait_event(ev_in[li])
-                layer(li)
-                ev_done[li].record(stream)
+                s.wait_event(ev_in[li])
+                layer(li, s=s)
+                ev_done[li].record(s)
             with torch.cuda.stream(d2h_s):
                 for li in range(L):
                     d2h_s.wait_event(ev_done[li])
                     h_out[li][0].copy_(out_dec[li], non_blocking=True)
                     h_out[li][1].copy_(out_pre[li], non_blocking=True)
-            stream.wait_stream(d2h_s)
-            stream.wait_stream(h2d_s)
+            s.wait_stream(d2h_s)
+            s.wait_stream(h2d_s)
 
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e2e_step()
         torch.cuda.synchronize(dev)
+        e2e_graph = None
+        if graph is not None:
+            # the same step (copies, calls, copies back) captured as one CUDA
+            # graph, as the timed step is: every replay copies the inputs in
+            # from pinned host memory and the outputs back out
+            e2e_graph = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream(dev)
+            cap.wait_stream(stream)
+            with torch.cuda.stream(cap):
+                with torch.cuda.graph(e2e_graph, stream=cap):
+                    e2e_step(cap)
+            stream.wait_stream(cap)
+            e2e_graph.replay()
+            torch.cuda.synchronize(dev)
         barrier(dist)
         e0.record(stream)
         for _ in range(args.e2e_steps):
-            e2e_step()
+            if e2e_graph is not None:
+                e2e_graph.replay()
+            else:
+                e2e_step()
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e_ms = max_over_ranks(dist, e0.elapsed_time(e1)) / args.e2e_steps
         line["e2e"] = {"value": n * acct["bytes_step"] / (e_ms / 1e3) / 1e9, "unit": "GB/s",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "ms_per_step": e_ms, "steps": args.e2e_steps,
-                       "how": "eager launches through the C ABI; per layer, pinned host->device "
-                              "copies of its inputs and device->host copies of its outputs on two "
-                              "copy streams, overlapped with the other layers' kernels"}
+                       "how": ("the C ABI calls and the copies captured as one CUDA graph per step "
+                               "(replayed like the timed step); " if e2e_graph is not None else
+                               "eager launches through the C ABI; ") +
+                              "per layer, pinned host->device copies of its inputs and "
+                              "device->host copies of its outputs on two copy streams, overlapped "
+                              "with the other layers' kernels"}
 
     # ---- fp8 (E4M3) cache variant of the decode path: append + decode + reduce
     if args.fp8_decode and w.head_dim == 128 and w.dtype == torch.bfloat16:
@@ -1058,7 +1099,7 @@ def main():
     ap.add_argument("--layer-pools", type=int, default=0,
                     help="distinct layer pools to allocate (0 = one per layer); the step always "
                          "runs every layer, cycling the pools")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--fused-append", type=int, default=1,
                     help="1: decode tokens are appended inside the decode launch")
     ap.add_argument("--side-by-side", type=int, default=1,

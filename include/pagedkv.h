@@ -227,8 +227,14 @@ pkv_status pkv_chunked_prefill_attention(void *out, const void *q, const void *k
  *   num_seqs/max_blocks_per_seq/max_seq_len/workspace for the decode,
  *   prefill_out/prefill_q/prefill_block_table/prefill_max_blocks/prior_len/
  *   chunk_len for the prefill; pools, head counts, sizes, scale and dtype are
- *   shared).  The chunk's own keys and values must already be in the pools,
- *   and the chunk's sequence must not be one of the decoded sequences.
+ *   shared).  The chunk's sequence must not be one of the decoded sequences.
+ *   chunk_k_new, chunk_v_new  the chunk's own new keys and values
+ *                [chunk_len][num_kv_heads][head_dim] (16-byte aligned), and
+ *   chunk_slot_mapping        their slots (int64 [chunk_len], as for
+ *                pkv_kv_append): the call first appends them (bit-exact, as
+ *                pkv_kv_append would) and the prefill reads them.  All three
+ *                null: the chunk's keys and values must already be in the
+ *                pools.
  *   prefill_sms  SMs given to the prefill (0: a quarter of the GPU).  The
  *                best split makes both halves end together; it depends on
  *                the batch (the decode's cache bytes) and the chunk.
@@ -268,6 +274,9 @@ typedef struct pkv_decode_prefill_args {
   float scale;
   pkv_dtype dtype;
   int prefill_sms;
+  const void *chunk_k_new;
+  const void *chunk_v_new;
+  const int64_t *chunk_slot_mapping;
 } pkv_decode_prefill_args;
 
 pkv_status pkv_decode_prefill_attention(const pkv_decode_prefill_args *args,

@@ -50,7 +50,9 @@ class DecodePrefillArgs(ctypes.Structure):
                 ("v_cache", ctypes.c_void_p), ("num_blocks", ctypes.c_int64),
                 ("num_q_heads", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
                 ("head_dim", ctypes.c_int), ("block_size", ctypes.c_int),
-                ("scale", ctypes.c_float), ("dtype", ctypes.c_int), ("prefill_sms", ctypes.c_int)]
+                ("scale", ctypes.c_float), ("dtype", ctypes.c_int), ("prefill_sms", ctypes.c_int),
+                ("chunk_k_new", ctypes.c_void_p), ("chunk_v_new", ctypes.c_void_p),
+                ("chunk_slot_mapping", ctypes.c_void_p)]
 
 
 class PagedKVError(RuntimeError):
@@ -304,10 +306,13 @@ def chunked_prefill_attention(out, q, k_cache, v_cache, block_table_row, prior_l
 def decode_prefill_attention(dec_out, dec_q, k_new, v_new, k_cache, v_cache, block_table, seq_lens,
                              max_seq_len: int, pre_out, pre_q, pre_block_table_row, prior_len: int,
                              scale: float, workspace=None, prefill_sms: int = 0,
-                             stream=None) -> None:
+                             stream=None, chunk_k_new=None, chunk_v_new=None,
+                             chunk_slots=None) -> None:
     """One layer's decode (as paged_decode_attention_append) and one chunk's
     prefill (as chunked_prefill_attention) side by side on disjoint SMs:
-    prefill_sms SMs for the prefill (0: a quarter of the GPU)."""
+    prefill_sms SMs for the prefill (0: a quarter of the GPU).  With
+    chunk_k_new / chunk_v_new [chunk, Hkv, D] and chunk_slots (int64 [chunk])
+    the call first appends the chunk's own keys and values (as kv_append)."""
     b, hq, d = dec_q.shape
     nb, hkv, bs, _ = k_cache.shape
     a = DecodePrefillArgs()
@@ -324,6 +329,8 @@ def decode_prefill_attention(dec_out, dec_q, k_new, v_new, k_cache, v_cache, blo
     a.k_cache, a.v_cache, a.num_blocks = _ptr(k_cache), _ptr(v_cache), nb
     a.num_q_heads, a.num_kv_heads, a.head_dim, a.block_size = hq, hkv, d, bs
     a.scale, a.dtype, a.prefill_sms = float(scale), _dtype_code(dec_q), int(prefill_sms)
+    a.chunk_k_new, a.chunk_v_new = _ptr(chunk_k_new), _ptr(chunk_v_new)
+    a.chunk_slot_mapping = _ptr(chunk_slots)
     st = load().pkv_decode_prefill_attention(ctypes.byref(a), _stream(stream))
     _check("pkv_decode_prefill_attention", st)
 

@@ -56,7 +56,7 @@ def test_binding_names_match_header(lib):
 
 def test_host_only_functions(lib):
     from paged_kv_cache_104_gb300 import binding
-    assert binding.abi_version() == 1
+    assert binding.abi_version() == 2
     assert binding.status_str(0) == "ok"
     assert binding.status_str(5) == "unsupported shape"
     # one split of 512 tokens needs no workspace; more need (D + 2) floats per

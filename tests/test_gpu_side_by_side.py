@@ -5,7 +5,10 @@ must equal those of the two calls made one after the other (kv_append of the
 chunk, paged_decode_attention_append, chunked_prefill): the prefill and the
 pools bit for bit, the decode bit for bit while both walk 512-token splits and
 to rounding once the batch is large enough for the balanced walk the decode
-takes when it runs alone; and stay within the bf16 tolerance of the oracle."""
+takes when it runs alone; and stay within the bf16 tolerance of the oracle.
+Given the chunk's new keys and values, the call appends them itself (the
+append launched first, the prefill as its programmatic dependent): the same
+results, bit for bit, as kv_append followed by the call."""
 import pytest
 import torch
 
@@ -21,8 +24,9 @@ def _bits(t):
     return t.detach().cpu().view(torch.int16)
 
 
-def _run_both(w, lay, x, prior, prefill_sms, dev="cuda"):
-    """Serial calls, then the side-by-side call on a second copy of the pools;
+def _run_both(w, lay, x, prior, prefill_sms, dev="cuda", chunk_in_call=False):
+    """Serial calls, then the side-by-side call on a second copy of the pools
+    (chunk_in_call: the call appends the chunk's keys and values itself);
     returns (serial decode, serial prefill, side decode, side prefill, pools)."""
     nd = lay.num_decode_tokens
     bt = lay.decode_block_table.to(dev).contiguous()
@@ -38,9 +42,14 @@ def _run_both(w, lay, x, prior, prefill_sms, dev="cuda"):
     pools = []
     for side in (False, True):
         kc, vc = x.k_cache.to(dev), x.v_cache.to(dev)
-        B.kv_append(k_pre, v_pre, kc, vc, slot_pre)
+        if not (side and chunk_in_call):
+            B.kv_append(k_pre, v_pre, kc, vc, slot_pre)
         od, op = torch.empty_like(q_dec), torch.empty_like(q_pre)
-        if side:
+        if side and chunk_in_call:
+            B.decode_prefill_attention(od, q_dec, k_dec, v_dec, kc, vc, bt, sl, msl, op, q_pre, bt_pre,
+                                       prior, w.scale, ws, prefill_sms=prefill_sms,
+                                       chunk_k_new=k_pre, chunk_v_new=v_pre, chunk_slots=slot_pre)
+        elif side:
             B.decode_prefill_attention(od, q_dec, k_dec, v_dec, kc, vc, bt, sl, msl, op, q_pre, bt_pre,
                                        prior, w.scale, ws, prefill_sms=prefill_sms)
         else:
@@ -53,13 +62,14 @@ def _run_both(w, lay, x, prior, prefill_sms, dev="cuda"):
     return outs, pools
 
 
+@pytest.mark.parametrize("chunk_in_call", [False, True])
 @pytest.mark.parametrize("prefill_sms", [8, 40, 100])
-def test_side_by_side_equals_serial_and_oracle(prefill_sms):
+def test_side_by_side_equals_serial_and_oracle(prefill_sms, chunk_in_call):
     w = G.custom_workload(torch.bfloat16, 32, 8, 128, seed=91)
     lens = [1, 17, 300, 512, 513, 1500, 2600, 4097]
     lay = W.make_layout(w, seq_lens_after=lens, prefill=(700, 600))
     x = W.draw_layer(w, lay, 0)
-    (sd, sp, bd, bp), pools = _run_both(w, lay, x, 700, prefill_sms)
+    (sd, sp, bd, bp), pools = _run_both(w, lay, x, 700, prefill_sms, chunk_in_call=chunk_in_call)
     assert torch.equal(_bits(sd), _bits(bd)), "decode differs from the serial calls"
     assert torch.equal(_bits(sp), _bits(bp)), "prefill differs from the serial calls"
     (k1, v1), (k2, v2) = pools
@@ -74,14 +84,15 @@ def test_side_by_side_equals_serial_and_oracle(prefill_sms):
 
 def test_side_by_side_full_size_layer():
     """The ragged 128-sequence batch with its 2,048-token chunk over 4,096
-    cached tokens, 40 SMs for the prefill: the prefill and the pools equal to
-    the serial calls bit for bit; the decode (512-token splits beside the
-    prefill, the balanced walk alone) to within a bf16 rounding step of its
-    values (|o| < 1)."""
+    cached tokens, 40 SMs for the prefill, the chunk appended by the call (as
+    the bench's step runs it): the prefill and the pools equal to the serial
+    calls bit for bit; the decode (512-token splits beside the prefill, the
+    balanced walk alone) to within a bf16 rounding step of its values
+    (|o| < 1)."""
     w = W.WORKLOADS["ragged_prefill"]
     lay = W.make_layout(w)
     x = W.draw_layer(w, lay, 0)
-    (sd, sp, bd, bp), pools = _run_both(w, lay, x, w.prefill_prior, 40)
+    (sd, sp, bd, bp), pools = _run_both(w, lay, x, w.prefill_prior, 40, chunk_in_call=True)
     assert torch.equal(_bits(sp), _bits(bp))
     (k1, v1), (k2, v2) = pools
     assert torch.equal(_bits(k1), _bits(k2)) and torch.equal(_bits(v1), _bits(v2))
@@ -106,8 +117,10 @@ def test_side_by_side_too_many_work_items_runs_serial():
     w = G.custom_workload(torch.bfloat16, 4, 2, 128, seed=94)
     lay = W.make_layout(w, seq_lens_after=[9, 2000], prefill=(0, 257 * 128))
     x = W.draw_layer(w, lay, 0)
-    (sd, sp, bd, bp), _ = _run_both(w, lay, x, 0, 20)
-    assert torch.equal(_bits(sd), _bits(bd)) and torch.equal(_bits(sp), _bits(bp))
+    for chunk_in_call in (False, True):
+        (sd, sp, bd, bp), (p1, p2) = _run_both(w, lay, x, 0, 20, chunk_in_call=chunk_in_call)
+        assert torch.equal(_bits(sd), _bits(bd)) and torch.equal(_bits(sp), _bits(bp))
+        assert torch.equal(_bits(p1[0]), _bits(p2[0])) and torch.equal(_bits(p1[1]), _bits(p2[1]))
 
 
 def test_side_by_side_prefill_sms_at_or_above_the_gpu():
@@ -116,8 +129,10 @@ def test_side_by_side_prefill_sms_at_or_above_the_gpu():
     w = G.custom_workload(torch.bfloat16, 8, 2, 128, seed=93)
     lay = W.make_layout(w, seq_lens_after=[40, 900], prefill=(0, 300))
     x = W.draw_layer(w, lay, 0)
-    (sd, sp, bd, bp), _ = _run_both(w, lay, x, 0, sms)
-    assert torch.equal(_bits(sd), _bits(bd)) and torch.equal(_bits(sp), _bits(bp))
+    for chunk_in_call in (False, True):
+        (sd, sp, bd, bp), (p1, p2) = _run_both(w, lay, x, 0, sms, chunk_in_call=chunk_in_call)
+        assert torch.equal(_bits(sd), _bits(bd)) and torch.equal(_bits(sp), _bits(bp))
+        assert torch.equal(_bits(p1[0]), _bits(p2[0])) and torch.equal(_bits(p1[1]), _bits(p2[1]))
 
 
 def test_side_by_side_rejects_fp32_and_bad_split():
@@ -138,3 +153,19 @@ def test_side_by_side_rejects_fp32_and_bad_split():
     x = W.draw_layer(w, lay, 0)
     with pytest.raises(B.PagedKVError):
         _run_both(w, lay, x, 0, -1)
+
+
+def test_side_by_side_chunk_append_needs_all_three():
+    """chunk_k_new, chunk_v_new and chunk_slots come together or not at all."""
+    w = G.custom_workload(torch.bfloat16, 4, 2, 128)
+    lay = W.make_layout(w, seq_lens_after=[30], prefill=(0, 20))
+    x = W.draw_layer(w, lay, 0, device="cuda")
+    nd = lay.num_decode_tokens
+    bt = lay.decode_block_table.cuda().contiguous()
+    ws = B.decode_workspace(1, 4, 128, 30)
+    with pytest.raises(B.PagedKVError):
+        B.decode_prefill_attention(torch.empty_like(x.q_decode), x.q_decode, x.k_new[:nd],
+                                   x.v_new[:nd], x.k_cache, x.v_cache, bt, lay.seq_lens.cuda(), 30,
+                                   torch.empty_like(x.q_prefill), x.q_prefill,
+                                   lay.block_table[lay.prefill_row].cuda(), 0, w.scale, ws,
+                                   prefill_sms=8, chunk_k_new=x.k_new[nd:])
