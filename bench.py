@@ -585,9 +585,10 @@ def run_flushed_decode(args, name, dev, stream, dist, n):
 
 def run_mla_decode(args, w, lay, dev, stream, dist, n):
     """Time decode over a latent (MLA-style) cache on the decode batch of the
-    workload: per layer latent_append of the decode tokens' latents, then the
-    decode call (query absorption, attention over the latents, split merge,
-    up-projection), every layer with its own pool, as one CUDA graph.
+    workload: per layer one decode call that appends the decode tokens'
+    latents (in the query absorption's launch), then attends over the
+    latents, merges the split partials and up-projects, every layer with its
+    own pool, as one CUDA graph.
     Algorithmic bytes: every stored latent once, the two projections, q read
     and out written, and the append."""
     from paged_kv_cache_104_gb300 import binding as B
@@ -609,7 +610,6 @@ def run_mla_decode(args, w, lay, dev, stream, dist, n):
     pools = [xs[li].pool for li in range(n_pools)]
     for li in range(L):
         xs[li].pool = None
-    slot = llay.slot_mapping[:nd].to(dev)
     bt = llay.decode_block_table.to(dev).contiguous()
     sl = llay.seq_lens.to(dev)
     msl = int(llay.seq_lens.max())
@@ -621,11 +621,11 @@ def run_mla_decode(args, w, lay, dev, stream, dist, n):
         for li in range(L):
             x = xs[li]
             c = pools[li % n_pools]
-            B.latent_append(x.c_new, c, slot, stream=s)
             if ev is not None:
                 ev[li][0].record(s)
+            # one call: the decode tokens' latents appended, then the decode
             B.mla_decode_attention(outs[li], x.q, x.w_k, x.w_v, c, bt, sl, msl, lw.scale, wsp,
-                                   stream=s)
+                                   stream=s, c_new=x.c_new)
             if ev is not None:
                 ev[li][1].record(s)
 
@@ -648,31 +648,31 @@ def run_mla_decode(args, w, lay, dev, stream, dist, n):
     gev = breakdown_events(g_ev, gev, step, L, 2, dev)
     dec_ms = sum(gev[li][0].elapsed_time(gev[li][1]) for li in range(L)) / L
     hbm_peak, _, peak_src = measured_peaks()
-    # the timed step is L x (latent append + decode call) and nothing else
+    # the timed step is L decode calls (each appending its tokens' latents)
     layer_ms = ms_step / L
     leg_gbs = (dec_bytes + app_bytes) / (layer_ms / 1e3) / 1e9
     return {
         "what": "decode over a latent (MLA-style) cache, rank 128, 32 query heads with per-head "
-                "up-projections: latent_append of the decode tokens + decode call (absorb, "
-                "attend over the latents, merge, up-project), all layers, one CUDA graph",
+                "up-projections: per layer one decode call (append the decode tokens' latents "
+                "and absorb the queries, attend over the latents, merge + up-project), all "
+                "layers, one CUDA graph",
         "ms_per_step": ms_step,
         "value": n * L * (dec_bytes + app_bytes) / (ms_step / 1e3) / 1e9, "unit": "GB/s",
         "decode_tokens_per_s": n * nd / (ms_step / 1e3),
         "layer_ms": layer_ms,
         "decode_ms_per_layer_events": dec_ms,
         "distinct_layer_pools": n_pools, "pool_gb_per_layer": pool_bytes / 1e9,
-        # per layer: latent_append, query absorption, attention, merge + up-projection
-        "gpu_launches": args.steps * L * 4,
+        # per layer: append + query absorption, attention, merge + up-projection
+        "gpu_launches": args.steps * L * 3,
         "roofline": {
-            "kernel": "latent_append + mla_decode_attention (query absorption + tcgen05 attention "
-                      "over the latents + fused merge and up-projection), one layer",
+            "kernel": "mla_decode_attention_append (latent append + query absorption, tcgen05 "
+                      "attention over the latents, fused merge and up-projection), one layer",
             "bound": "hbm",
             "achieved": leg_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": leg_gbs / hbm_peak,
             "traffic": None, "algorithmic_bytes_per_launch": dec_bytes + app_bytes,
-            "timing": "one layer's append + decode call = the timed step over L (CUDA events "
-                      "around the replays of a graph with no other work); "
-                      "decode_ms_per_layer_events brackets the decode call alone in a separately "
-                      "replayed graph with event nodes",
+            "timing": "one layer's call = the timed step over L (CUDA events around the replays "
+                      "of a graph with no other work); decode_ms_per_layer_events brackets each "
+                      "call in a separately replayed graph with event nodes",
             "traffic_note": "the call is three launches; ncu traffic is recorded for the "
                             "attention kernel alone (profiles/traffic.json, decode_mla_kernel)",
             "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"

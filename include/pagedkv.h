@@ -349,6 +349,22 @@ pkv_status pkv_mla_decode_attention(void *out, const void *q, const void *w_k, c
                                     int head_dim, int rank, int block_size, float scale,
                                     void *workspace, size_t workspace_bytes, pkv_stream_t stream);
 
+/* As pkv_mla_decode_attention, with each sequence's new latent appended in
+ * the same call: c_new [num_seqs][rank] (bf16, 16-byte aligned) goes to
+ * position seq_lens[b] - 1 of sequence b (its slot read from block_table), a
+ * byte-exact copy, before any latent is read.  The result and the pool equal
+ * those of pkv_latent_append at those slots followed by
+ * pkv_mla_decode_attention.  A length outside [1, max_seq_len] leaves the
+ * pool untouched for that sequence (the decode reports it); a block id
+ * outside the pool is skipped and reported in the device error word. */
+pkv_status pkv_mla_decode_attention_append(void *out, const void *q, const void *c_new,
+                                           const void *w_k, const void *w_v, void *c_cache,
+                                           const int32_t *block_table, const int32_t *seq_lens,
+                                           int num_seqs, int max_blocks_per_seq, int max_seq_len,
+                                           int64_t num_blocks, int num_q_heads, int head_dim,
+                                           int rank, int block_size, float scale, void *workspace,
+                                           size_t workspace_bytes, pkv_stream_t stream);
+
 /* ---------------------------------------------------------------------------
  * Prefix caching (host-only): chained block hashes and a hash -> block index.
  * "The KV cache and prefix caching", section "A prefix already in the cache

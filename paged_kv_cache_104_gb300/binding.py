@@ -29,6 +29,7 @@ EXPORTS = ("pkv_kv_append", "pkv_decode_workspace_bytes", "pkv_paged_decode_atte
            "pkv_get_device_error", "pkv_status_str", "pkv_abi_version",
            "pkv_kv_append_fp8", "pkv_paged_decode_attention_fp8",
            "pkv_latent_append", "pkv_mla_workspace_bytes", "pkv_mla_decode_attention",
+           "pkv_mla_decode_attention_append",
            "pkv_fnv1a64", "pkv_prefix_hash_blocks", "pkv_prefix_cache_create",
            "pkv_prefix_cache_destroy", "pkv_prefix_cache_size", "pkv_prefix_cache_insert",
            "pkv_prefix_cache_evict", "pkv_prefix_cache_match", "pkv_prefix_plan",
@@ -95,6 +96,9 @@ def open_library(path: str):
     lib.pkv_mla_decode_attention.argtypes = [p, p, p, p, p, p, p, i, i, i, i64, i, i, i, i, f,
                                              p, sz, p]
     lib.pkv_mla_decode_attention.restype = ctypes.c_int
+    lib.pkv_mla_decode_attention_append.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i64, i, i, i,
+                                                    i, f, p, sz, p]
+    lib.pkv_mla_decode_attention_append.restype = ctypes.c_int
     u64p = ctypes.POINTER(ctypes.c_uint64)
     i32p = ctypes.POINTER(ctypes.c_int32)
     lib.pkv_fnv1a64.argtypes = [p, sz]
@@ -260,14 +264,22 @@ def mla_workspace(num_seqs: int, num_q_heads: int, rank: int, max_seq_len: int, 
 
 
 def mla_decode_attention(out, q, w_k, w_v, c_cache, block_table, seq_lens, max_seq_len: int,
-                         scale: float, workspace=None, stream=None) -> None:
+                         scale: float, workspace=None, stream=None, c_new=None) -> None:
     """Decode over the latent pool [NB, bs, r]; q/out bf16 [B, Hq, D];
-    w_k, w_v bf16 [Hq, D, r]."""
+    w_k, w_v bf16 [Hq, D, r].  With c_new [B, r] each sequence's new latent is
+    first placed at position seq_lens[b] - 1 (the same call)."""
     b, hq, d = q.shape
     nb, bs, r = c_cache.shape
     if workspace is None:
         workspace = mla_workspace(b, hq, r, max_seq_len, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size()
+    if c_new is not None:
+        st = load().pkv_mla_decode_attention_append(
+            _ptr(out), _ptr(q), _ptr(c_new), _ptr(w_k), _ptr(w_v), _ptr(c_cache),
+            _ptr(block_table), _ptr(seq_lens), b, int(block_table.shape[1]), int(max_seq_len), nb,
+            hq, d, r, bs, float(scale), _ptr(workspace), ws_bytes, _stream(stream))
+        _check("pkv_mla_decode_attention_append", st)
+        return
     st = load().pkv_mla_decode_attention(
         _ptr(out), _ptr(q), _ptr(w_k), _ptr(w_v), _ptr(c_cache), _ptr(block_table),
         _ptr(seq_lens), b, int(block_table.shape[1]), int(max_seq_len), nb, hq, d, r, bs,

@@ -6,6 +6,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "host_cache.h"
@@ -486,12 +487,18 @@ size_t pkv_mla_workspace_bytes(int num_seqs, int num_q_heads, int rank, int max_
   return 2 * vec + pkv_decode_workspace_bytes(num_seqs, num_q_heads, rank, max_seq_len);
 }
 
-pkv_status pkv_mla_decode_attention(void* out, const void* q, const void* w_k, const void* w_v,
-                                    const void* c_cache, const int32_t* block_table,
-                                    const int32_t* seq_lens, int num_seqs, int max_blocks_per_seq,
-                                    int max_seq_len, int64_t num_blocks, int num_q_heads,
-                                    int head_dim, int rank, int block_size, float scale,
-                                    void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The latent decode call; c_new (optional): each sequence's new latent,
+// appended by the query absorption's launch.
+pkv_status mla_decode(void* out, const void* q, const void* c_new, const void* w_k,
+                      const void* w_v, void* c_cache, const int32_t* block_table,
+                      const int32_t* seq_lens, int num_seqs, int max_blocks_per_seq,
+                      int max_seq_len, int64_t num_blocks, int num_q_heads, int head_dim, int rank,
+                      int block_size, float scale, void* workspace, size_t workspace_bytes,
+                      pkv_stream_t stream) {
   if (num_q_heads < 1 || head_dim < 1 || rank < 1 || block_size < 1) return PKV_EINVAL;
   if (block_size != pkv::kBlockSize || num_q_heads != 32 || head_dim != 128 || rank != 128)
     return PKV_EUNSUPPORTED;
@@ -521,8 +528,14 @@ pkv_status pkv_mla_decode_attention(void* out, const void* q, const void* w_k, c
   void* q_lat = ws;          // absorbed queries [B][Hq][rank] bf16
   void* z = ws + vec;        // attention over the latent [B][Hq][rank] bf16
   char* part = ws + 2 * vec;
-  // 1) q~_h = W_K[h]^T q_h
-  if (pkv::launch_gemm_heads(q_lat, q, w_k, num_seqs, num_q_heads, s) != cudaSuccess)
+  // 1) q~_h = W_K[h]^T q_h (and, given c_new, each sequence's new latent
+  //    placed at position seq_lens[b] - 1)
+  const pkv::LatentAppend app{c_new, c_cache, block_table, seq_lens, max_blocks_per_seq,
+                              (int)std::min<int64_t>(max_seq_len,
+                                                     (int64_t)max_blocks_per_seq * block_size),
+                              num_blocks, err};
+  if (pkv::launch_gemm_heads(q_lat, q, w_k, num_seqs, num_q_heads, s, c_new ? &app : nullptr) !=
+      cudaSuccess)
     return PKV_ECUDA;
   // 2) z_h = softmax(scale q~_h . C^T) C over the latent pool
   const int splits = partial_slots_for(max_seq_len);
@@ -554,6 +567,34 @@ pkv_status pkv_mla_decode_attention(void* out, const void* q, const void* w_k, c
   // 3) merge of the partials fused with o_h = W_V[h] z_h
   if (pkv::launch_decode_mla(a, w_v, out, sms, s) != cudaSuccess) return PKV_ECUDA;
   return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_mla_decode_attention(void* out, const void* q, const void* w_k, const void* w_v,
+                                    const void* c_cache, const int32_t* block_table,
+                                    const int32_t* seq_lens, int num_seqs, int max_blocks_per_seq,
+                                    int max_seq_len, int64_t num_blocks, int num_q_heads,
+                                    int head_dim, int rank, int block_size, float scale,
+                                    void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+  return mla_decode(out, q, nullptr, w_k, w_v, const_cast<void*>(c_cache), block_table, seq_lens,
+                    num_seqs, max_blocks_per_seq, max_seq_len, num_blocks, num_q_heads, head_dim,
+                    rank, block_size, scale, workspace, workspace_bytes, stream);
+}
+
+pkv_status pkv_mla_decode_attention_append(void* out, const void* q, const void* c_new,
+                                           const void* w_k, const void* w_v, void* c_cache,
+                                           const int32_t* block_table, const int32_t* seq_lens,
+                                           int num_seqs, int max_blocks_per_seq, int max_seq_len,
+                                           int64_t num_blocks, int num_q_heads, int head_dim,
+                                           int rank, int block_size, float scale, void* workspace,
+                                           size_t workspace_bytes, pkv_stream_t stream) {
+  if (num_seqs > 0 && (!c_new || !aligned16(c_new))) return PKV_EINVAL;
+  return mla_decode(out, q, c_new, w_k, w_v, c_cache, block_table, seq_lens, num_seqs,
+                    max_blocks_per_seq, max_seq_len, num_blocks, num_q_heads, head_dim, rank,
+                    block_size, scale, workspace, workspace_bytes, stream);
 }
 
 pkv_status pkv_chunked_prefill_attention(void* out, const void* q, const void* k_cache,

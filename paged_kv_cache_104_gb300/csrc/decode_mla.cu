@@ -43,7 +43,7 @@
 //              unit.  Rows of keys past a sequence's end are zeroed in the
 //              tile, so stale pool bytes (even NaN) never meet p = 0 in P V.
 //   warp 4     TMA producer: the unit's q~ (32 rows) into a two-buffer ring,
-//              the latent blocks of each tile into a four-tile ring.
+//              the latent blocks of each tile into a five-tile ring.
 //   warp 5     TMEM allocator and issuer of the score products S^T (converged
 //              warp, one elected lane per instruction), as soon as a tile's
 //              latents are in: the scores of the next tiles are computed
@@ -54,7 +54,7 @@
 // shares of all sequences' stages, cut where sequences change) when the
 // batch gives every CTA at least 512 tokens, else 512-token splits; a piece
 // that covers its whole sequence writes z, the others write (m, l, O)
-// partials that the reduce kernel merges.  O^T is double-buffered across
+// partials that the merge + up-projection kernel launched next combines.  O^T is double-buffered across
 // pieces, so a piece's epilogue overlaps the next piece's products.
 // Every wait is bounded; on time-out the kernel records an error, stops
 // issuing work, lets its copies and products finish, frees its TMEM and
@@ -348,11 +348,15 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c,
       ok = __shfl_sync(kAllT, (int)ok, 0) != 0;
       ++di;
     };
-    // q~ comes from the kernel before this one in the stream: launched as its
+    // q~ comes from the kernel before this one in the stream (launched as its
     // programmatic dependent, this grid may start before that one has
-    // finished.  The latents do not depend on it, so the first piece's first
-    // tiles are requested before waiting for it; its q~ right after.
-    bool first_piece = true;
+    // finished), and so may the latent of each sequence's new token (the
+    // query absorption can append it).  Nothing is requested before that
+    // grid is done: latent tiles requested earlier also competed in HBM with
+    // its loads and delayed it (measured: 53.6 -> 51.7 us per layer on the
+    // ragged batch, 26.7 -> 26.0 us on the 2,301-token batch).
+    if (lane == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+    __syncwarp();
     while (ok && have) {
       publish(u, false);
       if (!ok) break;
@@ -360,15 +364,9 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c,
       const int next_ids = have_next ? load_ids(nu, 0) : 0;
       const int nblk = (u.tok_end - 1) / kBlockSize - u.tok_begin / kBlockSize + 1;
       const int ntile = tiles_of(u);
-      const int q_after = first_piece ? min(ntile, kNS) : 0;   // tiles issued before its q~
-      if (q_after == 0) load_q(u);
+      load_q(u);
       if (!ok) break;
       for (int i = 0; i < ntile; ++i, ++t) {
-        if (i == q_after && q_after > 0) {
-          if (lane == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
-          load_q(u);
-          if (!ok) break;
-        }
         if (i > 0 && (i * kBlkPerTile) % 32 == 0) ids = load_ids(u, i * kBlkPerTile);
         const int slot = t % kNS;
         if (lane == 0 && t >= (uint32_t)kNS)
@@ -387,11 +385,6 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c,
         if (lane < nb)
           tma4d(sbase + OFF_RING + slot * kTileBytes + lane * kBlockBytes, &tm_c, fb, 2 * blk, policy);
       }
-      if (ok && q_after == ntile) {   // a first piece of at most kNS tiles
-        if (lane == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
-        load_q(u);
-      }
-      first_piece = false;
       u = nu;
       have = have_next;
       ids = next_ids;

@@ -5,6 +5,8 @@
 //   * The merge of the latent attention's split partials fused with the
 //     output up-projection o_h = W_V[h] z_h (W_V[h] stored [D][r] = [N][K]);
 //     see merge_project_kernel.
+// The absorption's launch can also place each decode sequence's new latent
+// in the pool (the CTAs of head 0 and the first column quarter).
 // Absorption: one CTA of 4 warps covers one head, 64 rows and a quarter (32 columns) of
 // the output, so that a decode batch of 64-128 rows still spreads over 256-512
 // CTAs.  The CTA's 32 columns of W[h] are staged in shared memory with rows
@@ -42,15 +44,37 @@ __device__ __forceinline__ void ldsm4_t(uint32_t addr, uint32_t (&r)[4]) {
 __global__ void __launch_bounds__(128) gemm_heads_kernel(__nv_bfloat16* __restrict__ y,
                                                          const __nv_bfloat16* __restrict__ x,
                                                          const __nv_bfloat16* __restrict__ wts,
-                                                         int rows, int heads) {
+                                                         int rows, int heads,
+                                                         const LatentAppend app) {
   // a kernel launched next as a programmatic dependent (the latent
-  // attention) may start now; it waits for this grid before reading y
+  // attention) may start now; it waits for this grid before reading y or
+  // the pool
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int kQ = 32;                 // output columns per CTA
   // 128 k-rows x this CTA's 32 columns (rows of 40 elements)
   __shared__ __align__(16) __nv_bfloat16 ws[kGD * (kQ + 8)];
   const int h = blockIdx.y, n0 = blockIdx.z * kQ;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (app.c_new && blockIdx.y == 0 && blockIdx.z == 0) {
+    // the new latents of this CTA's 64 rows: 16-byte chunks, 16 per row, to
+    // position seq_lens[r] - 1 (a bit-exact copy; bad lengths or block ids
+    // are skipped, and block ids reported)
+    for (int i = tid; i < 64 * 16; i += 128) {
+      const int r = blockIdx.x * 64 + (i >> 4), c = i & 15;
+      if (r >= rows) break;
+      const int n = __ldg(app.seq_lens + r);
+      if (n < 1 || n > app.max_len) continue;
+      const int blk = __ldg(app.block_table + (int64_t)r * app.bt_stride + (n - 1) / kBlockSize);
+      if (blk < 0 || (int64_t)blk >= app.num_blocks) {
+        record_error(app.err, DEVERR_BLOCK_RANGE);
+        continue;
+      }
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(
+                          static_cast<const __nv_bfloat16*>(app.c_new) + (int64_t)r * kGD) + c);
+      reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(app.c_cache) +
+                               ((int64_t)blk * kBlockSize + (n - 1) % kBlockSize) * kGD)[c] = v;
+    }
+  }
   const int g = lane >> 2, t = lane & 3;
   const __nv_bfloat16* wh = wts + (int64_t)h * kGD * kGD;
   // this warp's 16 rows of x first: their loads overlap the staging of W
@@ -281,12 +305,14 @@ cudaError_t launch_merge_project(const DecodeArgs& a, const void* w_v, void* out
 }
 
 cudaError_t launch_gemm_heads(void* y, const void* x, const void* w, int rows, int heads,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, const LatentAppend* app) {
   if (rows <= 0) return cudaSuccess;
   const dim3 grid((rows + 63) / 64, heads, kGD / 32);
+  const LatentAppend none{};
   gemm_heads_kernel<<<grid, 128, 0, stream>>>(static_cast<__nv_bfloat16*>(y),
                                               static_cast<const __nv_bfloat16*>(x),
-                                              static_cast<const __nv_bfloat16*>(w), rows, heads);
+                                              static_cast<const __nv_bfloat16*>(w), rows, heads,
+                                              app ? *app : none);
   return cudaGetLastError();
 }
 

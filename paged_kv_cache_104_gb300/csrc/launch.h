@@ -110,14 +110,28 @@ cudaError_t launch_paged_decode_fp8(const DecodeArgs& a, int num_sms, cudaStream
 // piece (the others leave partials); then the merge + up-projection writes
 // o = W_V z into `out`.  The attention is launched as the programmatic
 // dependent of the kernel before it in the stream (the query absorption),
-// and waits for it only before reading a.q.
+// and waits for it before reading a.q or any latent.
 cudaError_t launch_decode_mla(const DecodeArgs& a, const void* w_v, void* out, int num_sms,
                               cudaStream_t stream);
+// The latent of each decode sequence's new token, placed by the query
+// absorption's launch at position seq_lens[r] - 1 of row r's block table
+// (rank 128, bf16, pool [num_blocks][16][128]).
+struct LatentAppend {
+  const void* c_new;        // [rows][128]
+  void* c_cache;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int bt_stride;
+  int max_len;              // lengths outside [1, max_len] are skipped
+  int64_t num_blocks;
+  int* err;
+};
 // y[r][h] = x[r][h] . W[h] (W[h] 128 x 128 bf16, stored [K][N]), bf16 in and
-// out.  Each CTA signals at its start that a programmatic dependent launch
-// may begin.
+// out; with app set, the same launch also appends each row's new latent.
+// Each CTA signals at its start that a programmatic dependent launch may
+// begin.
 cudaError_t launch_gemm_heads(void* y, const void* x, const void* w, int rows, int heads,
-                              cudaStream_t stream);
+                              cudaStream_t stream, const LatentAppend* app = nullptr);
 // The latent attention's merge of split partials fused with the output
 // up-projection o_h = W_V[h] z_h (launched as the attention's programmatic
 // dependent).

@@ -1,7 +1,9 @@
 """Latent (MLA-style) cache on the GPU against the oracle.
 
-latent_append must be byte-exact against ``oracle.mla.latent_append``.
-Decode over the latent pool (absorbed projections, attention over the
+latent_append must be byte-exact against ``oracle.mla.latent_append``, and
+the decode call that appends each sequence's new latent itself must leave the
+same pool and give the same result, bit for bit, as latent_append followed by
+the decode call.  Decode over the latent pool (absorbed projections, attention over the
 latents, up-projection) is compared with ``oracle.mla.mla_decode``, which
 reconstructs every head's keys and values from the latents in fp64, at the
 bf16 tolerance 2e-2."""
@@ -111,3 +113,58 @@ def test_mla_rejects_unsupported_shape_and_small_workspace():
     with pytest.raises(B.PagedKVError) as e:
         B.mla_decode_attention(out, x.q, x.w_k, x.w_v, x.pool, bt, sl, 700, w.scale, small)
     assert e.value.status == 3          # workspace too small
+
+
+@pytest.mark.parametrize("lens", [
+    [1, 2, 15, 16, 17, 33, 63, 64, 65, 127, 128, 129, 511, 512, 513, 1024, 1025, 1600],
+    "random80"])
+def test_mla_append_in_call_equals_append_then_decode(lens):
+    """pkv_mla_decode_attention_append == pkv_latent_append at the new
+    tokens' slots + pkv_mla_decode_attention: pools and outputs bit for bit
+    (NaN in every unused pool row), and the output within the tolerance of
+    the oracle."""
+    w = _workload(seed=13)
+    if lens == "random80":
+        g = torch.Generator().manual_seed(6)
+        lens = torch.randint(1, 2501, (80,), generator=g).tolist()
+    lay = W.make_layout(w, seq_lens_after=lens, prefill=(0, 0))
+    x = W.draw_latent(w, lay)
+    sep, rp = _run(w, lay, x, poison=True)
+    pool = x.pool.clone()
+    pool[~G.used_slot_mask(lay, 16)] = float("nan")
+    gp = pool.cuda()
+    q = x.q.cuda()
+    out = torch.empty_like(q)
+    B.mla_decode_attention(out, q, x.w_k.cuda(), x.w_v.cuda(), gp, lay.decode_block_table.cuda().contiguous(),
+                           lay.seq_lens.cuda(), int(lay.seq_lens.max()), w.scale,
+                           c_new=x.c_new.cuda())
+    torch.cuda.synchronize()
+    assert B.get_device_error() == 0
+    assert torch.equal(G.cpu(gp).view(torch.int16), rp.view(torch.int16))
+    assert torch.equal(G.cpu(out).view(torch.int16), sep.view(torch.int16))
+    ref = M.mla_decode(G.cpu(x.q), G.cpu(x.w_k), G.cpu(x.w_v), rp, lay.decode_block_table,
+                       lay.seq_lens, w.scale)
+    assert G.max_err(G.cpu(out), ref) <= TOL
+
+
+def test_mla_append_in_call_bad_block_id_is_reported():
+    """A block-table entry outside the pool at a sequence's last position:
+    the append skips it, the decode reads a valid block instead, and the error
+    word reports DEVERR_BLOCK_RANGE (2); no fault, the pool outside that row
+    untouched."""
+    w = _workload(seed=14)
+    lay = W.make_layout(w, seq_lens_after=[40, 300], prefill=(0, 0))
+    x = W.draw_latent(w, lay, device="cuda")
+    bt = lay.decode_block_table.clone().contiguous()
+    bt[1, (300 - 1) // 16] = lay.num_blocks + 7
+    before = x.pool.clone()
+    out = torch.empty_like(x.q)
+    B.mla_decode_attention(out, x.q, x.w_k, x.w_v, x.pool, bt.cuda(), lay.seq_lens.cuda(), 300,
+                           w.scale, c_new=x.c_new)
+    assert B.get_device_error() & 2
+    # sequence 0's new latent landed; nothing else changed
+    slot0 = int(lay.slot_mapping[0])
+    changed = (x.pool.view(torch.int16) != before.view(torch.int16)).any(dim=-1).nonzero()
+    assert [tuple(t) for t in changed.tolist()] in ([], [(slot0 // 16, slot0 % 16)])
+    assert torch.equal(x.pool[slot0 // 16, slot0 % 16].view(torch.int16),
+                       x.c_new[0].view(torch.int16))
