@@ -1027,9 +1027,20 @@ def run_ours(args, w, lay, acct):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e_ms = max_over_ranks(dist, e0.elapsed_time(e1)) / args.e2e_steps
+        # the same steps with eager launches (reported beside the graph's)
+        eager_ms = None
+        if e2e_graph is not None:
+            barrier(dist)
+            e0.record(stream)
+            for _ in range(args.e2e_steps):
+                e2e_step()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            eager_ms = max_over_ranks(dist, e0.elapsed_time(e1)) / args.e2e_steps
         line["e2e"] = {"value": n * acct["bytes_step"] / (e_ms / 1e3) / 1e9, "unit": "GB/s",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "ms_per_step": e_ms, "steps": args.e2e_steps,
+                       "eager_ms_per_step": eager_ms,
                        "how": ("the C ABI calls and the copies captured as one CUDA graph per step "
                                "(replayed like the timed step); " if e2e_graph is not None else
                                "eager launches through the C ABI; ") +

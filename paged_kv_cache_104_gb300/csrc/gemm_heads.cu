@@ -6,7 +6,7 @@
 //     output up-projection o_h = W_V[h] z_h (W_V[h] stored [D][r] = [N][K]);
 //     see merge_project_kernel.
 // The absorption's launch can also place each decode sequence's new latent
-// in the pool (the CTAs of head 0 and the first column quarter).
+// in the pool (the CTAs of the first column quarter, a few rows each).
 // Absorption: one CTA of 4 warps covers one head, 64 rows and a quarter (32 columns) of
 // the output, so that a decode batch of 64-128 rows still spreads over 256-512
 // CTAs.  The CTA's 32 columns of W[h] are staged in shared memory with rows
@@ -55,13 +55,19 @@ __global__ void __launch_bounds__(128) gemm_heads_kernel(__nv_bfloat16* __restri
   __shared__ __align__(16) __nv_bfloat16 ws[kGD * (kQ + 8)];
   const int h = blockIdx.y, n0 = blockIdx.z * kQ;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (app.c_new && blockIdx.y == 0 && blockIdx.z == 0) {
-    // the new latents of this CTA's 64 rows: 16-byte chunks, 16 per row, to
-    // position seq_lens[r] - 1 (a bit-exact copy; bad lengths or block ids
-    // are skipped, and block ids reported)
-    for (int i = tid; i < 64 * 16; i += 128) {
-      const int r = blockIdx.x * 64 + (i >> 4), c = i & 15;
-      if (r >= rows) break;
+  if (app.c_new && blockIdx.z == 0) {
+    // the new latents of this CTA's 64-row block, spread over its heads'
+    // CTAs (2 rows each for 32 heads): one 16-byte chunk per thread, copied
+    // to position seq_lens[r] - 1 (bit-exact; bad lengths or block ids are
+    // skipped, and block ids reported).  The chunk is requested first, so
+    // it arrives while the length and the block id are looked up.
+    const int per = (64 + heads - 1) / heads;
+    const int row_end = min(rows, blockIdx.x * 64 + 64);
+    for (int i = tid; i < per * 16; i += 128) {
+      const int r = blockIdx.x * 64 + blockIdx.y * per + (i >> 4), c = i & 15;
+      if (r >= row_end) break;
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(
+                          static_cast<const __nv_bfloat16*>(app.c_new) + (int64_t)r * kGD) + c);
       const int n = __ldg(app.seq_lens + r);
       if (n < 1 || n > app.max_len) continue;
       const int blk = __ldg(app.block_table + (int64_t)r * app.bt_stride + (n - 1) / kBlockSize);
@@ -69,8 +75,6 @@ __global__ void __launch_bounds__(128) gemm_heads_kernel(__nv_bfloat16* __restri
         record_error(app.err, DEVERR_BLOCK_RANGE);
         continue;
       }
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-                          static_cast<const __nv_bfloat16*>(app.c_new) + (int64_t)r * kGD) + c);
       reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(app.c_cache) +
                                ((int64_t)blk * kBlockSize + (n - 1) % kBlockSize) * kGD)[c] = v;
     }
