@@ -859,6 +859,25 @@ def run_ours(args, w, lay, acct):
         assert B.get_device_error() == 0, "device error word set during the serial step"
         ser_dec_ms = [ev_ser[li][0].elapsed_time(ev_ser[li][1]) for li in range(L)]
         pre_ms = [ev_ser[li][1].elapsed_time(ev_ser[li][2]) for li in range(L)]
+        # each half's span inside the pair: one eager step with the kernels'
+        # %globaltimer records (earliest CTA start, latest CTA end per grid)
+        spans = torch.tensor([[-1, 0, -1, 0]] * L, dtype=torch.int64, device=dev)
+        for li in range(L):
+            B.set_span_buffer(spans[li])
+            layer(li)
+        B.set_span_buffer(None)
+        torch.cuda.synchronize(dev)
+        assert B.get_device_error() == 0, "device error word set during the span step"
+        sp = spans.cpu().tolist()
+        in_pair = {
+            "prefill_ms": statistics.median((r[1] - r[0]) / 1e6 for r in sp),
+            "decode_main_ms": statistics.median((r[3] - r[2]) / 1e6 for r in sp),
+            "decode_start_after_prefill_start_us": statistics.median((r[2] - r[0]) / 1e3 for r in sp),
+            "prefill_end_before_decode_end_us": statistics.median((r[3] - r[1]) / 1e3 for r in sp),
+            "how": "medians over the layers of one eager step after the timed region; each "
+                   "kernel records its CTAs' earliest start and latest end (%globaltimer, "
+                   "pkv_set_span_buffer); the decode's split merge runs after both",
+        }
     ms_step = total_ms / args.steps
     n = ws
     value = n * acct["bytes_step"] / (ms_step / 1e3) / 1e9
@@ -936,6 +955,7 @@ def run_ours(args, w, lay, acct):
             "decode_ms_per_layer_alone": ser_dec,
             "decode_gbs_alone": acct["decode_bytes_layer"] / (ser_dec / 1e3) / 1e9,
             "prefill_ms_per_layer_alone": line["prefill_ms_per_layer"],
+            "in_pair": in_pair,
         }
         line["roofline"]["note"] = (
             "the decode runs side by side with the prefill and spans the pair; achieved = the "

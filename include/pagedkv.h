@@ -438,6 +438,19 @@ pkv_status pkv_get_device_error(int *code, int clear);
  */
 pkv_status pkv_l2_flush(const void *buf, size_t bytes, int *sink, pkv_stream_t stream);
 
+/*
+ * set_span_buffer -- a measurement aid for pkv_decode_prefill_attention,
+ * whose two halves overlap in time on one stream, so that events around the
+ * call see only the pair.  With buf set (device memory, 8-byte aligned, four
+ * uint64 the caller initialises to {UINT64_MAX, 0, UINT64_MAX, 0}), later
+ * side-by-side calls record, with atomic min / max, the earliest CTA start
+ * and the latest CTA end of the prefill (buf[0], buf[1]) and of the decode's
+ * main kernel (buf[2], buf[3]), in %globaltimer nanoseconds.  NULL turns it
+ * off (the default).  A process-wide setting, not thread-safe; PKV_EINVAL on
+ * a misaligned pointer.  Host-only.
+ */
+pkv_status pkv_set_span_buffer(unsigned long long *buf);
+
 /* Static description of a status code.  Host-only. */
 const char *pkv_status_str(pkv_status status);
 

@@ -33,7 +33,7 @@ EXPORTS = ("pkv_kv_append", "pkv_decode_workspace_bytes", "pkv_paged_decode_atte
            "pkv_fnv1a64", "pkv_prefix_hash_blocks", "pkv_prefix_cache_create",
            "pkv_prefix_cache_destroy", "pkv_prefix_cache_size", "pkv_prefix_cache_insert",
            "pkv_prefix_cache_evict", "pkv_prefix_cache_match", "pkv_prefix_plan",
-           "pkv_l2_flush")
+           "pkv_l2_flush", "pkv_set_span_buffer")
 NOALLOC_SCRATCH_BYTES = 32 << 20  # PKV_NOALLOC_SCRATCH_BYTES
 
 
@@ -82,6 +82,8 @@ def open_library(path: str):
     lib.pkv_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_int), i]
     lib.pkv_l2_flush.argtypes = [p, sz, p, p]
     lib.pkv_l2_flush.restype = ctypes.c_int
+    lib.pkv_set_span_buffer.argtypes = [p]
+    lib.pkv_set_span_buffer.restype = ctypes.c_int
     lib.pkv_status_str.argtypes = [i]
     lib.pkv_status_str.restype = ctypes.c_char_p
     lib.pkv_kv_append_fp8.argtypes = [p, p, p, p, p, p, p, i64, i64, i, i, i, p]
@@ -176,6 +178,12 @@ def l2_flush(buf, sink, stream=None) -> None:
     st = load().pkv_l2_flush(_ptr(buf), buf.numel() * buf.element_size(), _ptr(sink),
                              _stream(stream))
     _check("pkv_l2_flush", st)
+
+
+def set_span_buffer(buf=None) -> None:
+    """Record the side-by-side call's half spans into buf (int64 [4] on the
+    device, initialised by the caller); None turns it off."""
+    _check("pkv_set_span_buffer", load().pkv_set_span_buffer(_ptr(buf)))
 
 
 def kv_append(k_new, v_new, k_cache, v_cache, slot_mapping, stream=None) -> None:

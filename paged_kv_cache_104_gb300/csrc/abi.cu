@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "host_cache.h"
@@ -110,6 +111,21 @@ pkv_status check_heads(int num_q_heads, int num_kv_heads, int head_dim, int bloc
 extern "C" {
 
 int pkv_abi_version(void) { return 2; }
+
+}  // extern "C"
+
+namespace {
+// the span record of later side-by-side calls (pkv_set_span_buffer)
+std::atomic<unsigned long long*> g_span_buf{nullptr};
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_set_span_buffer(unsigned long long* buf) {
+  if (reinterpret_cast<uintptr_t>(buf) & 7u) return PKV_EINVAL;
+  g_span_buf.store(buf);
+  return PKV_OK;
+}
 
 const char* pkv_status_str(pkv_status s) {
   switch (s) {
@@ -659,6 +675,10 @@ pkv_status pkv_decode_prefill_attention(const pkv_decode_prefill_args* x, pkv_st
   pkv::PrefillArgs pa{x->prefill_out, x->prefill_q, x->k_cache, x->v_cache, x->prefill_block_table,
                       x->prefill_max_blocks, x->prior_len, x->chunk_len, x->num_blocks,
                       x->num_q_heads, x->num_kv_heads, x->scale, err};
+  if (unsigned long long* span = g_span_buf.load()) {
+    pa.span = span;
+    d.span = span + 2;
+  }
   const bool side_by_side = x->chunk_len > 0 && d.num_seqs > 0 && x->head_dim == 128 &&
                             x->dtype == PKV_BF16 && p_sms < sms &&
                             pkv::prefill_pair_persistent_ok(pa, p_sms);

@@ -158,6 +158,18 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
 __device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
+// A measurement aid: the earliest start and the latest end of a grid's CTAs,
+// in %globaltimer nanoseconds, into span[0] (atomic min) and span[1]
+// (atomic max).  Called by one thread of a CTA; span null: nothing.
+__device__ __forceinline__ void span_mark(unsigned long long* span, bool end) {
+  if (span) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (end) atomicMax(span + 1, t);
+    else atomicMin(span, t);
+  }
+}
+
 // fp8 (E4M3) conversions, hardware rounding: f32 -> e4m3 rounds to nearest
 // even and saturates finite values at +-448; e4m3 -> f16 is exact.
 // Element order follows memory order: `lo` is the byte / half at the lower address.

@@ -157,6 +157,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kNST);
 
   if (tid == 0) {
+    span_mark(a.span, false);
     for (int i = 0; i < kNST; ++i) {
       mbar_init(full0 + 8 * i, 1);
       mbar_init(empty0 + 8 * i, kCW);
@@ -531,6 +532,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
   // This CTA's work is done: the split merge launched next (a programmatic
   // dependent that waits for this grid to complete before it reads) may be
   // scheduled as SMs free up, instead of after the last CTA has exited.
+  if (tid == 0) span_mark(a.span, true);
   if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // Launched as the programmatic dependent of a persistent prefill on the
   // other SMs, this grid finishes only after that one, so the launches that

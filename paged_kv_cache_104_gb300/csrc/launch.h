@@ -89,6 +89,9 @@ struct DecodeArgs {
   // 1: the kernel keeps every sequence's length in shared memory after its
   // unit prefix sums (set by a launcher that sized shared memory for it)
   int lens_in_smem;
+  // optional span record (the bf16 decode's main kernel): {earliest CTA
+  // start, latest CTA end} in %globaltimer ns, by atomic min / max
+  unsigned long long* span;
 };
 // True if (dtype, head_dim, group) has a compiled decode kernel.
 bool decode_supported(int is_bf16, int head_dim, int group);
@@ -154,6 +157,8 @@ struct PrefillArgs {
   int num_kv_heads;
   float scale;
   int* err;
+  // optional span record, as DecodeArgs::span (the tcgen05 prefill)
+  unsigned long long* span = nullptr;
 };
 // tcgen05 path (bf16, head_dim 128, block_size 16): two streams of 128 query
 // rows per CTA sharing each K/V tile -- two query heads of one KV head when

@@ -219,6 +219,7 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
   };
 
   if (tid == 0) {
+    span_mark(a.span, false);
     mbar_init(bar(PB_Q), 1);
     for (int s = 0; s < NSK; ++s) {
       mbar_init(bar(PB_KF + s), kProdThreads);
@@ -579,6 +580,7 @@ prefill_pair_kernel(const __grid_constant__ PairParams p, const __grid_constant_
     tc_fence_before();
   }
   __syncthreads();
+  if (tid == 0) span_mark(a.span, true);
   if (warp == W_MMA) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),

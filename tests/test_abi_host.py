@@ -132,3 +132,12 @@ def test_prefill_rejects_bad_arguments_on_host(lib):
     assert call(dt=3) == 2
     assert call(bt=_nullp()) == 1
     assert call(d=96) == 5
+
+
+def test_span_buffer_setter_on_host(lib):
+    """pkv_set_span_buffer takes an 8-byte aligned pointer or NULL; it only
+    stores it (no CUDA call), so this runs without a GPU."""
+    import ctypes
+    assert lib.pkv_set_span_buffer(ctypes.c_void_p(0x1003)) == 1
+    assert lib.pkv_set_span_buffer(ctypes.c_void_p(0x1000)) == 0
+    assert lib.pkv_set_span_buffer(None) == 0

@@ -169,3 +169,28 @@ def test_side_by_side_chunk_append_needs_all_three():
                                    torch.empty_like(x.q_prefill), x.q_prefill,
                                    lay.block_table[lay.prefill_row].cuda(), 0, w.scale, ws,
                                    prefill_sms=8, chunk_k_new=x.k_new[nd:])
+
+
+def test_side_by_side_span_record():
+    """pkv_set_span_buffer: the side-by-side call records each half's
+    earliest CTA start and latest CTA end (ordered, the decode starting after
+    the prefill it depends on), with the results unchanged bit for bit; None
+    turns the record off again."""
+    w = G.custom_workload(torch.bfloat16, 32, 8, 128, seed=95)
+    lay = W.make_layout(w, seq_lens_after=[40, 900, 3000], prefill=(300, 400))
+    x = W.draw_layer(w, lay, 0)
+    (sd, sp, bd, bp), _ = _run_both(w, lay, x, 300, 40, chunk_in_call=True)
+    span = torch.tensor([-1, 0, -1, 0], dtype=torch.int64, device="cuda")
+    B.set_span_buffer(span)
+    try:
+        (sd2, sp2, bd2, bp2), _ = _run_both(w, lay, x, 300, 40, chunk_in_call=True)
+    finally:
+        B.set_span_buffer(None)
+    assert torch.equal(_bits(bd), _bits(bd2)) and torch.equal(_bits(bp), _bits(bp2))
+    p0, p1, d0, d1 = span.cpu().tolist()
+    assert 0 < p0 < p1 and 0 < d0 < d1, (p0, p1, d0, d1)
+    assert d0 >= p0
+    # off again: a further call leaves the record as it was
+    before = span.clone()
+    _run_both(w, lay, x, 300, 40, chunk_in_call=True)
+    assert torch.equal(span, before)
