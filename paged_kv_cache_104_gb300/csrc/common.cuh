@@ -7,6 +7,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -138,6 +139,12 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
 // fp32 store carrying an L2 eviction-priority hint.
 __device__ __forceinline__ void st_global_hint(float* dst, float v, uint64_t policy) {
   asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(dst), "f"(v), "l"(policy)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_global_hint_f16(__half* dst, __half v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.b16 [%0], %1, %2;" ::"l"(dst),
+               "h"(__half_as_ushort(v)), "l"(policy)
                : "memory");
 }
 

@@ -380,6 +380,53 @@ decode_reduce_kernel(const DecodeArgs a) {
   const float inv = 1.f / L;
   T* outp = static_cast<T*>(a.out) + (int64_t)warp_global * D;
   if constexpr (D == 128) {
+    if (a.partials_f16) {
+      // partials stored as O / l in fp16: lane = 4 columns (8 bytes of the
+      // 256-byte row); split s weighs 2^(m_s - M) l_s
+      const uint2* acc2 =
+          reinterpret_cast<const uint2*>(reinterpret_cast<const __half*>(a.ws_acc) + base * D) + lane;
+      // lanes 0 and 16 drop the row's two 128-byte lines once read
+      const bool drop = a.keep_partials && (reinterpret_cast<uintptr_t>(a.ws_acc) & 127u) == 0 &&
+                        (lane & 15) == 0;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s0 = 0; s0 < ns; s0 += 32) {
+        float wl = 0.f;
+        if (s0 + lane < ns) {
+          const float ms = a.ws_ml[(base + s0 + lane) * 2];
+          wl = ms == -INFINITY ? 0.f : exp2f(ms - M) * a.ws_ml[(base + s0 + lane) * 2 + 1];
+        }
+        const int cnt = min(32, ns - s0);
+        for (int k = 0; k < cnt; k += 8) {
+          const int c8 = min(8, cnt - k);
+          uint2 v[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (i < c8) v[i] = acc2[(int64_t)(s0 + k + i) * (D / 4)];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (i < c8) {
+              const float wgt = __shfl_sync(kFull, wl, k + i);
+              const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&v[i].x));
+              const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&v[i].y));
+              o.x = fmaf(wgt, lo.x, o.x);
+              o.y = fmaf(wgt, lo.y, o.y);
+              o.z = fmaf(wgt, hi.x, o.z);
+              o.w = fmaf(wgt, hi.y, o.w);
+            }
+          }
+          // every lane's read of these rows has returned (the FMAs used them)
+          __syncwarp();
+          if (drop) {
+            for (int i = 0; i < c8; ++i) discard_l2_line(acc2 + (int64_t)(s0 + k + i) * (D / 4));
+          }
+        }
+      }
+      Elem<T>::store(outp + lane * 4 + 0, o.x * inv);
+      Elem<T>::store(outp + lane * 4 + 1, o.y * inv);
+      Elem<T>::store(outp + lane * 4 + 2, o.z * inv);
+      Elem<T>::store(outp + lane * 4 + 3, o.w * inv);
+      return;
+    }
     // lane = 4-column group; split weights are computed once per lane (32
     // splits at a time) and broadcast, and 8 partial rows are loaded before
     // their FMAs so the L2 latency of the walk over splits overlaps

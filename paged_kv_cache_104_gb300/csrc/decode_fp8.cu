@@ -474,7 +474,7 @@ decode_fp8_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
         if (direct)
           outp[row * kHD + d] = __float2bfloat16_rn(O * rl);
         else
-          a.ws_acc[pidx * kHD + d] = O * vscale;
+          reinterpret_cast<__half*>(a.ws_acc)[pidx * kHD + d] = __float2half_rn(O * rl);
       }
       if (!direct && lane == 0) {
         a.ws_ml[pidx * 2 + 0] = M;
@@ -490,6 +490,7 @@ cudaError_t launch_fp8_g(const DecodeArgs& args, int num_sms, cudaStream_t strea
   using C = F8Cfg<G>;
   DecodeArgs a = args;
   a.balanced = a.ws_np != nullptr && stage_plan_fits(a, kStageTok);
+  a.partials_f16 = 1;
   CUtensorMap tm_k, tm_v;
   const int64_t rows = a.num_blocks * a.num_kv_heads * kBlockSize;
   if (!encode_pool_map_u8(&tm_k, a.k_cache, rows) || !encode_pool_map_u8(&tm_v, a.v_cache, rows))

@@ -519,8 +519,9 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
         for (int k = 0; k < kCW; ++k) O = fmaf(wk[k], comb[(k * G + h) * kCombRowM + d], O);
         if (direct)
           outp[row * kHD + d] = __float2bfloat16_rn(O * rl);
-        else
-          st_global_hint(a.ws_acc + pidx * kHD + d, O, keep);
+        else   // O / l in fp16: half the bytes of the partial's trip through memory
+          st_global_hint_f16(reinterpret_cast<__half*>(a.ws_acc) + pidx * kHD + d,
+                             __float2half_rn(O * rl), keep);
       }
       if (!direct && lane == 0) {
         a.ws_ml[pidx * 2 + 0] = M;
@@ -545,6 +546,7 @@ cudaError_t launch_g(const DecodeArgs& args, int num_sms, cudaStream_t stream, b
   using C = MCfg<G>;
   DecodeArgs a = args;
   a.keep_partials = dependent ? 0 : 1;
+  a.partials_f16 = 1;
   // the balanced walk when the decode has the GPU to itself; beside a
   // prefill the 512-token splits measured faster
   a.balanced = a.ws_np != nullptr && !dependent && stage_plan_fits(a, kStageTok);

@@ -89,6 +89,10 @@ struct DecodeArgs {
   // 1: the kernel keeps every sequence's length in shared memory after its
   // unit prefix sums (set by a launcher that sized shared memory for it)
   int lens_in_smem;
+  // 1: a split partial is stored as O / l in fp16 (head_dim 128: 256 B a
+  // row, half the bytes of fp32 O) beside its fp32 (m, l); set by the bf16
+  // and fp8 tensor-core decodes, whose outputs are bf16.  0: fp32 O.
+  int partials_f16;
   // optional span record (the bf16 decode's main kernel): {earliest CTA
   // start, latest CTA end} in %globaltimer ns, by atomic min / max
   unsigned long long* span;
