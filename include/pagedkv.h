@@ -96,9 +96,11 @@ pkv_status pkv_kv_append(const void *k_new, const void *v_new, void *k_cache, vo
 /*
  * Bytes of device workspace paged_decode_attention needs for these sizes
  * (0 when no sequence can need more than one split, max_seq_len <= 512).
- * Otherwise: fp32 partials of ceil(max_seq_len / 512) + 1 slots per
- * (sequence, query head) row, each head_dim values plus a (max, sum) pair,
- * and one int per row for the partial count.  Host-only, no GPU use.  The
+ * Otherwise: room for fp32 partials of ceil(max_seq_len / 512) + 1 slots
+ * per (sequence, query head) row, each head_dim values plus a (max, sum)
+ * pair, and one int per row for the partial count (the bf16 and fp8
+ * tensor-core decodes store their partials as fp16 in half of that room).
+ * Host-only, no GPU use.  The
  * workspace holds no state between calls: every value a call reads there it
  * wrote earlier in the same call, so it needs no clearing.
  */
