@@ -848,11 +848,12 @@ def run_ours(args, w, lay, acct):
                for li in range(L)] if w.prefill_chunk else [])
     ser_dec_ms = None
     if side:
-        # in the timed steps the decode and the prefill of a layer overlap:
-        # the events bracket the pair, which the decode spans, so the decode's
-        # rate over the timed region is its bytes over the pair's time.  The
-        # prefill's own time (and the decode's alone) comes from one serial
-        # step (decode, then prefill, each on the whole GPU) right after.
+        # in the timed steps the decode and the prefill of a layer overlap,
+        # and the decode spans the pair, so the decode's rate over the timed
+        # region is its bytes over a layer's time.  Each half's time alone
+        # comes from one serial step (decode, then prefill, each on the whole
+        # GPU) right after, and each half's span inside the pair from one
+        # more step with the span record.
         ev_ser = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(L)]
         step(ev_ser, serial=True)
         torch.cuda.synchronize(dev)
