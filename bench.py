@@ -669,12 +669,14 @@ def run_mla_decode(args, w, lay, dev, stream, dist, n):
                       "attention over the latents, fused merge and up-projection), one layer",
             "bound": "hbm",
             "achieved": leg_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": leg_gbs / hbm_peak,
-            "traffic": None, "algorithmic_bytes_per_launch": dec_bytes + app_bytes,
+            "traffic": profiled_traffic("decode_mla_kernel", "decode_mla.cu"),
+            "algorithmic_bytes_per_launch": dec_bytes + app_bytes,
             "timing": "one layer's call = the timed step over L (CUDA events around the replays "
                       "of a graph with no other work); decode_ms_per_layer_events brackets each "
                       "call in a separately replayed graph with event nodes",
-            "traffic_note": "the call is three launches; ncu traffic is recorded for the "
-                            "attention kernel alone (profiles/traffic.json, decode_mla_kernel)",
+            "traffic_note": "the call is three launches; traffic is the DRAM bytes of its "
+                            "attention launch alone, captured at this size (the absorption and "
+                            "the merge read W_K, W_V, q and the partials: a few MB more)",
             "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
             else "fallback 6.8 TB/s",
         },
