@@ -94,11 +94,20 @@ __global__ void __launch_bounds__(128) gemm_heads_kernel(__nv_bfloat16* __restri
     af[ks][2] = ra < rows ? __ldg(xa + ks * 8 + 4 + t) : 0u;
     af[ks][3] = rb < rows ? __ldg(xb + ks * 8 + 4 + t) : 0u;
   }
-  // columns n0 .. n0+31 of every row of W[k][n], 4 chunks each
-  for (int i = tid; i < kGD * 4; i += 128) {
-    const int r = i >> 2, c = i & 3;
-    *reinterpret_cast<uint4*>(ws + r * (kQ + 8) + c * 8) =
-        __ldg(reinterpret_cast<const uint4*>(wh + (int64_t)r * kGD + n0) + c);
+  // columns n0 .. n0+31 of every row of W[k][n], 4 chunks each (a thread's
+  // four pieces requested before any is stored)
+  {
+    uint4 wv[kGD * 4 / 128];
+#pragma unroll
+    for (int j = 0; j < kGD * 4 / 128; ++j) {
+      const int i = tid + j * 128, r = i >> 2, c = i & 3;
+      wv[j] = __ldg(reinterpret_cast<const uint4*>(wh + (int64_t)r * kGD + n0) + c);
+    }
+#pragma unroll
+    for (int j = 0; j < kGD * 4 / 128; ++j) {
+      const int i = tid + j * 128, r = i >> 2, c = i & 3;
+      *reinterpret_cast<uint4*>(ws + r * (kQ + 8) + c * 8) = wv[j];
+    }
   }
   __syncthreads();
   if (r0 >= rows) return;
@@ -233,10 +242,22 @@ __global__ void __launch_bounds__(kMThreads) merge_project_kernel(const DecodeAr
   const int h = blockIdx.y, b0 = blockIdx.x * kMRows;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const __nv_bfloat16* wh = wts + (int64_t)h * kGD * kGD;
-  for (int i = tid; i < kGD * 16; i += kMThreads) {
-    const int r = i >> 4, c = i & 15;
-    *reinterpret_cast<uint4*>(ws + r * kGRow + c * 8) =
-        __ldg(reinterpret_cast<const uint4*>(wh + (int64_t)r * kGD) + c);
+  {
+    // all eight of a thread's 16-byte pieces are requested before any is
+    // stored: a CTA that starts only when the attention's last CTAs leave
+    // its SM stages W_V in one memory latency, not eight
+    constexpr int kPer = kGD * 16 / kMThreads;
+    uint4 wv[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int i = tid + j * kMThreads, r = i >> 4, c = i & 15;
+      wv[j] = __ldg(reinterpret_cast<const uint4*>(wh + (int64_t)r * kGD) + c);
+    }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int i = tid + j * kMThreads, r = i >> 4, c = i & 15;
+      *reinterpret_cast<uint4*>(ws + r * kGRow + c * 8) = wv[j];
+    }
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // ---- z rows 2w, 2w + 1
