@@ -163,6 +163,27 @@ def _check(fn: str, status: int):
         raise PagedKVError(fn, status, load().pkv_status_str(status).decode())
 
 
+# debug mode: host-side checks of the index arrays before each call
+_debug = os.environ.get("PKV_DEBUG", "") not in ("", "0")
+
+
+def set_debug(flag: bool) -> None:
+    """Turn the host-side index checks (``validate.py``) on or off."""
+    global _debug
+    _debug = bool(flag)
+
+
+def _validate(fn: str, check: str, *args, **kw) -> None:
+    """In debug mode, run validate.<check>(*args, **kw) before the call."""
+    if not _debug:
+        return
+    from . import validate as V
+    try:
+        getattr(V, check)(*args, **kw)
+    except V.ValidationError as e:
+        raise PagedKVError(fn, V.PKV_EINVAL, str(e)) from None
+
+
 def status_str(status: int) -> str:
     return load().pkv_status_str(status).decode()
 
@@ -189,6 +210,7 @@ def set_span_buffer(buf=None) -> None:
 def kv_append(k_new, v_new, k_cache, v_cache, slot_mapping, stream=None) -> None:
     """k_new, v_new [T, Hkv, D]; pools [NB, Hkv, bs, D]; slot_mapping [T] int64."""
     nb, hkv, bs, d = k_cache.shape
+    _validate("pkv_kv_append", "check_slots", slot_mapping, nb, bs)
     st = load().pkv_kv_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
                               _ptr(slot_mapping), int(slot_mapping.shape[0]), nb, hkv, d, bs,
                               _dtype_code(k_cache), _stream(stream))
@@ -211,6 +233,8 @@ def paged_decode_attention(out, q, k_cache, v_cache, block_table, seq_lens, max_
     int32; seq_lens [B] int32 (after the append); max_seq_len >= max(seq_lens)."""
     b, hq, d = q.shape
     nb, hkv, bs, _ = k_cache.shape
+    _validate("pkv_paged_decode_attention", "check_decode", block_table, seq_lens,
+              max_seq_len, nb, bs)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = load().pkv_paged_decode_attention(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
@@ -226,6 +250,8 @@ def paged_decode_attention_append(out, q, k_new, v_new, k_cache, v_cache, block_
     position seq_lens[b] - 1 and attend, in one launch."""
     b, hq, d = q.shape
     nb, hkv, bs, _ = k_cache.shape
+    _validate("pkv_paged_decode_attention_append", "check_decode", block_table,
+              seq_lens, max_seq_len, nb, bs, appends=True)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = load().pkv_paged_decode_attention_append(
         _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
@@ -239,6 +265,7 @@ def kv_append_fp8(k_new, v_new, k_cache, v_cache, k_scale, v_scale, slot_mapping
     """bf16 k_new, v_new [T, Hkv, D] -> E4M3 codes of x / scale[h] in uint8
     pools [NB, Hkv, bs, D]; k_scale, v_scale float32 [Hkv] on the device."""
     nb, hkv, bs, d = k_cache.shape
+    _validate("pkv_kv_append_fp8", "check_slots", slot_mapping, nb, bs)
     st = load().pkv_kv_append_fp8(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
                                   _ptr(k_scale), _ptr(v_scale), _ptr(slot_mapping),
                                   int(slot_mapping.shape[0]), nb, hkv, d, bs, _stream(stream))
@@ -250,6 +277,8 @@ def paged_decode_attention_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block
     """Decode over uint8 E4M3 pools; q/out bf16 [B, Hq, D]."""
     b, hq, d = q.shape
     nb, hkv, bs, _ = k_cache.shape
+    _validate("pkv_paged_decode_attention_fp8", "check_decode", block_table, seq_lens,
+              max_seq_len, nb, bs)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = load().pkv_paged_decode_attention_fp8(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
@@ -261,6 +290,7 @@ def paged_decode_attention_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block
 def latent_append(c_new, c_cache, slot_mapping, stream=None) -> None:
     """bf16 c_new [T, r] -> latent pool [NB, bs, r] at slot_mapping (int64)."""
     nb, bs, r = c_cache.shape
+    _validate("pkv_latent_append", "check_slots", slot_mapping, nb, bs)
     st = load().pkv_latent_append(_ptr(c_new), _ptr(c_cache), _ptr(slot_mapping),
                                   int(slot_mapping.shape[0]), nb, r, bs, _stream(stream))
     _check("pkv_latent_append", st)
@@ -278,6 +308,8 @@ def mla_decode_attention(out, q, w_k, w_v, c_cache, block_table, seq_lens, max_s
     first placed at position seq_lens[b] - 1 (the same call)."""
     b, hq, d = q.shape
     nb, bs, r = c_cache.shape
+    _validate("pkv_mla_decode_attention", "check_decode", block_table, seq_lens,
+              max_seq_len, nb, bs, appends=c_new is not None)
     if workspace is None:
         workspace = mla_workspace(b, hq, r, max_seq_len, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size()
@@ -303,6 +335,8 @@ def paged_decode_attention_noalloc(out, q, k_cache, v_cache, block_table, seq_le
     allocate device memory."""
     b, hq, d = q.shape
     nb, hkv, bs, _ = k_cache.shape
+    _validate("pkv_paged_decode_attention_noalloc", "check_decode", block_table,
+              seq_lens, max_seq_len, nb, bs)
     st = load().pkv_paged_decode_attention_noalloc(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
         b, int(block_table.shape[1]), int(max_seq_len), nb, hq, hkv, d, bs, float(scale),
@@ -316,6 +350,8 @@ def chunked_prefill_attention(out, q, k_cache, v_cache, block_table_row, prior_l
     positions prior_len .. prior_len+C-1 and its K/V are already appended."""
     c, hq, d = q.shape
     nb, hkv, bs, _ = k_cache.shape
+    _validate("pkv_chunked_prefill_attention", "check_prefill", block_table_row,
+              prior_len, c, nb, bs)
     st = load().pkv_chunked_prefill_attention(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table_row),
         int(block_table_row.shape[0]), int(prior_len), c, nb, hq, hkv, d, bs, float(scale),
@@ -335,6 +371,12 @@ def decode_prefill_attention(dec_out, dec_q, k_new, v_new, k_cache, v_cache, blo
     the call first appends the chunk's own keys and values (as kv_append)."""
     b, hq, d = dec_q.shape
     nb, hkv, bs, _ = k_cache.shape
+    _validate("pkv_decode_prefill_attention", "check_decode", block_table, seq_lens,
+              max_seq_len, nb, bs, appends=True)
+    _validate("pkv_decode_prefill_attention", "check_prefill", pre_block_table_row,
+              prior_len, int(pre_q.shape[0]), nb, bs)
+    if chunk_slots is not None:
+        _validate("pkv_decode_prefill_attention", "check_slots", chunk_slots, nb, bs)
     a = DecodePrefillArgs()
     a.decode_out, a.decode_q = _ptr(dec_out), _ptr(dec_q)
     a.k_new, a.v_new = _ptr(k_new), _ptr(v_new)

@@ -35,7 +35,7 @@ def _rank_main(rank, port, out):
 
 def test_barrier_and_max_over_ranks_world_size_2():
     port = _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         out = mgr.dict()
         mp.spawn(_rank_main, args=(port, out), nprocs=2, join=True)
         res = dict(out)
