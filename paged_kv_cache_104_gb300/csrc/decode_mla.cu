@@ -156,6 +156,12 @@ __device__ __forceinline__ void tma4d(uint32_t dst, const CUtensorMap* map, uint
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(0), "r"(w), "l"(policy)
       : "memory");
 }
+// Bring one 4 KiB block of the pool into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma4d_prefetch_l2(const CUtensorMap* map, int w) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %1, %1, %2}];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(w)
+               : "memory");
+}
 __device__ __forceinline__ void tma2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x,
                                       int y) {
   asm volatile(
@@ -354,10 +360,20 @@ decode_mla_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_c,
     // q~ comes from the kernel before this one in the stream (launched as its
     // programmatic dependent, this grid may start before that one has
     // finished), and so may the latent of each sequence's new token (the
-    // query absorption can append it).  Nothing is requested before that
-    // grid is done: latent tiles requested earlier also competed in HBM with
-    // its loads and delayed it (measured: 53.6 -> 51.7 us per layer on the
-    // ragged batch, 26.7 -> 26.0 us on the 2,301-token batch).
+    // query absorption can append it).  Nothing is requested into shared
+    // memory before that grid is done: latent tiles requested earlier
+    // competed in HBM with its loads and delayed it (measured: 53.6 -> 51.7
+    // us per layer on the ragged batch, 26.7 -> 26.0 us on the 2,301-token
+    // batch).  Only the first tile of the first piece is prefetched into L2
+    // (32 KiB per CTA; a later copy reads L2, which also holds the appended
+    // latent once that grid is done): 23.0 -> 22.6 us per layer on the
+    // 2,301-token batch, the ragged batch unchanged; two tiles were no
+    // faster.
+    if (have) {
+      const int nblk0 = (u.tok_end - 1) / kBlockSize - u.tok_begin / kBlockSize + 1;
+      if (lane < min(nblk0, kBlkPerTile) && ids >= 0 && (int64_t)ids < a.num_blocks)
+        tma4d_prefetch_l2(&tm_c, 2 * ids);
+    }
     if (lane == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
     __syncwarp();
     while (ok && have) {
