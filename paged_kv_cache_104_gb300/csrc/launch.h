@@ -79,12 +79,12 @@ struct DecodeArgs {
   // alone; beside a prefill, whose re-read K/V lives in L2, plain stores
   // measured faster.
   int keep_partials;
-  // 1: the balanced walk of the bf16, fp8 and latent decodes (set by their launchers
-  // when ws_np is given and the decode runs alone): the KV-head stages of all
-  // sequences are cut into equal shares,
-  // one per CTA, and the main kernel records in ws_np how many partials each
-  // (sequence, KV head) left for the merge; 0: 512-token splits, the merge
-  // derives their count from seq_lens.
+  // 1: the balanced walk of the bf16, fp8 and latent decodes (set by their
+  // launchers when ws_np is given and the decode runs alone, or, for the bf16
+  // decode with grouped stages, also beside a prefill): the stages of all
+  // sequences are cut into equal shares, one per CTA, and the main kernel
+  // records in ws_np how many partials each (sequence, KV head) left for the
+  // merge; 0: 512-token splits, the merge derives their count from seq_lens.
   int balanced;
   // 1: the kernel keeps every sequence's length in shared memory after its
   // unit prefix sums (set by a launcher that sized shared memory for it)
