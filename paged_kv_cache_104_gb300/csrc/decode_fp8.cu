@@ -128,7 +128,7 @@ __device__ __forceinline__ uint4 lds128(const unsigned char* p) {
   return *reinterpret_cast<const uint4*>(p);
 }
 
-template <int G>
+template <int G, bool HS>
 __global__ void __launch_bounds__(kThreads8, G <= 8 ? 3 : 2)
 decode_fp8_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v) {
@@ -153,17 +153,22 @@ decode_fp8_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
     *abort_flag = 0;
     fence_mbar_init();
   }
-  // balanced walk over 64-token stages when the batch gives every CTA at
-  // least kMinStagesPerCta of them; otherwise 512-token splits
+  // The walk's streams: (sequence, group of kBPS KV heads) with one
+  // 16-token block per stage (HS), or (sequence, KV head) with kBPS blocks
+  // per stage.  Balanced walk when the batch gives every CTA at least 512
+  // tokens of stages; otherwise 512-token splits.
+  DecodeArgs aw = a;
+  if (HS) aw.num_kv_heads = a.num_kv_heads / kBPS;
+  constexpr int kWalkTok = HS ? kBlockSize : kStageTok;
   // the sequence lengths after the prefix sums, when the launcher made room
   int* lens = a.lens_in_smem ? cu + a.num_seqs + 1 : nullptr;
-  plan_units(a, cu, a.balanced ? kStageTok : 0, 0, lens);
+  plan_units(aw, cu, a.balanced ? kWalkTok : 0, 0, lens);
   __syncthreads();
   const bool balanced =
-      a.balanced && (int64_t)cu[a.num_seqs] >= (int64_t)kMinStagesPerCta * gridDim.x;
+      a.balanced && (int64_t)cu[a.num_seqs] >= (int64_t)(kSplitTokens / kWalkTok) * gridDim.x;
   if (a.balanced && !balanced) {
     __syncthreads();
-    plan_units(a, cu, 0, 0, lens);
+    plan_units(aw, cu, 0, 0, lens);
     __syncthreads();
   }
   volatile int* vabort = abort_flag;
@@ -177,17 +182,18 @@ decode_fp8_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
     const uint64_t policy = policy_evict_first();
     uint32_t issued = 0;
     bool ok = true;
-    Walk wk = walk_begin(a, cu, balanced, lens);
+    Walk wk = walk_begin(aw, cu, balanced, lens);
     Unit u;
-    while (ok && walk_next(a, cu, kStageTok, wk, u)) {
+    while (ok && walk_next(aw, cu, kWalkTok, wk, u)) {
       const int blk0 = u.tok_begin / kBlockSize;
       const int nblk = (u.tok_end - 1) / kBlockSize - blk0 + 1;
       const int32_t* bt_row = a.block_table + (int64_t)u.b * a.bt_stride + blk0;
       int my_blk = 0;
-      const int nst = (nblk + kBPS - 1) / kBPS;
+      const int nst = HS ? nblk : (nblk + kBPS - 1) / kBPS;
       for (int st = 0; st < nst; ++st, ++issued) {
-        if ((st * kBPS) % 32 == 0) {  // next window of 32 block ids, one per lane
-          const int idx = st * kBPS + lane;
+        const int bps = HS ? 1 : kBPS;   // blocks per stage
+        if ((st * bps) % 32 == 0) {  // next window of 32 block ids, one per lane
+          const int idx = st * bps + lane;
           my_blk = 0;
           if (idx < nblk) {
             my_blk = __ldg(bt_row + idx);
@@ -204,12 +210,16 @@ decode_fp8_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
         }
         __syncwarp();
         if (*vabort) { ok = false; break; }
-        const int nb = min(kBPS, nblk - st * kBPS);
+        // tile i of the stage: HS, head u.g * kBPS + i of the stage's block;
+        // otherwise block st * kBPS + i of head u.g
+        const int nb = HS ? kBPS : min(kBPS, nblk - st * kBPS);
         int rows[kBPS];
 #pragma unroll
         for (int i = 0; i < kBPS; ++i)
-          rows[i] = (__shfl_sync(kAll8, my_blk, (st * kBPS + i) & 31) * a.num_kv_heads + u.g) *
-                    kBlockSize;
+          rows[i] = HS ? (__shfl_sync(kAll8, my_blk, st & 31) * a.num_kv_heads + u.g * kBPS + i) *
+                             kBlockSize
+                       : (__shfl_sync(kAll8, my_blk, (st * kBPS + i) & 31) * a.num_kv_heads + u.g) *
+                             kBlockSize;
         if (lane == 0) {
           const uint32_t fb = full0 + 8 * buf;
           mbar_arrive_expect_tx(fb, (uint32_t)(nb * 2 * kTile8));
@@ -239,14 +249,16 @@ decode_fp8_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
   __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(a.out);
   uint32_t consumed = 0;
 
-  Walk wk = walk_begin(a, cu, balanced, lens);
+  Walk wk = walk_begin(aw, cu, balanced, lens);
   Unit u;
-  while (walk_next(a, cu, kStageTok, wk, u)) {
-    const int hq0 = u.g * G;
+  while (walk_next(aw, cu, kWalkTok, wk, u)) {
+    const int head = HS ? u.g * kBPS + warp : u.g;   // this warp's KV head
+    const int hq0 = head * G;
     // the merge reads how many partials this (sequence, KV head) left
-    if (a.balanced && u.s == 0 && tid == 0) a.ws_np[u.b * a.num_kv_heads + u.g] = u.ns;
-    const float sl2 = a.scale * __ldg(a.k_scale + u.g) * 1.4426950408889634f;
-    const float vscale = __ldg(a.v_scale + u.g);
+    if (a.balanced && u.s == 0 && (HS ? lane == 0 : tid == 0))
+      a.ws_np[u.b * a.num_kv_heads + head] = u.ns;
+    const float sl2 = a.scale * __ldg(a.k_scale + head) * 1.4426950408889634f;
+    const float vscale = __ldg(a.v_scale + head);
     // Q^T fragments: head 8nt + g, dims 32t + 4ks + {0,1} (b0) and {2,3} (b1)
     uint32_t qf[NT][8][2];
 #pragma unroll
@@ -282,14 +294,14 @@ decode_fp8_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
     }
 
     const int nblk = (u.tok_end - 1) / kBlockSize - u.tok_begin / kBlockSize + 1;
-    const int nst = (nblk + kBPS - 1) / kBPS;
+    const int nst = HS ? nblk : (nblk + kBPS - 1) / kBPS;
     for (int st = 0; st < nst; ++st, ++consumed) {
       const int buf = consumed % kNST8;
       const uint32_t phase = (consumed / kNST8) & 1;
       if (!*vabort) {
         if (!mbar_wait(full0 + 8 * buf, phase, a.err)) *vabort = 1;
       }
-      const int tok0 = u.tok_begin + (st * kBPS + warp) * kBlockSize;
+      const int tok0 = u.tok_begin + (HS ? st : st * kBPS + warp) * kBlockSize;
       const int valid = min(kBlockSize, u.tok_end - tok0);
       uint4 kg0, kg1, kh0, kh1, va, vb, vc, vd;
       if (valid > 0) {
@@ -420,7 +432,7 @@ decode_fp8_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
       }
     }
 
-    // ---- merge the four warps of this unit; V's scale applies here
+    // ---- l summed over the lanes of each head
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -429,67 +441,102 @@ decode_fp8_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
         l_run[nt][j] += __shfl_xor_sync(kAll8, l_run[nt][j], 8);
         l_run[nt][j] += __shfl_xor_sync(kAll8, l_run[nt][j], 16);
       }
+    const bool direct = (u.ns == 1);
+    if constexpr (HS) {
+      // this warp saw every key of the unit for its own heads: O / l (V's
+      // scale applied) goes out straight from the accumulators, dims
+      // 16g + 2mt and the next one per lane and tile
+      __half* ws_half = reinterpret_cast<__half*>(a.ws_acc);
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int hh = 8 * nt + 2 * t + j;
-        if (hh < G) {
-          if (g == 0) {
-            comb_ml[(warp * G + hh) * 2 + 0] = m_run[nt][j];
-            comb_ml[(warp * G + hh) * 2 + 1] = l_run[nt][j];
+        for (int j = 0; j < 2; ++j) {
+          const int hh = 8 * nt + 2 * t + j;
+          if (hh < G) {
+            const float rl = vscale / l_run[nt][j];
+            const int64_t row = (int64_t)u.b * a.num_q_heads + hq0 + hh;
+            const int64_t pidx = row * a.max_splits + u.s;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+              const int d = 16 * g + 2 * mt;
+              const float x0 = o[nt][mt][j] * rl, x1 = o[nt][mt][j + 2] * rl;
+              if (direct)
+                *reinterpret_cast<__nv_bfloat162*>(outp + row * kHD + d) = __floats2bfloat162_rn(x0, x1);
+              else
+                *reinterpret_cast<__half2*>(ws_half + pidx * kHD + d) = __floats2half2_rn(x0, x1);
+            }
+            if (!direct && g == 0) {
+              a.ws_ml[pidx * 2 + 0] = m_run[nt][j];
+              a.ws_ml[pidx * 2 + 1] = l_run[nt][j];
+            }
           }
-          float* crow = comb + (warp * G + hh) * kCombRow + 16 * g;
+        }
+    } else {
+      // ---- otherwise merge the four warps of this unit (each saw a quarter
+      // of its blocks); V's scale applies here
 #pragma unroll
-          for (int mt = 0; mt < 8; ++mt)   // pair slot mt stored at mt ^ g: no bank conflicts
-            *reinterpret_cast<float2*>(crow + 2 * (mt ^ g)) =
-                make_float2(o[nt][mt][j], o[nt][mt][j + 2]);
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int hh = 8 * nt + 2 * t + j;
+          if (hh < G) {
+            if (g == 0) {
+              comb_ml[(warp * G + hh) * 2 + 0] = m_run[nt][j];
+              comb_ml[(warp * G + hh) * 2 + 1] = l_run[nt][j];
+            }
+            float* crow = comb + (warp * G + hh) * kCombRow + 16 * g;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt)   // pair slot mt stored at mt ^ g: no bank conflicts
+              *reinterpret_cast<float2*>(crow + 2 * (mt ^ g)) =
+                  make_float2(o[nt][mt][j], o[nt][mt][j + 2]);
+          }
+        }
+      named_bar_sync(1, kConsumers8);
+      // warp w merges heads w, w + 4, ...: the combine weights once per head,
+      // then 4 dims per lane
+      for (int h = warp; h < G; h += kCW) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kCW; ++k) M = fmaxf(M, comb_ml[(k * G + h) * 2]);
+        float wk[kCW], L = 0.f;
+#pragma unroll
+        for (int k = 0; k < kCW; ++k) {
+          const float mk = comb_ml[(k * G + h) * 2];
+          wk[k] = (mk == -INFINITY) ? 0.f : ex2(mk - M);
+          L = fmaf(wk[k], comb_ml[(k * G + h) * 2 + 1], L);
+        }
+        const float rl = vscale / L;
+        const int64_t row = (int64_t)u.b * a.num_q_heads + hq0 + h;
+        const int64_t pidx = row * a.max_splits + u.s;
+#pragma unroll
+        for (int i = 0; i < kHD / 32; ++i) {
+          const int d = lane + 32 * i;
+          const int dp = (d & ~15) | ((((d & 15) >> 1) ^ (d >> 4)) << 1) | (d & 1);
+          float O = 0.f;
+#pragma unroll
+          for (int k = 0; k < kCW; ++k) O = fmaf(wk[k], comb[(k * G + h) * kCombRow + dp], O);
+          if (direct)
+            outp[row * kHD + d] = __float2bfloat16_rn(O * rl);
+          else
+            reinterpret_cast<__half*>(a.ws_acc)[pidx * kHD + d] = __float2half_rn(O * rl);
+        }
+        if (!direct && lane == 0) {
+          a.ws_ml[pidx * 2 + 0] = M;
+          a.ws_ml[pidx * 2 + 1] = L;
         }
       }
-    named_bar_sync(1, kConsumers8);
-    // warp w merges heads w, w + 4, ...: the combine weights once per head,
-    // then 4 dims per lane
-    const bool direct = (u.ns == 1);
-    for (int h = warp; h < G; h += kCW) {
-      float M = -INFINITY;
-#pragma unroll
-      for (int k = 0; k < kCW; ++k) M = fmaxf(M, comb_ml[(k * G + h) * 2]);
-      float wk[kCW], L = 0.f;
-#pragma unroll
-      for (int k = 0; k < kCW; ++k) {
-        const float mk = comb_ml[(k * G + h) * 2];
-        wk[k] = (mk == -INFINITY) ? 0.f : ex2(mk - M);
-        L = fmaf(wk[k], comb_ml[(k * G + h) * 2 + 1], L);
-      }
-      const float rl = vscale / L;
-      const int64_t row = (int64_t)u.b * a.num_q_heads + hq0 + h;
-      const int64_t pidx = row * a.max_splits + u.s;
-#pragma unroll
-      for (int i = 0; i < kHD / 32; ++i) {
-        const int d = lane + 32 * i;
-        const int dp = (d & ~15) | ((((d & 15) >> 1) ^ (d >> 4)) << 1) | (d & 1);
-        float O = 0.f;
-#pragma unroll
-        for (int k = 0; k < kCW; ++k) O = fmaf(wk[k], comb[(k * G + h) * kCombRow + dp], O);
-        if (direct)
-          outp[row * kHD + d] = __float2bfloat16_rn(O * rl);
-        else
-          reinterpret_cast<__half*>(a.ws_acc)[pidx * kHD + d] = __float2half_rn(O * rl);
-      }
-      if (!direct && lane == 0) {
-        a.ws_ml[pidx * 2 + 0] = M;
-        a.ws_ml[pidx * 2 + 1] = L;
-      }
+      named_bar_sync(1, kConsumers8);
     }
-    named_bar_sync(1, kConsumers8);
   }
 }
 
-template <int G>
+template <int G, bool HS>
 cudaError_t launch_fp8_g(const DecodeArgs& args, int num_sms, cudaStream_t stream) {
   using C = F8Cfg<G>;
   DecodeArgs a = args;
-  a.balanced = a.ws_np != nullptr && stage_plan_fits(a, kStageTok);
+  DecodeArgs aw = a;
+  if (HS) aw.num_kv_heads = a.num_kv_heads / kBPS;
+  a.balanced = a.ws_np != nullptr && stage_plan_fits(aw, HS ? kBlockSize : kStageTok);
   a.partials_f16 = 1;
   CUtensorMap tm_k, tm_v;
   const int64_t rows = a.num_blocks * a.num_kv_heads * kBlockSize;
@@ -504,13 +551,13 @@ cudaError_t launch_fp8_g(const DecodeArgs& args, int num_sms, cudaStream_t strea
     if (a.lens_in_smem) smem = with;
   }
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  cudaError_t e = allow_dynamic_smem(decode_fp8_kernel<G>, (int)smem);
+  cudaError_t e = allow_dynamic_smem(decode_fp8_kernel<G, HS>, (int)smem);
   if (e != cudaSuccess) return e;
   const int by_smem = (int)((228 * 1024) / (smem + 1024));
   const int per_sm = by_smem < 1 ? 1 : (by_smem > (G <= 8 ? 3 : 2) ? (G <= 8 ? 3 : 2) : by_smem);
   const int64_t upper = (int64_t)a.num_seqs * a.num_kv_heads * a.max_splits;
   const int grid = (int)(upper < (int64_t)num_sms * per_sm ? upper : (int64_t)num_sms * per_sm);
-  decode_fp8_kernel<G><<<grid, kThreads8, smem, stream>>>(a, tm_k, tm_v);
+  decode_fp8_kernel<G, HS><<<grid, kThreads8, smem, stream>>>(a, tm_k, tm_v);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.max_splits <= 1) return e;
   return launch_decode_reduce_bf16_128(a, stream);
@@ -521,12 +568,14 @@ cudaError_t launch_fp8_g(const DecodeArgs& args, int num_sms, cudaStream_t strea
 cudaError_t launch_paged_decode_fp8(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
   if (a.chunk_prior >= 0 || a.split_tokens % kStageTok != 0 || !a.k_scale || !a.v_scale)
     return cudaErrorInvalidValue;
+  // one block of kBPS KV heads per stage when the heads form such groups
+  const bool hs = a.num_kv_heads % kBPS == 0;
   switch (a.num_q_heads / a.num_kv_heads) {
-    case 1: return launch_fp8_g<1>(a, num_sms, stream);
-    case 2: return launch_fp8_g<2>(a, num_sms, stream);
-    case 4: return launch_fp8_g<4>(a, num_sms, stream);
-    case 8: return launch_fp8_g<8>(a, num_sms, stream);
-    case 16: return launch_fp8_g<16>(a, num_sms, stream);
+    case 1: return hs ? launch_fp8_g<1, true>(a, num_sms, stream) : launch_fp8_g<1, false>(a, num_sms, stream);
+    case 2: return hs ? launch_fp8_g<2, true>(a, num_sms, stream) : launch_fp8_g<2, false>(a, num_sms, stream);
+    case 4: return hs ? launch_fp8_g<4, true>(a, num_sms, stream) : launch_fp8_g<4, false>(a, num_sms, stream);
+    case 8: return hs ? launch_fp8_g<8, true>(a, num_sms, stream) : launch_fp8_g<8, false>(a, num_sms, stream);
+    case 16: return hs ? launch_fp8_g<16, true>(a, num_sms, stream) : launch_fp8_g<16, false>(a, num_sms, stream);
     default: return cudaErrorInvalidValue;
   }
 }
