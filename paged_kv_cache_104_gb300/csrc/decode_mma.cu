@@ -608,7 +608,12 @@ template <int G, bool FUSE, bool HS>
 cudaError_t launch_g(const DecodeArgs& args, int num_sms, cudaStream_t stream, bool dependent) {
   using C = MCfg<G>;
   DecodeArgs a = args;
-  a.keep_partials = dependent ? 0 : 1;
+  // Partials kept in L2 (evict-last, dropped by the merge once read), except
+  // for per-head stages beside a prefill: their 512-token splits leave some
+  // 12 MB of partials a layer, which crowded the prefill's L2-resident K/V
+  // (pair 490 -> 498 us).  The balanced walk's few partials do not (pair
+  // 470.6-471.3 -> 468.9-470.1 us at 43-44 prefill SMs).
+  a.keep_partials = (dependent && !HS) ? 0 : 1;
   a.partials_f16 = 1;
   // The balanced walk, except for the per-head stages beside a prefill,
   // where 512-token splits measured faster.  With a group of kBPS heads per

@@ -75,9 +75,9 @@ struct DecodeArgs {
   const float* v_scale;
   // 1: the main kernel stores split partials with an L2 evict-last hint and
   // the merge drops each partial line from L2 once read (no write-back);
-  // 0: plain stores.  Set by the bf16 decode launcher when the decode runs
-  // alone; beside a prefill, whose re-read K/V lives in L2, plain stores
-  // measured faster.
+  // 0: plain stores.  Set by the bf16 decode launcher, except for per-head
+  // stages beside a prefill, whose re-read K/V lives in L2: there the many
+  // partials of 512-token splits made plain stores faster.
   int keep_partials;
   // 1: the balanced walk of the bf16, fp8 and latent decodes (set by their
   // launchers when ws_np is given and the decode runs alone, or, for the bf16
