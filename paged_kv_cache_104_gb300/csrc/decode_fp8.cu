@@ -8,14 +8,18 @@
 // bottleneck" mentions (section "What the profile said"; the pages give no
 // format).  The cache is half the bytes of bf16, and decode is HBM-bound.
 //
-// Same unit structure as the bf16 kernel -- persistent CTAs walking (sequence,
-// KV head) streams in equal per-CTA shares of 64-token stages, or in 512-token
-// splits for small batches, one producer warp streaming each block's K
-// and V tiles with 2-D TMA (one 16-row x 128-byte box each, 128-byte swizzle)
-// into a 4-stage ring, four consumer warps taking one block per stage -- but
-// the products are turned around: keys are the M side of the m16n8k16 tile
-// and the G query heads its N side (8 columns, or 16 for G = 16), so one
-// block costs 8 + 8 products instead of 16 + 16 with heads padded to 16 rows.
+// Same unit structure as the bf16 kernel -- persistent CTAs walking streams
+// in equal per-CTA shares of stages, or in 512-token splits for small
+// batches; a stage is one 16-token block of a group of four KV heads when the
+// heads form such groups (each consumer warp following one head through the
+// unit and writing its own result), otherwise four blocks of one KV head
+// (merged across the warps at each unit's end); one producer warp streams
+// each (block, head) tile of K and V with 2-D TMA (one 16-row x 128-byte box
+// each, 128-byte swizzle) into a 4-stage ring, four consumer warps taking one
+// tile per stage -- but the products are turned around: keys are the M side
+// of the m16n8k16 tile and the G query heads its N side (8 columns, or 16 for
+// G = 16), so one block costs 8 + 8 products instead of 16 + 16 with heads
+// padded to 16 rows.
 //   S^T = K . Q^T   A = K (16 keys x 16 dims), B = Q^T
 //   O^T = V^T . P^T A = V^T (16 dims x 16 keys), B = P^T
 // Each lane reads its share of the fp8 codes straight from the ring into
@@ -128,6 +132,10 @@ __device__ __forceinline__ uint4 lds128(const unsigned char* p) {
   return *reinterpret_cast<const uint4*>(p);
 }
 
+// G: query heads per KV head.  HS (grouped stages): a stage is one block of a
+// group of kBPS KV heads, warp w following head w with that head's scales;
+// otherwise kBPS blocks of one KV head, merged across the warps at each
+// unit's end.
 template <int G, bool HS>
 __global__ void __launch_bounds__(kThreads8, G <= 8 ? 3 : 2)
 decode_fp8_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,

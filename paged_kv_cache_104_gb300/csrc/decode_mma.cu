@@ -158,6 +158,10 @@ __device__ __forceinline__ void st_global_hint_f16x2(__half* dst, float lo, floa
                : "memory");
 }
 
+// G: query heads per KV head.  FUSE: each sequence's new key and value are
+// appended in the same launch.  HS (grouped stages): a stage is one block of
+// a group of kBPS KV heads, warp w following head w; otherwise kBPS blocks of
+// one KV head, merged across the warps at each unit's end.
 template <int G, bool FUSE, bool HS>
 __global__ void __launch_bounds__(kThreadsM, G <= 8 ? 3 : 2)
 decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
