@@ -111,6 +111,17 @@ def test_side_by_side_group_of_one(hq, hkv):
     assert torch.equal(_bits(sd), _bits(bd)) and torch.equal(_bits(sp), _bits(bp))
 
 
+def test_side_by_side_per_head_stages():
+    """Two KV heads, too few for a group of four: beside the prefill the
+    decode keeps one head per stage and 512-token splits; still equal to the
+    serial calls."""
+    w = G.custom_workload(torch.bfloat16, 16, 2, 128, seed=95)
+    lay = W.make_layout(w, seq_lens_after=[5, 700, 1300], prefill=(130, 250))
+    x = W.draw_layer(w, lay, 0)
+    (sd, sp, bd, bp), _ = _run_both(w, lay, x, 130, 16)
+    assert torch.equal(_bits(sd), _bits(bd)) and torch.equal(_bits(sp), _bits(bp))
+
+
 def test_side_by_side_too_many_work_items_runs_serial():
     """514 work items (257 query tiles x 2 head pairs) exceed the persistent
     list: serial, same results."""
