@@ -118,10 +118,9 @@ struct Walk {
   int64_t end;
 };
 
-// The balanced walk needs a workspace for the piece counts and at least
-// kMinStagesPerCta stages per CTA (so no stream is cut into more pieces than
-// the workspace has partial slots); otherwise the split walk.
-constexpr int kMinStagesPerCta = kSplitTokens / 64;
+// The balanced walk needs a workspace for the piece counts and shares of at
+// least kSplitTokens tokens of stages per CTA (so no stream is cut into more
+// pieces than the workspace has partial slots); otherwise the split walk.
 
 // True if the stage prefix sums of this call fit an int: every counted
 // sequence has at most max_seq_len tokens (longer ones are rejected).
