@@ -85,3 +85,102 @@ def test_debug_mode_raises_before_the_library(monkeypatch):
         assert e.value.status == 1
     finally:
         B.set_debug(False)
+
+
+def _small():
+    """4 blocks of 16 rows, 2 KV heads, head_dim 8, 4 query heads (CPU)."""
+    nb, hkv, bs, d, hq = 4, 2, 16, 8, 4
+    bf = torch.bfloat16
+    t = dict(
+        kc=torch.zeros(nb, hkv, bs, d, dtype=bf), vc=torch.zeros(nb, hkv, bs, d, dtype=bf),
+        kc8=torch.zeros(nb, hkv, bs, d, dtype=torch.uint8),
+        vc8=torch.zeros(nb, hkv, bs, d, dtype=torch.uint8),
+        sc=torch.ones(hkv), k_new=torch.zeros(2, hkv, d, dtype=bf),
+        v_new=torch.zeros(2, hkv, d, dtype=bf), q=torch.zeros(2, hq, d, dtype=bf),
+        out=torch.zeros(2, hq, d, dtype=bf),
+        bt=torch.tensor([[0, 1], [2, 3]], dtype=torch.int32),
+        lens=torch.tensor([5, 20], dtype=torch.int32),
+        c_cache=torch.zeros(nb, bs, d, dtype=bf), c_new=torch.zeros(2, d, dtype=bf),
+        w=torch.zeros(hq, d, d, dtype=bf))
+    return t
+
+
+def _calls():
+    """(name, call, message) with one bad entry each."""
+    i32 = lambda v: torch.tensor(v, dtype=torch.int32)
+    i64 = lambda v: torch.tensor(v, dtype=torch.int64)
+    same_row = i32([[0, 1], [0, 1]]), i32([17, 17])   # both new tokens at block 1, row 0
+    return [
+        ("kv_append_fp8", lambda t: B.kv_append_fp8(t["k_new"], t["v_new"], t["kc8"], t["vc8"],
+                                                     t["sc"], t["sc"], i64([3, 3])), "more than once"),
+        ("latent_append", lambda t: B.latent_append(t["c_new"], t["c_cache"], i64([0, 64])),
+         "outside the pool"),
+        ("paged_decode_attention_fp8",
+         lambda t: B.paged_decode_attention_fp8(t["out"], t["q"], t["kc8"], t["vc8"], t["sc"],
+                                                t["sc"], i32([[0, 1], [2, 9]]), t["lens"], 32, 1.0),
+         "block_table"),
+        ("mla_decode_attention (appending)",
+         lambda t: B.mla_decode_attention(t["out"], t["q"], t["w"], t["w"], t["c_cache"],
+                                          same_row[0], same_row[1], 32, 1.0, c_new=t["c_new"]),
+         "more than once"),
+        ("paged_decode_attention_noalloc",
+         lambda t: B.paged_decode_attention_noalloc(t["out"], t["q"], t["kc"], t["vc"], t["bt"],
+                                                    i32([5, 40]), 32, 1.0), "seq_lens"),
+        ("paged_decode_attention_append",
+         lambda t: B.paged_decode_attention_append(t["out"], t["q"], t["k_new"], t["v_new"], t["kc"],
+                                                   t["vc"], same_row[0], same_row[1], 32, 1.0),
+         "more than once"),
+        ("chunked_prefill_attention",
+         lambda t: B.chunked_prefill_attention(torch.zeros(20, 4, 8, dtype=torch.bfloat16),
+                                               torch.zeros(20, 4, 8, dtype=torch.bfloat16),
+                                               t["kc"], t["vc"], i32([0]), 0, 1.0), "need"),
+        ("decode_prefill_attention (chunk slots)",
+         lambda t: B.decode_prefill_attention(
+             t["out"], t["q"], t["k_new"], t["v_new"], t["kc"], t["vc"], t["bt"], t["lens"], 32,
+             torch.zeros(2, 4, 8, dtype=torch.bfloat16), torch.zeros(2, 4, 8, dtype=torch.bfloat16),
+             i32([3]), 0, 1.0, chunk_k_new=t["k_new"], chunk_v_new=t["v_new"],
+             chunk_slots=i64([0, 99])), "outside the pool"),
+    ]
+
+
+@pytest.mark.parametrize("case", range(len(_calls())), ids=[c[0] for c in _calls()])
+def test_debug_mode_covers_every_wrapper(case, monkeypatch):
+    """Each wrapper runs its host checks in debug mode and raises PKV_EINVAL
+    for a bad entry without reaching the library."""
+    name, call, match = _calls()[case]
+    def no_library():
+        raise AssertionError("the library was reached")
+    monkeypatch.setattr(B, "load", no_library)
+    B.set_debug(True)
+    try:
+        with pytest.raises(B.PagedKVError, match=match) as e:
+            call(_small())
+        assert e.value.status == 1
+    finally:
+        B.set_debug(False)
+
+
+def test_debug_mode_lets_good_calls_through(monkeypatch):
+    """Valid index arrays pass the host checks: the call goes on to the
+    library (stubbed here to stop it)."""
+    class Reached(Exception):
+        pass
+    def stub():
+        raise Reached
+    monkeypatch.setattr(B, "load", stub)
+    t = _small()
+    B.set_debug(True)
+    try:
+        with pytest.raises(Reached):
+            B.paged_decode_attention_append(t["out"], t["q"], t["k_new"], t["v_new"], t["kc"],
+                                            t["vc"], t["bt"], t["lens"], 32, 1.0)
+        with pytest.raises(Reached):
+            B.kv_append_fp8(t["k_new"], t["v_new"], t["kc8"], t["vc8"], t["sc"], t["sc"],
+                            torch.tensor([3, 20], dtype=torch.int64))
+        with pytest.raises(Reached):
+            B.chunked_prefill_attention(torch.zeros(20, 4, 8, dtype=torch.bfloat16),
+                                        torch.zeros(20, 4, 8, dtype=torch.bfloat16),
+                                        t["kc"], t["vc"], torch.tensor([0, 1], dtype=torch.int32),
+                                        0, 1.0)
+    finally:
+        B.set_debug(False)
