@@ -73,19 +73,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking probe: has the phase with the given parity completed?
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Wait for the phase with the given parity to complete, for at most about
 // one second.  Returns false (and records DEVERR_TIMEOUT) on time-out.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err) {
@@ -99,17 +86,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* er
   return false;
 }
 
-// 1-D bulk copy global -> shared, completing on an mbarrier (TMA engine).
-// dst, src 16-byte aligned; bytes a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-// Same, with an L2 eviction-priority hint (createpolicy result).
+// 1-D bulk copy global -> shared, completing on an mbarrier (TMA engine), with
+// an L2 eviction-priority hint (createpolicy result).  dst, src 16-byte
+// aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes,
                                               uint32_t bar, uint64_t policy) {
   asm volatile(
@@ -136,12 +115,7 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
-// fp32 store carrying an L2 eviction-priority hint.
-__device__ __forceinline__ void st_global_hint(float* dst, float v, uint64_t policy) {
-  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(dst), "f"(v), "l"(policy)
-               : "memory");
-}
-
+// fp16 store carrying an L2 eviction-priority hint.
 __device__ __forceinline__ void st_global_hint_f16(__half* dst, __half v, uint64_t policy) {
   asm volatile("st.global.L2::cache_hint.b16 [%0], %1, %2;" ::"l"(dst),
                "h"(__half_as_ushort(v)), "l"(policy)
