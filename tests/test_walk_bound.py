@@ -57,3 +57,30 @@ def test_split_walk_units_fit_the_partial_slots():
         units = [(s, min(n, s + SPLIT)) for s in range(0, n, SPLIT)]
         assert len(units) == -(-n // SPLIT)
         assert units[-1][1] == n and all(e - b <= SPLIT for b, e in units)
+
+
+def test_latent_walk_with_padding_fits_the_partial_slots():
+    """The latent decode's walk: 128-token stages, four empty stages counted
+    after each sequence's real ones, shares of at least four stages.  The
+    padding follows the real stages, so the real ones still fall to at most
+    ceil(n / 512) + 1 CTAs."""
+    rng = random.Random(77)
+    stage, pad, min_stages = 128, 4, SPLIT // 128
+    checked = 0
+    for _ in range(300):
+        lens = [max(1, int(rng.expovariate(1 / rng.choice([300, 3000, 12000]))))
+                for _ in range(rng.randint(1, 160))]
+        ctas = rng.choice([148, 152, rng.randint(1, 400)])
+        streams, pos = [], 0
+        for n in lens:
+            real = -(-n // stage)
+            streams.append((pos, real, n))
+            pos += real + pad
+        if pos < min_stages * ctas:
+            continue
+        sh = shares(pos, ctas)
+        for first, real, n in streams:
+            pieces = sum(1 for b, e in sh if b < first + real and e > first)
+            assert pieces <= -(-n // SPLIT) + 1, (n, pieces)
+        checked += 1
+    assert checked > 50
